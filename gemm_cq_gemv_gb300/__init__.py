@@ -1,0 +1,15 @@
+"""GB300 (sm_103a) low-bit GEMV / GEMM: CQ-WxA8 and Q4_0.
+
+The compute lives in ``libcqgemv.so`` (hand-written CUDA, C ABI in
+``include/cqgemv.h``); this package is a thin ctypes binding with the same function
+names plus the seeded input generators in ``synth``.  Loading is lazy; the first call
+raises if the shared library has not been built.
+"""
+
+from ._binding import (CQError, LIB_PATH, SIGNATURES, a8_quantize, cq_abi_version,
+                       cq_codebook, cq_codebook_fit, cq_encode, cq_gemv, cq_gemv_workspace_bytes,
+                       cq_status_string, lib, make_codebook, q4_0_gemv, q4_0_quantize)
+
+__all__ = ["CQError", "LIB_PATH", "SIGNATURES", "a8_quantize", "cq_abi_version", "cq_codebook",
+           "cq_codebook_fit", "cq_encode", "cq_gemv", "cq_gemv_workspace_bytes",
+           "cq_status_string", "lib", "make_codebook", "q4_0_gemv", "q4_0_quantize"]

@@ -1,0 +1,206 @@
+"""ctypes binding of ``libcqgemv.so`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (``include/cqgemv.h``),
+takes CUDA tensors, checks dtype / device / contiguity / shape, passes raw device
+pointers and sizes across the C ABI and raises ``CQError`` on a non-OK status.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback of any kind: if
+the shared library is missing or does not load, every call raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcqgemv.so")
+
+CQ_OK = 0
+_STATUS = {0: "CQ_OK", 1: "CQ_ERR_INVALID_ARG", 2: "CQ_ERR_ALIGNMENT", 3: "CQ_ERR_UNSUPPORTED",
+           4: "CQ_ERR_CUDA", 5: "CQ_ERR_DEVICE_TIMEOUT", 6: "CQ_ERR_WORKSPACE"}
+
+
+class CQError(RuntimeError):
+    def __init__(self, fn, status, cuda_err=0):
+        name = _STATUS.get(status, f"status {status}")
+        msg = f"{fn} failed: {name}"
+        if status == 4:
+            msg += f" (cudaError {cuda_err})"
+        super().__init__(msg)
+        self.status = status
+
+
+class cq_codebook(ctypes.Structure):
+    _fields_ = [("cb", ctypes.c_float * 28)]
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "cq_status_string": (ctypes.c_char_p, [_INT]),
+    "cq_last_cuda_error": (_INT, []),
+    "cq_abi_version": (_INT, []),
+    "cq_codebook_fit": (_INT, [_P, _I64, _INT, _INT, _P, _P]),
+    "cq_encode": (_INT, [_P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _P]),
+    "a8_quantize": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "cq_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
+    "cq_gemv": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _I64,
+                       _P, _P, _SZ, _P]),
+    "q4_0_quantize": (_INT, [_P, _I64, _I64, _P, _P]),
+    "q4_0_gemv": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P]),
+}
+
+
+def lib():
+    """Load ``libcqgemv.so`` (once).  Raises if it is missing: nothing runs without it."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                "g.build()\"` (nvcc, sm_103a). There is no fallback implementation.")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t, dtype, name, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn, status):
+    if status != CQ_OK:
+        raise CQError(fn, status, lib().cq_last_cuda_error())
+
+
+def make_codebook(cb28):
+    """Build the C ``cq_codebook`` from 28 floats (``cb2 | cb3 | cb4``)."""
+    vals = [float(v) for v in (cb28.tolist() if hasattr(cb28, "tolist") else cb28)]
+    if len(vals) != 28:
+        raise ValueError("codebook needs 28 floats (cb2[4] | cb3[8] | cb4[16])")
+    c = cq_codebook()
+    for i, v in enumerate(vals):
+        c.cb[i] = v
+    return c
+
+
+def _cbk(cb):
+    return cb if isinstance(cb, cq_codebook) else make_codebook(cb)
+
+
+def cq_status_string(status: int) -> str:
+    return lib().cq_status_string(status).decode()
+
+
+def cq_abi_version() -> int:
+    return lib().cq_abi_version()
+
+
+def cq_codebook_fit(samples, L, iters=200, levels_out=None, stream=None):
+    """A1: Lloyd-Max levels (float32 [L]) from float64 samples on the GPU."""
+    s = _ptr(samples, torch.float64, "samples")
+    if levels_out is None:
+        levels_out = torch.empty(L, dtype=torch.float32, device=samples.device)
+    _check("cq_codebook_fit", lib().cq_codebook_fit(s, samples.numel(), L, iters,
+                                                     _ptr(levels_out, torch.float32, "levels_out"),
+                                                     _stream(stream)))
+    return levels_out
+
+
+def cq_encode(W, b, cb, packed=None, norms=None, g=128, stream=None):
+    """A2: CQ-encode W [N, K] float32 -> (packed uint8 [N, K/128, 16b], norms int16 [N, K/128])."""
+    N, K = W.shape
+    wp = _ptr(W, torch.float32, "W", 2)
+    if packed is None:
+        packed = torch.empty((N, K // 128, 16 * b), dtype=torch.uint8, device=W.device)
+    if norms is None:
+        norms = torch.empty((N, K // 128), dtype=torch.int16, device=W.device)
+    c = _cbk(cb)
+    _check("cq_encode", lib().cq_encode(wp, N, K, g, b, ctypes.byref(c),
+                                        _ptr(packed, torch.uint8, "packed"),
+                                        _ptr(norms, torch.int16, "norms"), _stream(stream)))
+    return packed, norms
+
+
+def a8_quantize(X, Xq=None, scale=None, stream=None):
+    """A3: X [B, K] float32 -> (Xq int8 [B, K], scale float32 [B])."""
+    B, K = X.shape
+    xp = _ptr(X, torch.float32, "X", 2)
+    if Xq is None:
+        Xq = torch.empty((B, K), dtype=torch.int8, device=X.device)
+    if scale is None:
+        scale = torch.empty((B,), dtype=torch.float32, device=X.device)
+    _check("a8_quantize", lib().a8_quantize(xp, B, K, _ptr(Xq, torch.int8, "Xq"),
+                                            _ptr(scale, torch.float32, "scale"), _stream(stream)))
+    return Xq, scale
+
+
+def cq_gemv_workspace_bytes(B, K) -> int:
+    return int(lib().cq_gemv_workspace_bytes(B, K))
+
+
+def cq_gemv(packed, norms, N, K, b, cb, Xq, scale, Y=None, workspace=None, g=128, stream=None):
+    """A4+A5: Y [B, N] float32 = decode GEMV of CQ weights with int8 activations."""
+    B = Xq.shape[0]
+    if Y is None:
+        Y = torch.empty((B, N), dtype=torch.float32, device=Xq.device)
+    need = cq_gemv_workspace_bytes(B, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=Xq.device)
+    c = _cbk(cb)
+    _check("cq_gemv", lib().cq_gemv(_ptr(packed, torch.uint8, "packed"),
+                                    _ptr(norms, torch.int16, "norms"), N, K, g, b, ctypes.byref(c),
+                                    _ptr(Xq, torch.int8, "Xq"), _ptr(scale, torch.float32, "scale"),
+                                    B, _ptr(Y, torch.float32, "Y"),
+                                    _ptr(workspace, torch.uint8, "workspace"),
+                                    workspace.numel(), _stream(stream)))
+    return Y
+
+
+def q4_0_quantize(W, blocks=None, stream=None):
+    """A7: W [N, K] float32 -> Q4_0 blocks uint8 [N, ceil(K/32)*18]."""
+    N, K = W.shape
+    if blocks is None:
+        blocks = torch.empty((N, ((K + 31) // 32) * 18), dtype=torch.uint8, device=W.device)
+    _check("q4_0_quantize", lib().q4_0_quantize(_ptr(W, torch.float32, "W", 2), N, K,
+                                                _ptr(blocks, torch.uint8, "blocks"), _stream(stream)))
+    return blocks
+
+
+def q4_0_gemv(blocks, N, K, X, Y=None, stream=None):
+    """A8: Y [B, N] float32 = Q4_0 decode GEMV with float32 activations X [B, K]."""
+    B = X.shape[0]
+    if Y is None:
+        Y = torch.empty((B, N), dtype=torch.float32, device=X.device)
+    _check("q4_0_gemv", lib().q4_0_gemv(_ptr(blocks, torch.uint8, "blocks"), N, K,
+                                        _ptr(X, torch.float32, "X"), B, _ptr(Y, torch.float32, "Y"),
+                                        _stream(stream)))
+    return Y

@@ -1,0 +1,42 @@
+// Library-wide entry points of libcqgemv: status strings, error bookkeeping, version.
+#include "common.cuh"
+
+namespace cq {
+
+namespace {
+thread_local int g_last_cuda_error = 0;
+int g_sm_count[64] = {0};
+}  // namespace
+
+void set_last_cuda_error(int code) { g_last_cuda_error = code; }
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace cq
+
+extern "C" const char* cq_status_string(cq_status s) {
+    switch (s) {
+        case CQ_OK: return "CQ_OK";
+        case CQ_ERR_INVALID_ARG: return "CQ_ERR_INVALID_ARG";
+        case CQ_ERR_ALIGNMENT: return "CQ_ERR_ALIGNMENT";
+        case CQ_ERR_UNSUPPORTED: return "CQ_ERR_UNSUPPORTED";
+        case CQ_ERR_CUDA: return "CQ_ERR_CUDA";
+        case CQ_ERR_DEVICE_TIMEOUT: return "CQ_ERR_DEVICE_TIMEOUT";
+        case CQ_ERR_WORKSPACE: return "CQ_ERR_WORKSPACE";
+    }
+    return "CQ_ERR_UNKNOWN";
+}
+
+extern "C" int cq_last_cuda_error(void) { return cq::g_last_cuda_error; }
+
+extern "C" int cq_abi_version(void) { return CQGEMV_ABI_VERSION; }

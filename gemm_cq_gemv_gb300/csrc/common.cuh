@@ -1,0 +1,73 @@
+// Shared device/host helpers of libcqgemv (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "cqgemv.h"
+
+namespace cq {
+
+constexpr int kGroup = 128;
+
+// Remembers the last CUDA error code per host thread (cq_last_cuda_error).
+void set_last_cuda_error(int code);
+
+inline cq_status check_launch() {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_last_cuda_error((int)e);
+        return CQ_ERR_CUDA;
+    }
+    return CQ_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// float64 -> IEEE binary16 bits, one round-to-nearest-even step (ties to even),
+// written from the binary16 definition: 1 sign bit, 5 exponent bits (bias 15),
+// 10 fraction bits, subnormals with unit 2^-24, overflow to infinity.
+__device__ __forceinline__ uint16_t f64_to_f16_bits_rne(double x) {
+    unsigned long long u = (unsigned long long)__double_as_longlong(x);
+    uint32_t sign = (uint32_t)(u >> 48) & 0x8000u;
+    u &= 0x7FFFFFFFFFFFFFFFull;
+    uint32_t ebits = (uint32_t)(u >> 52);
+    if (ebits == 0x7FF) {  // inf / nan
+        return (uint16_t)(sign | 0x7C00u | ((u & 0xFFFFFFFFFFFFFull) ? 0x200u : 0u));
+    }
+    if (ebits == 0) return (uint16_t)sign;  // float64 zero / subnormal -> signed zero
+    int e = (int)ebits - 1023;
+    unsigned long long m = (u & 0xFFFFFFFFFFFFFull) | (1ull << 52);  // 53-bit significand
+    if (e > 15) return (uint16_t)(sign | 0x7C00u);
+    if (e >= -14) {
+        unsigned long long hm = m >> 42;                 // 11 bits incl. the leading one
+        unsigned long long rem = m & ((1ull << 42) - 1);
+        const unsigned long long half = 1ull << 41;
+        if (rem > half || (rem == half && (hm & 1ull))) hm++;
+        uint32_t eh = (uint32_t)(e + 15);
+        if (hm == 2048ull) { hm = 1024ull; eh++; }
+        if (eh >= 31u) return (uint16_t)(sign | 0x7C00u);
+        return (uint16_t)(sign | (eh << 10) | (uint32_t)(hm & 0x3FFull));
+    }
+    // subnormal binary16: value / 2^-24 = m * 2^(e - 28)
+    int shift = 28 - e;                                   // >= 43
+    if (shift >= 64) return (uint16_t)sign;
+    unsigned long long q = m >> shift;
+    unsigned long long rem = m & ((1ull << shift) - 1);
+    unsigned long long half = 1ull << (shift - 1);
+    if (rem > half || (rem == half && (q & 1ull))) q++;
+    return (uint16_t)(sign | (uint32_t)q);               // q == 1024 is the smallest normal
+}
+
+// IEEE binary16 bits -> float32 (exact).
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+}  // namespace cq

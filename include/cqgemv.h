@@ -1,0 +1,145 @@
+/*
+ * cqgemv.h - C ABI of the GB300 (sm_103a) low-bit GEMV / GEMM library (libcqgemv.so).
+ *
+ * Two weight formats:
+ *
+ *  CQ-WxA8 ("14MB 装下 45M 参数：拆解 Needle 的 .cact 单文件与 W4A8 量化魔法", §一 and §三;
+ *  "免解析加载的秘诀：mmap 直读张量与 Needle 的秒级冷启动", section "mmap 之下张量按偏移直读"):
+ *    a matmul weight W is stored pre-transposed [out = N, in = K]; each row is cut into
+ *    groups of g = 128 along K; each group is rotated by the normalised Walsh-Hadamard
+ *    transform, every rotated coordinate is replaced by the index of the nearest
+ *    Lloyd-Max Gaussian codeword (b = 1..4 bits), and the group's L2 norm is kept in
+ *    FP16.  Reconstruction: w_group = (cb[idx] * norm / sqrt(g)) @ H, H = Hu / sqrt(g)
+ *    (Hu the Sylvester Hadamard matrix, entries +-1).  Activations are int8 per token.
+ *
+ *  Q4_0 (Minueza-32M -> KMCU v1 page, §2 "Q4_0 量化" and §3 "行对齐到 32"):
+ *    rows zero-padded to a multiple of 32; 32-weight blocks of 18 bytes: fp16 scale
+ *    d = max_abs / 8 (little-endian, bytes 0..1), then 16 bytes of nibbles
+ *    q + 8 with q = clip(rint(w / d), -8, 7), the low nibble holding the even index.
+ *
+ * Conventions shared by every call:
+ *  - All array pointers are CUDA DEVICE memory owned by the caller; the library keeps no
+ *    pointer after a call returns and allocates no device memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
+ *    work: they are asynchronous and do not synchronise.
+ *  - Arguments are validated before anything is launched; a failed check returns an
+ *    error status and launches nothing.
+ *  - Row-major layouts; sizes are element counts unless named *_bytes.
+ *  - Pointers must be 16-byte aligned (CQ_ERR_ALIGNMENT otherwise), except the
+ *    Q4_0 block array, which needs no alignment.
+ *  - CQ_ERR_CUDA means a CUDA runtime call or launch failed; cq_last_cuda_error()
+ *    returns its cudaError_t code.
+ */
+#ifndef CQGEMV_H
+#define CQGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CQGEMV_ABI_VERSION 1
+#define CQ_GROUP 128            /* CQ group size along K (Needle .cact page, §一) */
+#define Q4_0_BLOCK 32           /* weights per Q4_0 block (KMCU page, §2)          */
+#define Q4_0_BLOCK_BYTES 18     /* bytes per Q4_0 block  (KMCU page, §2)          */
+
+typedef enum cq_status {
+    CQ_OK = 0,
+    CQ_ERR_INVALID_ARG = 1,     /* bad shape, NULL pointer, g != 128, b not in 1..4, ... */
+    CQ_ERR_ALIGNMENT = 2,       /* a pointer is not 16-byte aligned                      */
+    CQ_ERR_UNSUPPORTED = 3,     /* no sm_103 device, or a size the kernels do not cover  */
+    CQ_ERR_CUDA = 4,            /* CUDA runtime / launch error (see cq_last_cuda_error)  */
+    CQ_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait gave up                    */
+    CQ_ERR_WORKSPACE = 6        /* workspace missing or smaller than *_workspace_bytes   */
+} cq_status;
+
+/* Codebook table: cb2[4] | cb3[8] | cb4[16], each ascending, in N(0,1) units - the
+ * header table of the Needle .cact page, §一.  b = 1 ignores it and uses the analytic
+ * +-sqrt(2/pi) of the Needle mmap page.  Passed by pointer to HOST memory; copied by
+ * value into kernel parameters. */
+typedef struct cq_codebook {
+    float cb[28];
+} cq_codebook;
+
+/* Human-readable name of a status. Never NULL. */
+const char* cq_status_string(cq_status s);
+/* cudaError_t code of the last CQ_ERR_CUDA returned on the calling host thread (0 if none). */
+int cq_last_cuda_error(void);
+/* CQGEMV_ABI_VERSION of the loaded library. */
+int cq_abi_version(void);
+
+/* ---- A1: Lloyd-Max Gaussian codebook fit (Needle .cact page, §一: Lloyd-Max on
+ * 400k Gaussian samples, 200 iterations).  Levels start at the N(0,1) quantiles
+ * (t + 0.5) / L; one iteration puts thresholds at the midpoints of adjacent levels
+ * (a sample equal to a threshold joins the lower cell) and moves each level to the
+ * float64 mean of its cell (an empty cell keeps its level).
+ *   samples    [n] float64, device
+ *   L          number of levels, 2..16
+ *   levels_out [L] float32, device, ascending
+ * Errors: INVALID_ARG (n < 1, L out of range, iters < 0, NULL).  One CTA; meant for
+ * offline use. */
+cq_status cq_codebook_fit(const double* samples, int64_t n, int L, int iters,
+                          float* levels_out, void* stream);
+
+/* ---- A2: CQ encode (Needle .cact page, §一).  For each row o and group j:
+ *   r = Hu @ w (float64 butterflies, natural order), n = sqrt(sum_i w_i^2) (float64,
+ *   summed in index order, no fused multiply-add), idx_i = argmin_t |r_i / n - cb[t]|
+ *   (float64; ties -> lowest index; n == 0 -> all indices 0), norm = fp16(n) (one
+ *   round-to-nearest-even step from float64).
+ *   W       [N][K] float32 ([out, in])
+ *   packed  [N][K/128][16*b] uint8: index i of a group in bits [b*i, b*i+b) of the
+ *           group's little-endian bytes (b = 4: low nibble = even column)
+ *   norms   [N][K/128] uint16 (IEEE binary16 bits)
+ * Bit-exact with the CPU oracle.  Errors: INVALID_ARG (K % 128, g != 128, b not in
+ * 1..4, N or K < 1, NULL), ALIGNMENT. */
+cq_status cq_encode(const float* W, int64_t N, int64_t K, int g, int b,
+                    const cq_codebook* cbk, uint8_t* packed, uint16_t* norms, void* stream);
+
+/* ---- A3: per-token symmetric int8 activations (Needle .cact page, §一: ACT_BITS 8).
+ *   s_t = float32(max_k |X[t][k]|) / 127 (IEEE float32 division; 1 if the token is
+ *   all zero), Xq[t][k] = clip(rint(X[t][k] / s_t), -127, 127).
+ *   X [B][K] float32 -> Xq [B][K] int8, scale [B] float32.  Bit-exact with the oracle.
+ * Errors: INVALID_ARG (B or K < 1, NULL), ALIGNMENT. */
+cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* Xq, float* scale,
+                      void* stream);
+
+/* ---- A4 + A5: decode GEMV (Needle .cact page, §三: each output row streams along
+ * the reduction axis; §一: reconstruction formula).  Computes, in float32,
+ *   Y[t][o] = s_t * sum_j (norm[o][j] / 128) * sum_i cb[idx[o][j][i]] * xr[t][128 j + i]
+ * with xr = Hu @ Xq per group (the rotated int8 activations, exact integers), which
+ * equals (W_hat @ (s * Xq)^T)^T in real arithmetic because Hu is symmetric.
+ * The rotation is done once per call into `workspace` and shared by every row.
+ *   packed, norms  as written by cq_encode
+ *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
+ *   Y  [B][N] float32
+ *   workspace      device scratch of at least cq_gemv_workspace_bytes(B, K) bytes
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, CUDA. */
+size_t cq_gemv_workspace_bytes(int64_t B, int64_t K);
+cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
+                  int g, int b, const cq_codebook* cbk, const int8_t* Xq,
+                  const float* scale, int64_t B, float* Y, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* ---- A7: Q4_0 quantize (KMCU page, §2, §3).
+ *   W [N][K] float32 -> blocks [N][ceil(K/32) * 18] uint8; per block: d = amax / 8
+ *   (float32; 1 if amax == 0), q = clip(rint(w / d), -8, 7) with float32 division,
+ *   nibble = q + 8, byte k = nib[2k] | nib[2k+1] << 4, scale stored as fp16(d) (RNE).
+ *   Columns K..32*ceil(K/32)-1 are zero padding (nibble 8).  Bit-exact with the oracle.
+ * Errors: INVALID_ARG, ALIGNMENT (W only). */
+cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks, void* stream);
+
+/* ---- A8: Q4_0 decode GEMV (KMCU page, §2, §3: fixed-length 32 inner loop over
+ * row-aligned blocks).  Y[t][o] = sum_blocks fp32(d) * sum_k (nib - 8) * X[t][k],
+ * float32 accumulation; padding columns are skipped.
+ *   blocks [N][ceil(K/32) * 18] uint8 (any alignment), X [B][K] float32, Y [B][N] float32
+ * Errors: INVALID_ARG, ALIGNMENT (X, Y), CUDA. */
+cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t B,
+                    float* Y, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CQGEMV_H */

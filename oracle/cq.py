@@ -131,7 +131,11 @@ def cq_encode(W: np.ndarray, b: int, cb28: np.ndarray, g: int = GROUP):
         raise ValueError("K must be a multiple of the group size")
     levels = codebook_levels(cb28, b)
     G = K // g
-    idx, n = _encode_groups(W.reshape(N * G, g), levels)
+    flat = W.reshape(N * G, g)
+    idx = np.empty((N * G, g), dtype=np.int64)
+    n = np.empty(N * G, dtype=np.float64)
+    for c0 in range(0, N * G, 8192):          # chunks only bound host memory
+        idx[c0:c0 + 8192], n[c0:c0 + 8192] = _encode_groups(flat[c0:c0 + 8192], levels)
     norms16 = n.astype(np.float16).view(np.uint16).reshape(N, G)
     packed = pack_indices(idx, b).reshape(N, G, 16 * b)
     return packed, norms16

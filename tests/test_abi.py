@@ -1,0 +1,99 @@
+"""The C-ABI library loads, exports every function ``include/*.h`` declares, and rejects
+bad arguments on the host before launching anything (no GPU needed)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import gemm_cq_gemv_gb300 as cq
+from gemm_cq_gemv_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+DECL = re.compile(r"^\s*(?:const\s+char\s*\*|cq_status|size_t|int)\s+(\w+)\s*\(", re.M)
+
+
+def _declared():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        with open(h) as f:
+            names += DECL.findall(f.read())
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return cq.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in cq.SIGNATURES, f"binding lacks a signature for {n}"
+
+
+def test_status_strings_and_version(lib):
+    assert cq.cq_abi_version() == 1
+    for code, name in [(0, "CQ_OK"), (1, "CQ_ERR_INVALID_ARG"), (2, "CQ_ERR_ALIGNMENT"),
+                       (3, "CQ_ERR_UNSUPPORTED"), (4, "CQ_ERR_CUDA"), (5, "CQ_ERR_DEVICE_TIMEOUT"),
+                       (6, "CQ_ERR_WORKSPACE")]:
+        assert cq.cq_status_string(code) == name
+    assert cq.cq_status_string(99) == "CQ_ERR_UNKNOWN"
+
+
+def test_workspace_size_query(lib):
+    assert cq.cq_gemv_workspace_bytes(1, 4096) == 4096 * 4
+    assert cq.cq_gemv_workspace_bytes(0, 4096) == 0
+
+
+# Host-side validation: fake (never dereferenced) pointers; every call below must return
+# an error before any CUDA call is made.
+A = 0x10000   # 16-byte aligned fake address
+M = 0x10004   # misaligned fake address
+
+
+def _cb():
+    return ctypes.byref(cq.make_codebook([0.0] * 28))
+
+
+def test_encode_validation(lib):
+    INV, ALN = 1, 2
+    assert lib.cq_encode(A, 4, 100, 128, 4, _cb(), A, A, None) == INV     # K % 128
+    assert lib.cq_encode(A, 4, 128, 64, 4, _cb(), A, A, None) == INV      # g != 128
+    assert lib.cq_encode(A, 4, 128, 128, 0, _cb(), A, A, None) == INV     # b = 0
+    assert lib.cq_encode(A, 4, 128, 128, 5, _cb(), A, A, None) == INV     # b = 5
+    assert lib.cq_encode(None, 4, 128, 128, 4, _cb(), A, A, None) == INV  # NULL
+    assert lib.cq_encode(A, 0, 128, 128, 4, _cb(), A, A, None) == INV     # N = 0
+    assert lib.cq_encode(M, 4, 128, 128, 4, _cb(), A, A, None) == ALN
+
+
+def test_a8_and_q4_validation(lib):
+    INV, ALN = 1, 2
+    assert lib.a8_quantize(A, 0, 16, A, A, None) == INV
+    assert lib.a8_quantize(A, 1, 16, M, A, None) == ALN
+    assert lib.q4_0_quantize(A, 1, 0, A, None) == INV
+    assert lib.q4_0_quantize(M, 1, 32, A, None) == ALN
+    assert lib.q4_0_gemv(A, 1, 0, A, 1, A, None) == INV
+    assert lib.q4_0_gemv(A, 1, 32, A, 1, M, None) == ALN
+
+
+def test_gemv_validation(lib):
+    INV, ALN, WS = 1, 2, 6
+    f = lib.cq_gemv
+    assert f(A, A, 8, 100, 128, 4, _cb(), A, A, 1, A, A, 1 << 20, None) == INV
+    assert f(A, A, 8, 128, 128, 7, _cb(), A, A, 1, A, A, 1 << 20, None) == INV
+    assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 0, A, A, 1 << 20, None) == INV
+    assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 1, M, A, 1 << 20, None) == ALN
+    assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 2, A, A, 16, None) == WS
+    assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 2, A, None, 1 << 20, None) == WS
+
+
+def test_codebook_fit_validation(lib):
+    assert lib.cq_codebook_fit(A, 100, 1, 10, A, None) == 1
+    assert lib.cq_codebook_fit(A, 100, 17, 10, A, None) == 1
+    assert lib.cq_codebook_fit(None, 100, 4, 10, A, None) == 1
