@@ -1,0 +1,446 @@
+"""Throughput of the low-bit decode GEMV path on GB300 (one JSON line on rank 0).
+
+A step is one decode pass (batch 1) over the large-shape workload: CQ-W4A8 GEMV
+(``a8_quantize`` -> rotation -> ``cq_gemv``) and Q4_0 GEMV (``q4_0_gemv``) on the four
+matrices [8192, 8192], [28672, 8192], [8192, 28672] and the lm_head [128256, 4096]
+(1.15 GB of packed weights per step, far larger than L2, so no flush is needed).
+Weights are encoded once before timing (offline, as the format intends); the timed
+region holds only the decode work.  ``value`` is algorithmic GB/s: packed indices +
+norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step time.
+
+``--impl reference`` times the CPU oracle as it stands on a bounded sample of the same
+workload.  ``--gpus N`` (under torchrun) runs N independent replicas, one per GPU:
+the path needs no exchange, so there is no collective beyond the timing barrier.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("decode GEMV GB/s & Gweights/s (frac of HBM); prefill GEMM TFLOP/s "
+          "(frac of TC peak)")
+WORKLOAD = ("large-shape decode, batch 1: CQ-W4A8 GEMV (4-bit, group 128, int8 per-token "
+            "activations) and Q4_0 GEMV on [8192,8192], [28672,8192], [8192,28672], "
+            "lm_head [128256,4096]")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_codebook():
+    """The committed Lloyd-Max table (cb2 | cb3 | cb4 as float32 bit patterns)."""
+    with open(os.path.join(ROOT, "tests", "golden", "codebook_seed0.json")) as f:
+        d = json.load(f)
+    hexes = d["cb2_f32_hex"] + d["cb3_f32_hex"] + d["cb4_f32_hex"]
+    return np.array([int(h, 16) for h in hexes], dtype=np.uint32).view(np.float32)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("gemv.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "gemm_cq_gemv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, alg_bytes_per_launch):
+    """DRAM bytes per launch for ``kernel``, scaled from the committed ncu capture.
+
+    The capture covers one matrix of the workload (``profiles/traffic.json``); its
+    DRAM-bytes / algorithmic-bytes ratio is applied to this run's algorithmic bytes per
+    launch.  None when the kernel source changed since the counters were taken.
+    """
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(kernel)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return int(round(rec["traffic_over_algorithmic"] * alg_bytes_per_launch))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        with open(self.out.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------
+# The GPU arm
+# ------------------------------------------------------------------------------------
+def build_workload(dev, cb, torch, cq, synth, only=None):
+    """Encode the large-shape weights once (device) and allocate every step buffer."""
+    mats = []
+    for i, m in enumerate(synth.LARGE):
+        if only and m.name not in only:
+            continue
+        g = torch.Generator(device=dev)
+        g.manual_seed(synth.weight_seed(4, i))
+        W = torch.randn((m.N, m.K), device=dev, generator=g) * 0.02
+        packed, norms = cq.cq_encode(W, 4, cb)
+        blocks = cq.q4_0_quantize(W)
+        del W
+        gx = torch.Generator(device=dev)
+        gx.manual_seed(synth.activation_seed(4, 1) + i)
+        X = torch.randn((1, m.K), device=dev, generator=gx)
+        mats.append(dict(
+            m=m, packed=packed, norms=norms, blocks=blocks, X=X,
+            Xq=torch.empty((1, m.K), dtype=torch.int8, device=dev),
+            s=torch.empty((1,), dtype=torch.float32, device=dev),
+            ws=torch.empty((cq.cq_gemv_workspace_bytes(1, m.K),), dtype=torch.uint8, device=dev),
+            Ycq=torch.empty((1, m.N), dtype=torch.float32, device=dev),
+            Yq4=torch.empty((1, m.N), dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()   # release the float32 weights before anything is timed
+    return mats
+
+
+def step_bytes(mats):
+    cq_b = sum(d["packed"].numel() + 2 * d["norms"].numel() + d["m"].K + 4 + 4 * d["m"].N
+               for d in mats)
+    q4_b = sum(d["blocks"].numel() + 4 * d["m"].K + 4 * d["m"].N for d in mats)
+    weights = sum(2 * d["m"].N * d["m"].K for d in mats)
+    return cq_b, q4_b, weights
+
+
+def run_step(mats, cb, cq, events=None, kinds=("cq", "q4_0")):
+    """One decode pass.  With ``events``, brackets each GEMV launch for per-kernel time."""
+    for d in mats:
+        m = d["m"]
+        if "cq" in kinds:
+            cq.a8_quantize(d["X"], Xq=d["Xq"], scale=d["s"])
+            if events is not None:
+                events["cq_gemv"][0].append(_ev())
+            cq.cq_gemv(d["packed"], d["norms"], m.N, m.K, 4, cb, d["Xq"], d["s"], Y=d["Ycq"],
+                       workspace=d["ws"])
+            if events is not None:
+                events["cq_gemv"][1].append(_ev())
+        if "q4_0" in kinds:
+            if events is not None:
+                events["q4_0_gemv"][0].append(_ev())
+            cq.q4_0_gemv(d["blocks"], m.N, m.K, d["X"], Y=d["Yq4"])
+            if events is not None:
+                events["q4_0_gemv"][1].append(_ev())
+
+
+def reduce_max(x, dist, device):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _ev():
+    import torch
+    e = torch.cuda.Event(enable_timing=True)
+    e.record()
+    return e
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import gemm_cq_gemv_gb300 as cq
+    from gemm_cq_gemv_gb300 import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cb = cq.make_codebook(load_codebook())
+    mats = build_workload(dev, cb, torch, cq, synth, only=args.case)
+    kinds = tuple(args.kernels)
+    cq_b, q4_b, weights = step_bytes(mats)
+    cq_b = cq_b if "cq" in kinds else 0
+    q4_b = q4_b if "q4_0" in kinds else 0
+    weights = weights // 2 * len(kinds)
+    total_b = cq_b + q4_b
+
+    for _ in range(args.warmup):
+        run_step(mats, cb, cq, kinds=kinds)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.4)
+    events = {"cq_gemv": ([], []), "q4_0_gemv": ([], [])}
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        run_step(mats, cb, cq, events, kinds=kinds)
+    t1.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = reduce_max(t0.elapsed_time(t1) / args.steps, dist, dev)
+
+    per_kernel = {}
+    for k, (a, b) in events.items():
+        if a:
+            tot = sum(x.elapsed_time(y) for x, y in zip(a, b))
+            per_kernel[k] = {"ms_total": tot, "launches": len(a)}
+    if args.no_e2e:
+        if rank == 0:
+            print(json.dumps({"ms_per_step": ms, "kernels": per_kernel,
+                              "GBps": total_b / (ms * 1e-3) / 1e9}), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    # end to end through the public API with host buffers: pinned H2D of the step's
+    # activations, the decode pass, D2H of the step's outputs
+    host_x = [torch.empty(d["X"].shape, dtype=torch.float32, pin_memory=True).copy_(d["X"])
+              for d in mats]
+    host_y = [torch.empty((2, d["m"].N), dtype=torch.float32, pin_memory=True) for d in mats]
+    h2d = sum(x.numel() * 4 for x in host_x)
+    d2h = sum(y.numel() * 4 for y in host_y)
+
+    def e2e_step():
+        for d, hx in zip(mats, host_x):
+            d["X"].copy_(hx, non_blocking=True)
+        run_step(mats, cb, cq, kinds=kinds)
+        for d, hy in zip(mats, host_y):
+            hy[0].copy_(d["Ycq"][0], non_blocking=True)
+            hy[1].copy_(d["Yq4"][0], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max((time.perf_counter() - a) * 1e3 / args.steps, dist, dev)
+
+    if rank == 0:
+        peaks, kind = load_peaks()
+        hbm = float(peaks["hbm_gbs"])
+        dom = max(per_kernel, key=lambda k: per_kernel[k]["ms_total"])
+        dom_bytes = cq_b if dom == "cq_gemv" else q4_b
+        dk = per_kernel[dom]
+        achieved = dom_bytes * args.steps / (dk["ms_total"] * 1e-3) / 1e9
+        value = world * total_b / (ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+            "config": {"workload": WORKLOAD, "batch": 1, "group": 128, "cq_bits": 4,
+                       "bytes_per_step": total_b, "weights_per_step": weights,
+                       "l2": "inputs larger than L2 (1.15 GB of weights per step)",
+                       "parallelism": f"replicas x{world}"},
+            "gweights_per_s": round(world * weights / (ms * 1e-3) / 1e9, 2),
+            "frac_of_hbm": round(value / world / hbm, 4),
+            "kernels": {k: {"launches": v["launches"], "ms_total": round(v["ms_total"], 4),
+                            "GBps": round((cq_b if k == "cq_gemv" else q4_b) * args.steps /
+                                          (v["ms_total"] * 1e-3) / 1e9, 1)}
+                        for k, v in per_kernel.items()},
+            "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                         "peak_source": f"{kind} (MEASURED_PEAKS.json hbm_gbs)" if kind == "measured"
+                         else "fallback 6.8 TB/s",
+                         "algorithmic_bytes_per_launch": dom_bytes // len(mats),
+                         "traffic": recorded_traffic(dom, dom_bytes // len(mats))},
+            "e2e": {"value": round(world * total_b / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps * len(mats) * (3 * ("cq" in kinds) + ("q4_0" in kinds)),
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------
+# The oracle arm (CPU): the oracle as it stands, on a bounded sample of the workload
+# ------------------------------------------------------------------------------------
+def oracle_sample_step(rows, cb, synth, oracle, state):
+    """Oracle GEMV of ``rows`` rows of every large matrix (both formats); returns bytes."""
+    nbytes = 0
+    for d in state:
+        m = d["m"]
+        nbytes += d["p"].nbytes + d["n"].nbytes + m.K + 4 + 4 * rows
+        oracle.cq_gemv_ref(d["p"], d["n"], 4, cb, d["q"], d["s"])
+        nbytes += d["b"].nbytes + 4 * m.K + 4 * rows
+        oracle.q4_0_gemv_ref(d["b"], m.K, d["X"])
+    return nbytes
+
+
+def oracle_state(rows, cb, synth, oracle):
+    state = []
+    for i, m in enumerate(synth.LARGE):
+        W = synth.weights(rows, m.K, seed=synth.weight_seed(4, i))
+        X = synth.activations(1, m.K, seed=synth.activation_seed(4, 1) + i)
+        p, n = oracle.cq_encode(W, 4, cb)
+        q, s = oracle.a8_quantize(X)
+        state.append(dict(m=m, p=p, n=n, q=q, s=s, X=X, b=oracle.q4_0_quantize(W)))
+    return state
+
+
+def cpu_baseline(rows):
+    import oracle
+    from gemm_cq_gemv_gb300 import synth
+    cb = load_codebook()
+    state = oracle_state(rows, cb, synth, oracle)
+    oracle_sample_step(rows, cb, synth, oracle, state)
+    reps, nbytes = 4, 0
+    a = time.perf_counter()
+    for _ in range(reps):
+        nbytes += oracle_sample_step(rows, cb, synth, oracle, state)
+    dt = time.perf_counter() - a
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{reps} x {rows} rows of each large matrix, CQ-W4A8 and Q4_0, batch 1 "
+                      f"(float64 reconstruction + product), {dt:.1f} s"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from gemm_cq_gemv_gb300 import synth
+    cb = load_codebook()
+    rows = args.cpu_rows
+    state = oracle_state(rows, cb, synth, oracle)
+    for _ in range(args.warmup):
+        oracle_sample_step(rows, cb, synth, oracle, state)
+    a = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += oracle_sample_step(rows, cb, synth, oracle, state)
+    dt = time.perf_counter() - a
+    value = nbytes / dt / 1e9
+    ms = dt * 1e3 / args.steps
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "batch": 1, "group": 128, "cq_bits": 4,
+                   "parallelism": "cpu oracle, rank 0"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{rows} rows of each large matrix per step, both formats"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=256,
+                    help="rows per matrix in the oracle sample (CPU baseline / reference arm)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="time the device step only and print a short line (profiling runs)")
+    ap.add_argument("--case", nargs="*", default=None,
+                    help="restrict to these large matrices (sq8k up28k down28k lm_head)")
+    ap.add_argument("--kernels", nargs="*", default=["cq", "q4_0"], choices=["cq", "q4_0"])
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+    else:
+        gpu_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

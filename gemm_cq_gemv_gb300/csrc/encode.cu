@@ -212,16 +212,19 @@ q4_0_quantize_kernel(const float* __restrict__ W, int64_t N, int64_t K, int64_t 
         amax = fmaxf(amax, fabsf(v[k]));
     }
     const float d = (amax > 0.0f) ? __fdiv_rn(amax, 8.0f) : 1.0f;
-    uint8_t* o = out + bid * 18;
-    const uint16_t d16 = __half_as_ushort(__float2half_rn(d));
-    o[0] = (uint8_t)(d16 & 0xFF);
-    o[1] = (uint8_t)(d16 >> 8);
+    // 18 bytes as nine little-endian 16-bit words (the block start is 2-byte aligned):
+    // word 0 = fp16(d), word 1 + k = nibble bytes 2k and 2k+1.
+    uint16_t* o = reinterpret_cast<uint16_t*>(out + bid * 18);
+    o[0] = __half_as_ushort(__float2half_rn(d));
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        float q0 = fminf(fmaxf(rintf(__fdiv_rn(v[2 * k], d)), -8.0f), 7.0f);
-        float q1 = fminf(fmaxf(rintf(__fdiv_rn(v[2 * k + 1], d)), -8.0f), 7.0f);
-        const uint32_t n0 = (uint32_t)((int)q0 + 8), n1 = (uint32_t)((int)q1 + 8);
-        o[2 + k] = (uint8_t)(n0 | (n1 << 4));
+    for (int k = 0; k < 8; ++k) {
+        uint32_t word = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float q = fminf(fmaxf(rintf(__fdiv_rn(v[4 * k + j], d)), -8.0f), 7.0f);
+            word |= (uint32_t)((int)q + 8) << (4 * j);
+        }
+        o[1 + k] = (uint16_t)word;
     }
 }
 

@@ -96,8 +96,8 @@ def test_cq_gemv_batch_consistency():
     q, s = cq.a8_quantize(to_dev(X))
     Yb = to_host(cq.cq_gemv(packed, norms, 333, 1024, 3, cb, q, s))
     for t in range(7):
-        Y1 = to_host(cq.cq_gemv(packed, norms, 333, 1024, 3, cb, q[t:t + 1].contiguous(),
-                                s[t:t + 1].contiguous()))
+        Y1 = to_host(cq.cq_gemv(packed, norms, 333, 1024, 3, cb, q[t:t + 1].clone(),
+                                s[t:t + 1].clone()))
         assert np.allclose(Yb[t], Y1[0], rtol=1e-5, atol=1e-6 * np.abs(Y1).max())
 
 
