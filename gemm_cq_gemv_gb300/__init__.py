@@ -6,10 +6,11 @@ names plus the seeded input generators in ``synth``.  Loading is lazy; the first
 raises if the shared library has not been built.
 """
 
-from ._binding import (CQError, LIB_PATH, SIGNATURES, a8_quantize, cq_abi_version,
-                       cq_codebook, cq_codebook_fit, cq_encode, cq_gemv, cq_gemv_workspace_bytes,
+from ._binding import (CQError, LIB_PATH, NOALLOC_MAX_ELEMS, SIGNATURES, a8_quantize, cq_abi_version,
+                       cq_codebook, cq_codebook_fit, cq_encode, cq_gemv, cq_gemv_noalloc,
+                       cq_gemv_workspace_bytes,
                        cq_status_string, lib, make_codebook, q4_0_gemv, q4_0_quantize)
 
-__all__ = ["CQError", "LIB_PATH", "SIGNATURES", "a8_quantize", "cq_abi_version", "cq_codebook",
-           "cq_codebook_fit", "cq_encode", "cq_gemv", "cq_gemv_workspace_bytes",
+__all__ = ["CQError", "LIB_PATH", "NOALLOC_MAX_ELEMS", "SIGNATURES", "a8_quantize", "cq_abi_version", "cq_codebook",
+           "cq_codebook_fit", "cq_encode", "cq_gemv", "cq_gemv_noalloc", "cq_gemv_workspace_bytes",
            "cq_status_string", "lib", "make_codebook", "q4_0_gemv", "q4_0_quantize"]

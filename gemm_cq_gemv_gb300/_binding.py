@@ -52,6 +52,8 @@ SIGNATURES = {
     "cq_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
     "cq_gemv": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _I64,
                        _P, _P, _SZ, _P]),
+    "cq_gemv_noalloc": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P,
+                               _P, _I64, _P, _P]),
     "q4_0_quantize": (_INT, [_P, _I64, _I64, _P, _P]),
     "q4_0_gemv": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P]),
 }
@@ -182,6 +184,25 @@ def cq_gemv(packed, norms, N, K, b, cb, Xq, scale, Y=None, workspace=None, g=128
                                     B, _ptr(Y, torch.float32, "Y"),
                                     _ptr(workspace, torch.uint8, "workspace"),
                                     workspace.numel(), _stream(stream)))
+    return Y
+
+
+NOALLOC_MAX_ELEMS = 1 << 20   # CQ_GEMV_NOALLOC_MAX_ELEMS
+
+
+def cq_gemv_noalloc(packed, norms, N, K, b, cb, Xq, scale, Y=None, g=128, stream=None):
+    """``cq_gemv`` for callers that cannot allocate a workspace: the library's fixed
+    4 MiB scratch holds the rotated activations (B * K <= 2**20).  Calls that overlap on
+    the GPU share that scratch and race; the first call on a device must precede any
+    stream capture.  ``Y`` may be passed preallocated."""
+    B = Xq.shape[0]
+    if Y is None:
+        Y = torch.empty((B, N), dtype=torch.float32, device=Xq.device)
+    c = _cbk(cb)
+    _check("cq_gemv_noalloc", lib().cq_gemv_noalloc(
+        _ptr(packed, torch.uint8, "packed"), _ptr(norms, torch.int16, "norms"), N, K, g, b,
+        ctypes.byref(c), _ptr(Xq, torch.int8, "Xq"), _ptr(scale, torch.float32, "scale"), B,
+        _ptr(Y, torch.float32, "Y"), _stream(stream)))
     return Y
 
 

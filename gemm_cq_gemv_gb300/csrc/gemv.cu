@@ -11,6 +11,8 @@
 //   * warps are persistent (grid-stride over tiles) and the activations of the call
 //     sit in shared memory, loaded once per CTA.
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace cq {
@@ -470,4 +472,75 @@ extern "C" cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, cons
         if (s != CQ_OK) return s;
     }
     return CQ_OK;
+}
+
+// ---------------------------------------------------------------------------------
+// cq_gemv_noalloc: the decode GEMV for callers that may not allocate device memory.
+//
+// Some callers cannot hand this library a workspace: code that runs inside a host
+// framework which owns every device allocation (an inference-server plugin, an engine
+// that reserves its whole memory budget at start-up) may not call cudaMalloc while it
+// executes, because an allocation can stall the device and breaks the fixed budget.
+// This entry point keeps the rotated activations in a fixed scratch array that is
+// part of the library image instead.
+//
+//  * The scratch is a file-scope __device__ array of CQ_GEMV_NOALLOC_MAX_ELEMS floats
+//    (4 MiB).  Every GPU on which the library is loaded holds it until the process
+//    exits.  B * K larger than that is rejected with CQ_ERR_WORKSPACE.
+//  * Host code cannot use the array's name as a device address, so the first call on
+//    each device looks the address up (cudaGetSymbolAddress, with that device current)
+//    and caches it; make that first call before any stream capture.
+//  * Every call shares the one array and it keeps the previous call's contents.  Each
+//    call overwrites the B * K entries it reads before reading them, so nothing needs
+//    clearing; but two calls that run at the same time on the GPU (different streams,
+//    overlapping) race on the array.  Serialise them (one stream, or events).
+//  * Nothing here allocates: no cudaMalloc / cudaFree, no library routine that does.
+// ---------------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) float g_noalloc_xr[CQ_GEMV_NOALLOC_MAX_ELEMS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+cq_status noalloc_scratch(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return CQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_xr);   // current device = dev
+        if (e != cudaSuccess || p == nullptr) {
+            set_last_cuda_error((int)e);
+            return CQ_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return CQ_OK;
+}
+
+}  // namespace
+
+extern "C" cq_status cq_gemv_noalloc(const uint8_t* packed, const uint16_t* norms, int64_t N,
+                                     int64_t K, int g, int b, const cq_codebook* cbk,
+                                     const int8_t* Xq, const float* scale, int64_t B, float* Y,
+                                     void* stream) {
+    if (!packed || !norms || !cbk || !Xq || !scale || !Y || N < 1 || K < 1 || B < 1)
+        return CQ_ERR_INVALID_ARG;
+    if (g != kGroup || K % kGroup != 0 || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
+    if (B > (int64_t)CQ_GEMV_NOALLOC_MAX_ELEMS || K > (int64_t)CQ_GEMV_NOALLOC_MAX_ELEMS ||
+        B * K > (int64_t)CQ_GEMV_NOALLOC_MAX_ELEMS)
+        return CQ_ERR_WORKSPACE;
+    if (!aligned16(packed) || !aligned16(norms) || !aligned16(Xq) || !aligned16(scale) ||
+        !aligned16(Y))
+        return CQ_ERR_ALIGNMENT;
+    float* scratch = nullptr;
+    const cq_status s = noalloc_scratch(&scratch);
+    if (s != CQ_OK) return s;
+    return cq_gemv(packed, norms, N, K, g, b, cbk, Xq, scale, B, Y, scratch,
+                   (size_t)CQ_GEMV_NOALLOC_MAX_ELEMS * sizeof(float), stream);
 }

@@ -122,6 +122,24 @@ cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64
                   const float* scale, int64_t B, float* Y, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* ---- cq_gemv without a workspace (the paper has no counterpart to this entry point:
+ * it is a library convenience).  Same computation, arguments and errors as cq_gemv, minus the
+ * workspace, for callers that may not allocate device memory - typically code running
+ * inside a host framework that owns every device allocation (an inference-server
+ * plugin, an engine with a fixed memory budget) and forbids cudaMalloc while it runs.
+ * The rotated activations go to a fixed scratch array inside the library image:
+ *  - CQ_GEMV_NOALLOC_MAX_ELEMS floats (4 MiB), held on every GPU that loads the
+ *    library until the process exits; B * K above it returns CQ_ERR_WORKSPACE;
+ *  - the first call on a device looks up the array's device address (with that device
+ *    current) and caches it: make that first call before any stream capture;
+ *  - all calls share the array; each call writes what it reads, so no clearing is
+ *    needed, but calls that overlap on the GPU (concurrent streams) race on it;
+ *  - allocates nothing (no cudaMalloc / cudaFree, no allocating library routine). */
+#define CQ_GEMV_NOALLOC_MAX_ELEMS (1u << 20)
+cq_status cq_gemv_noalloc(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
+                          int g, int b, const cq_codebook* cbk, const int8_t* Xq,
+                          const float* scale, int64_t B, float* Y, void* stream);
+
 /* ---- A7: Q4_0 quantize (KMCU page, §2, §3).
  *   W [N][K] float32 -> blocks [N][ceil(K/32) * 18] uint8; per block: d = amax / 8
  *   (float32; 1 if amax == 0), q = clip(rint(w / d), -8, 7) with float32 division,
