@@ -205,6 +205,66 @@ def _ev():
     return e
 
 
+def build_prefill(dev, cb, torch, cq, synth, M):
+    """The 20-layer synthetic 45M-parameter model (layer-major), encoded 4-bit on device."""
+    gx = torch.Generator(device=dev)
+    gx.manual_seed(synth.activation_seed(3, M))
+    acts = {K: cq.a8_quantize(torch.randn((M, K), device=dev, generator=gx)) for K in (512, 1536)}
+    items, flops = [], 0
+    for i, (layer, m) in enumerate(synth.prefill_matrices()):
+        g = torch.Generator(device=dev)
+        g.manual_seed(synth.weight_seed(3, i))
+        W = torch.randn((m.N, m.K), device=dev, generator=g) * 0.02
+        packed, norms = cq.cq_encode(W, 4, cb)
+        q, s = acts[m.K]
+        items.append((packed, norms, m.N, m.K, q, s,
+                      torch.empty((M, m.N), dtype=torch.bfloat16, device=dev)))
+        flops += 2 * M * m.N * m.K
+    probs = cq.make_gemm_problems(items)
+    ws = torch.empty((cq.cq_gemm_grouped_workspace_bytes(probs, M),), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    return dict(items=items, probs=probs, ws=ws, flops=flops, M=M)
+
+
+def time_prefill(pf, cb, cq, torch, steps, warmup):
+    """Device time of the grouped prefill GEMM (rotation + tcgen05 GEMM), CUDA events."""
+    f = lambda: cq.cq_gemm_grouped(pf["probs"], pf["M"], 4, cb, workspace=pf["ws"])
+    for _ in range(warmup):
+        f()
+    torch.cuda.synchronize()
+    cq.cq_device_error()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    cq.cq_device_error()
+    return e0.elapsed_time(e1) / steps
+
+
+def prefill_report(dev, cb, torch, cq, synth, steps, warmup, peaks, kind):
+    out = {"workload": "20-layer 45M-parameter model (q,o 512x512; k,v 128x512; up 1536x512; "
+                       "down 512x1536), CQ-W4A8, one grouped launch of 120 matrices",
+           "dtype": "bf16 MMA, fp32 accumulate, bf16 out"}
+    peak = float(peaks["bf16_tflops"])
+    for M in synth.PREFILL_TOKENS:
+        pf = build_prefill(dev, cb, torch, cq, synth, M)
+        ms = time_prefill(pf, cb, cq, torch, steps, warmup)
+        tf = pf["flops"] / (ms * 1e-3) / 1e12
+        out[f"M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "gflop": round(pf["flops"] / 1e9, 2),
+                        "frac": round(tf / peak, 4)}
+        del pf
+        torch.cuda.empty_cache()
+    big = out[f"M{synth.PREFILL_TOKENS[-1]}"]
+    out["roofline"] = {"kernel": "cq_gemm_kernel", "bound": "tensor", "achieved": big["tflops"],
+                       "peak": peak, "unit": "TFLOP/s", "frac": big["frac"],
+                       "peak_source": (f"{kind} bf16_tflops (burst; the GEMM is timed alone)"),
+                       "workload": f"M={synth.PREFILL_TOKENS[-1]}"}
+    return out
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
     import gemm_cq_gemv_gb300 as cq
@@ -217,6 +277,13 @@ def gpu_arm(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     cb = cq.make_codebook(load_codebook())
+    if args.prefill_only:
+        pf = build_prefill(dev, cb, torch, cq, synth, args.prefill_m)
+        ms = time_prefill(pf, cb, cq, torch, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"prefill_M": args.prefill_m, "ms": ms,
+                              "tflops": pf["flops"] / (ms * 1e-3) / 1e12}), flush=True)
+        return
     mats = build_workload(dev, cb, torch, cq, synth, only=args.case)
     kinds = tuple(args.kernels)
     cq_b, q4_b, weights = step_bytes(mats)
@@ -330,8 +397,13 @@ def gpu_arm(args, rank, world, local_rank):
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": args.steps * len(mats) * (3 * ("cq" in kinds) + ("q4_0" in kinds)),
+            "gpu_launches_note": "per decode step: a8_quantize, rotation and cq_gemv kernels per "
+                                 "CQ matrix, one q4_0_gemv kernel per Q4_0 matrix",
             "clocks": clocks,
         }
+        if not args.no_prefill:
+            line["prefill"] = prefill_report(dev, cb, torch, cq, synth, max(3, args.steps // 5),
+                                             args.warmup, peaks, kind)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
         print(json.dumps(line), flush=True)
@@ -430,6 +502,10 @@ def main(argv=None):
     ap.add_argument("--case", nargs="*", default=None,
                     help="restrict to these large matrices (sq8k up28k down28k lm_head)")
     ap.add_argument("--kernels", nargs="*", default=["cq", "q4_0"], choices=["cq", "q4_0"])
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill GEMM report")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the grouped prefill GEMM (profiling runs)")
+    ap.add_argument("--prefill-m", type=int, default=2048)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")

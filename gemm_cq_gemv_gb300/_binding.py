@@ -34,6 +34,12 @@ class cq_codebook(ctypes.Structure):
     _fields_ = [("cb", ctypes.c_float * 28)]
 
 
+class cq_gemm_problem(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("norms", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("Xq", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("Y", ctypes.c_void_p)]
+
+
 _lib = None
 
 _P = ctypes.c_void_p
@@ -54,6 +60,13 @@ SIGNATURES = {
                        _P, _P, _SZ, _P]),
     "cq_gemv_noalloc": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P,
                                _P, _I64, _P, _P]),
+    "cq_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
+    "cq_gemm": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _I64,
+                       _P, _P, _SZ, _P]),
+    "cq_gemm_grouped_workspace_bytes": (_SZ, [ctypes.POINTER(cq_gemm_problem), _INT, _I64]),
+    "cq_gemm_grouped": (_INT, [ctypes.POINTER(cq_gemm_problem), _INT, _I64, _INT, _INT,
+                               ctypes.POINTER(cq_codebook), _P, _SZ, _P]),
+    "cq_device_error": (_INT, [_P]),
     "q4_0_quantize": (_INT, [_P, _I64, _I64, _P, _P]),
     "q4_0_gemv": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P]),
 }
@@ -185,6 +198,64 @@ def cq_gemv(packed, norms, N, K, b, cb, Xq, scale, Y=None, workspace=None, g=128
                                     _ptr(workspace, torch.uint8, "workspace"),
                                     workspace.numel(), _stream(stream)))
     return Y
+
+
+def cq_gemm_workspace_bytes(M, K) -> int:
+    return int(lib().cq_gemm_workspace_bytes(M, K))
+
+
+def cq_gemm(packed, norms, N, K, b, cb, Xq, scale, Y=None, workspace=None, g=128, stream=None):
+    """A4+A6: Y [M, N] bfloat16 = prefill GEMM of CQ weights with int8 activations."""
+    M = Xq.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=Xq.device)
+    need = cq_gemm_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=Xq.device)
+    c = _cbk(cb)
+    _check("cq_gemm", lib().cq_gemm(_ptr(packed, torch.uint8, "packed"),
+                                    _ptr(norms, torch.int16, "norms"), N, K, g, b, ctypes.byref(c),
+                                    _ptr(Xq, torch.int8, "Xq"), _ptr(scale, torch.float32, "scale"),
+                                    M, _ptr(Y, torch.bfloat16, "Y"),
+                                    _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                    _stream(stream)))
+    return Y
+
+
+def make_gemm_problems(items):
+    """``items``: sequence of (packed, norms, N, K, Xq, scale, Y) tensors / ints."""
+    arr = (cq_gemm_problem * len(items))()
+    for i, (packed, norms, N, K, Xq, scale, Y) in enumerate(items):
+        arr[i].packed = _ptr(packed, torch.uint8, "packed").value
+        arr[i].norms = _ptr(norms, torch.int16, "norms").value
+        arr[i].N, arr[i].K = N, K
+        arr[i].Xq = _ptr(Xq, torch.int8, "Xq").value
+        arr[i].scale = _ptr(scale, torch.float32, "scale").value
+        arr[i].Y = _ptr(Y, torch.bfloat16, "Y").value
+    return arr
+
+
+def cq_gemm_grouped_workspace_bytes(problems, M) -> int:
+    return int(lib().cq_gemm_grouped_workspace_bytes(problems, len(problems), M))
+
+
+def cq_gemm_grouped(problems, M, b, cb, workspace=None, g=128, stream=None, device=None):
+    """A6 grouped: every problem (a ``cq_gemm_problem`` array) in persistent launches."""
+    need = cq_gemm_grouped_workspace_bytes(problems, M)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8,
+                                device=device or torch.device("cuda"))
+    c = _cbk(cb)
+    _check("cq_gemm_grouped", lib().cq_gemm_grouped(problems, len(problems), M, g, b,
+                                                    ctypes.byref(c),
+                                                    _ptr(workspace, torch.uint8, "workspace"),
+                                                    workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def cq_device_error(stream=None):
+    """Raise CQError(CQ_ERR_DEVICE_TIMEOUT) if a bounded device wait gave up (clears it)."""
+    _check("cq_device_error", lib().cq_device_error(_stream(stream)))
 
 
 NOALLOC_MAX_ELEMS = 1 << 20   # CQ_GEMV_NOALLOC_MAX_ELEMS

@@ -122,6 +122,49 @@ cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64
                   const float* scale, int64_t B, float* Y, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* ---- A4 + A6: prefill GEMM on the tensor cores (Needle .cact page, §三: prefill is a
+ * GEMM over the same [out, in] rows; §一: reconstruction formula).  Computes
+ *   Y[t][o] = bf16( s_t / 128 * sum_k bf16(xr[t][k]) * bf16(cb[idx[o][k]] * norm[o][k/128]) )
+ * with xr = Hu @ Xq per group (rotated once per call into `workspace`, bf16), tcgen05
+ * MMA with fp32 accumulation in tensor memory.  Only b = 4 is implemented
+ * (CQ_ERR_UNSUPPORTED otherwise).  N must be a multiple of 16.
+ *   Xq [M][K] int8, scale [M] float32 (a8_quantize), Y [M][N] bf16 (uint16 bits)
+ *   workspace: >= cq_gemm_workspace_bytes(M, K) bytes, 256-byte aligned
+ * A device-side wait that does not complete within 2 s sets a device error flag and
+ * the kernel returns early; cq_device_error() reports it as CQ_ERR_DEVICE_TIMEOUT.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
+size_t cq_gemm_workspace_bytes(int64_t M, int64_t K);
+cq_status cq_gemm(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K, int g,
+                  int b, const cq_codebook* cbk, const int8_t* Xq, const float* scale,
+                  int64_t M, uint16_t* Y, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/* One matrix of a grouped prefill launch: all pointers device memory; problems that
+ * share an activation pass the same Xq pointer (and the same K), which is rotated once. */
+typedef struct cq_gemm_problem {
+    const uint8_t* packed;
+    const uint16_t* norms;
+    int64_t N;
+    int64_t K;
+    const int8_t* Xq;
+    const float* scale;
+    uint16_t* Y;
+} cq_gemm_problem;
+
+/* ---- A6 grouped: every problem of `probs` (host array of `count`) with the same M in
+ * one persistent launch per 128 problems (e.g. the 120 matrices of a 20-layer model,
+ * layer-major).  Same arithmetic, limits and errors as cq_gemm; the workspace holds one
+ * rotated copy per distinct Xq: cq_gemm_grouped_workspace_bytes(probs, count, M). */
+size_t cq_gemm_grouped_workspace_bytes(const cq_gemm_problem* probs, int count, int64_t M);
+cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, int64_t M, int g, int b,
+                          const cq_codebook* cbk, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Reports (and clears) the device error flag raised by a bounded wait that timed out in
+ * a GEMM launch on the current device: CQ_ERR_DEVICE_TIMEOUT if raised, else CQ_OK.
+ * Synchronises `stream`. */
+cq_status cq_device_error(void* stream);
+
 /* ---- cq_gemv without a workspace (the paper has no counterpart to this entry point:
  * it is a library convenience).  Same computation, arguments and errors as cq_gemv, minus the
  * workspace, for callers that may not allocate device memory - typically code running

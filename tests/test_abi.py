@@ -97,3 +97,25 @@ def test_codebook_fit_validation(lib):
     assert lib.cq_codebook_fit(A, 100, 1, 10, A, None) == 1
     assert lib.cq_codebook_fit(A, 100, 17, 10, A, None) == 1
     assert lib.cq_codebook_fit(None, 100, 4, 10, A, None) == 1
+
+
+def test_gemm_validation(lib):
+    INV, ALN, UNS, WS = 1, 2, 3, 6
+    f = lib.cq_gemm
+    big = 1 << 30
+    assert f(A, A, 256, 512, 128, 3, _cb(), A, A, 256, A, A, big, None) == UNS   # only b = 4
+    assert f(A, A, 250, 512, 128, 4, _cb(), A, A, 256, A, A, big, None) == INV   # N % 16
+    assert f(A, A, 256, 500, 128, 4, _cb(), A, A, 256, A, A, big, None) == INV   # K % 128
+    assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 0, A, A, big, None) == INV     # M = 0
+    assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 256, M, A, big, None) == ALN
+    assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 256, A, A, 100, None) == WS
+    assert cq.cq_gemm_workspace_bytes(300, 512) == (300 * 512 * 2 + 255) // 256 * 256
+    # grouped: problems sharing an activation count it once
+    probs = (cq.cq_gemm_problem * 3)()
+    for i, (n, k, x) in enumerate([(256, 512, A), (128, 512, A), (512, 1536, A + 4096)]):
+        probs[i].packed, probs[i].norms, probs[i].N, probs[i].K = A, A, n, k
+        probs[i].Xq, probs[i].scale, probs[i].Y = x, A, A
+    assert lib.cq_gemm_grouped_workspace_bytes(probs, 3, 512) == 512 * 512 * 2 + 512 * 1536 * 2
+    assert lib.cq_gemm_grouped(probs, 3, 512, 128, 4, _cb(), A, 1000, None) == WS
+    probs[1].K = 1024   # same Xq with a different K is rejected
+    assert lib.cq_gemm_grouped(probs, 3, 512, 128, 4, _cb(), A, big, None) == INV
