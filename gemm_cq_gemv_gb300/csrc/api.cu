@@ -40,3 +40,27 @@ extern "C" const char* cq_status_string(cq_status s) {
 extern "C" int cq_last_cuda_error(void) { return cq::g_last_cuda_error; }
 
 extern "C" int cq_abi_version(void) { return CQGEMV_ABI_VERSION; }
+
+extern "C" cq_status cq_device_error(void* stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { cq::set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+    unsigned int* words[2] = {cq::gemm_error_word(dev), cq::gemv_error_word(dev)};
+    cudaStream_t cs = cq::as_stream(stream);
+    bool raised = false;
+    for (unsigned int* w : words) {
+        if (!w) continue;   // no kernel of that unit launched on this device yet
+        unsigned int host = 0;
+        e = cudaMemcpyAsync(&host, w, sizeof(host), cudaMemcpyDeviceToHost, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+        if (e != cudaSuccess) { cq::set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+        if (host) {
+            raised = true;
+            const unsigned int zero = 0;
+            e = cudaMemcpyAsync(w, &zero, sizeof(zero), cudaMemcpyHostToDevice, cs);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+            if (e != cudaSuccess) { cq::set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+        }
+    }
+    return raised ? CQ_ERR_DEVICE_TIMEOUT : CQ_OK;
+}

@@ -30,6 +30,12 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Device error words raised by bounded waits (one file-scope __device__ word per
+// translation unit); each returns the cached device address for `dev`, or nullptr if
+// no kernel of that unit has been set up on it yet.
+unsigned int* gemm_error_word(int dev);
+unsigned int* gemv_error_word(int dev);
+
 // float64 -> IEEE binary16 bits, one round-to-nearest-even step (ties to even),
 // written from the binary16 definition: 1 sign bit, 5 exponent bits (bias 15),
 // 10 fraction bits, subnormals with unit 2^-24, overflow to infinity.

@@ -573,6 +573,13 @@ void fill_levels(float (&lv)[16], int b, const cq_codebook* cbk) {
 }
 
 }  // namespace
+
+unsigned int* gemm_error_word(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    return g_err_ptr[dev];
+}
+
 }  // namespace cq
 
 using namespace cq;
@@ -718,23 +725,3 @@ extern "C" cq_status cq_gemm(const uint8_t* packed, const uint16_t* norms, int64
     return cq_gemm_grouped(&q, 1, M, g, b, cbk, workspace, workspace_bytes, stream);
 }
 
-extern "C" cq_status cq_device_error(void* stream) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
-    unsigned int* err = nullptr;
-    if (dev >= 0 && dev < 64) err = g_err_ptr[dev];
-    if (!err) return CQ_OK;   // no GEMM launched on this device yet
-    unsigned int host = 0;
-    cudaStream_t cs = as_stream(stream);
-    e = cudaMemcpyAsync(&host, err, sizeof(host), cudaMemcpyDeviceToHost, cs);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
-    if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
-    if (host) {
-        const unsigned int zero = 0;
-        e = cudaMemcpyAsync(err, &zero, sizeof(zero), cudaMemcpyHostToDevice, cs);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
-        return CQ_ERR_DEVICE_TIMEOUT;
-    }
-    return CQ_OK;
-}

@@ -76,7 +76,124 @@ __device__ __forceinline__ float reduce_rows8(const float (&a)[kRows], int lane)
 }
 
 // ---------------------------------------------------------------------------------
+// Shared pieces of the two GEMV kernels.
+//
+// One CTA of 16 warps per SM, persistent over row tiles.  Warp w owns K-segment slots
+// (w mod nsl) - plus slot + 16 when K has more than 16 segments - so its activation
+// slice is loaded into registers once per kernel; when K has fewer segments than warps
+// the warps sharing a segment split the tile into row groups of 8.  Every tile therefore
+// needs a cross-warp sum: each warp drops its per-row partials into one of kSlots
+// shared slots and arrives on the slot's mbarrier; the warp whose turn it is (tile
+// index mod 16) waits for all 16 arrivals, adds the partials in warp order
+// (deterministic) and frees the slot.  No CTA-wide barrier stalls the streaming warps.
+// ---------------------------------------------------------------------------------
+constexpr int kWarps2 = 16;
+constexpr int kSlots = 4;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b))
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     smem_u32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait (2 s): on expiry raise the device error flag and give up (the result of
+// the call is then undefined and cq_device_error() reports the timeout).
+__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err) {
+    if (mbar_try(b, parity)) return;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(b, parity)) return;
+        if ((i & 255u) == 0u && global_ns() - t0 > 2000000000ull) {
+            atomicOr(err, 2u);
+            return;
+        }
+    }
+}
+
+struct Reduce {
+    float* part;        // [kSlots][16][TB][8]
+    uint64_t* full;     // [kSlots]
+    uint64_t* empty;    // [kSlots]
+};
+
+// Stores this warp's row partials of tile number `it` and, on its turn, reduces the tile.
+// `fin(t, rr, sum)` receives the sum for token t of tile row rr.
+template <int TB, typename Fin>
+__device__ __forceinline__ void tile_reduce(const Reduce& rd, const float (&acc)[TB][kRows], int it,
+                                            int w, int lane, int nsl, int tile_rows, int ntok,
+                                            unsigned int* err, Fin fin) {
+    const int slot = it % kSlots;
+    const uint32_t ph = (uint32_t)((it / kSlots) & 1);
+    float v[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) v[t] = reduce_rows8(acc[t], lane);
+    mbar_wait(&rd.empty[slot], ph ^ 1u, err);
+    if ((lane & 3) == 0) {
+#pragma unroll
+        for (int t = 0; t < TB; ++t)
+            rd.part[((slot * kWarps2 + w) * TB + t) * kRows + ((lane >> 2) & 7)] = v[t];
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rd.full[slot]);
+    if (w == it % kWarps2) {
+        mbar_wait(&rd.full[slot], ph, err);
+        for (int idx = lane; idx < TB * tile_rows; idx += 32) {
+            const int t = idx / tile_rows, rr = idx % tile_rows;
+            const int g = rr / kRows, r = rr % kRows;
+            if (t < ntok) {
+                float sum = 0.0f;
+                for (int ss = 0; ss < nsl; ++ss)
+                    sum += rd.part[((slot * kWarps2 + g * nsl + ss) * TB + t) * kRows + r];
+                fin(t, rr, sum);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rd.empty[slot]);
+    }
+}
+
+__device__ __forceinline__ void init_reduce_bars(const Reduce& rd) {
+    for (int s = 0; s < kSlots; ++s) {
+        mbar_init(&rd.full[s], kWarps2);
+        mbar_init(&rd.empty[s], 1);
+    }
+}
+
+constexpr size_t reduce_bytes(int tb) {
+    return (size_t)kSlots * kWarps2 * tb * kRows * sizeof(float) + 2 * kSlots * sizeof(uint64_t);
+}
+
+// ---------------------------------------------------------------------------------
 // A5: CQ GEMV.  Y[t][o] = s_t / 128 * sum_j norm[o][j] * sum_i cb[idx] * xr[t][128 j + i]
+// Codewords come from a shared-memory table indexed by two consecutive indices (2b
+// bits): entry e = (cb[e mod 2^b], cb[e / 2^b]), replicated once per bank so every lane
+// reads its own copy (conflict-free 64-bit loads); the pair multiplies a pair of
+// activations with one packed fp32x2 FMA.  The packed rows of the next tile are
+// prefetched into L2 while the current one is decoded.
 // ---------------------------------------------------------------------------------
 struct CqGemvParams {
     const uint8_t* packed;
@@ -84,21 +201,24 @@ struct CqGemvParams {
     const float* xr;      // [B][K] rotated activations
     const float* scale;   // [B]
     float* Y;             // [B][N]
+    unsigned int* err;    // device error flag
     int64_t N;
     int K;
     int nseg;             // ceil(K / 1024)
+    int rg;               // row groups per tile
     int t0;               // first token of this pass
     int ntok;             // tokens in this pass (<= TB)
     float lv[16];
 };
 
-template <int BITS>
-__device__ __forceinline__ uint32_t extract_idx(const uint32_t (&w)[BITS], int i) {
-    const int pos = BITS * i;
+template <int NB>
+__device__ __forceinline__ uint32_t extract_bits(const uint32_t* w, int p) {
+    // bits [NB p, NB p + NB) of the little-endian word string w
+    const int pos = NB * p;
     const int wi = pos >> 5, sh = pos & 31;
     uint32_t v = w[wi] >> sh;
-    if (sh + BITS > 32) v |= w[wi + 1] << (32 - sh);
-    return v & ((1u << BITS) - 1u);
+    if (sh + NB > 32) v |= w[wi + 1] << (32 - sh);
+    return v & ((1u << NB) - 1u);
 }
 
 template <int BITS>
@@ -115,272 +235,432 @@ __device__ __forceinline__ void load_packed(uint32_t (&w)[BITS], const uint8_t* 
     }
 }
 
-template <int BITS, int TB>
-__global__ void __launch_bounds__(kThreads) cq_gemv_kernel(const CqGemvParams p) {
-    extern __shared__ __align__(16) float smem[];
-    float* lut = smem;                      // [16][32]: entry t replicated once per bank
-    float* xs = smem + 16 * 32;             // [TB][nseg * 1024], zero padded
-    const int lane = threadIdx.x & 31;
-    const int segK = p.nseg * kSeg;
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+template <int BITS, int TB, int SPW>
+__global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvParams p) {
     constexpr int L = 1 << BITS;
-    for (int i = threadIdx.x; i < 16 * 32; i += kThreads) {
-        const int t = (i >> 5) & (L - 1);
-        float v = 0.0f;
+    constexpr int E = 1 << (2 * BITS);
+    extern __shared__ __align__(16) float2 lut2[];                      // [E][32]
+    Reduce rd;
+    rd.part = reinterpret_cast<float*>(lut2 + E * 32);
+    rd.full = reinterpret_cast<uint64_t*>(rd.part + kSlots * kWarps2 * TB * kRows);
+    rd.empty = rd.full + kSlots;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    for (int i = tid; i < E * 32; i += kWarps2 * 32) {
+        const int e = i >> 5;
+        float a = 0.0f, b = 0.0f;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) v = (u == t) ? p.lv[u] : v;
-        lut[i] = v;
+        for (int u = 0; u < L; ++u) {
+            a = (u == (e & (L - 1))) ? p.lv[u] : a;
+            b = (u == (e >> BITS)) ? p.lv[u] : b;
+        }
+        lut2[i] = make_float2(a, b);
     }
-    for (int i = threadIdx.x; i < TB * segK; i += kThreads) {
-        const int t = i / segK, k = i - t * segK;
-        xs[i] = (t < p.ntok && k < p.K) ? p.xr[(int64_t)(p.t0 + t) * p.K + k] : 0.0f;
+    if (tid == 0) init_reduce_bars(rd);
+    const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
+    const int slot = w % nsl, rgi = w / nsl;
+    const bool busy = rgi < p.rg;
+    float2 xx[SPW][TB][16];
+#pragma unroll
+    for (int i = 0; i < SPW; ++i) {
+        const int seg = slot + i * kWarps2;
+        const int pos0 = seg * kSeg + lane * 32;
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            const bool ok = busy && seg < p.nseg && pos0 < p.K && t < p.ntok;
+            const float* src = p.xr + (int64_t)(p.t0 + t) * p.K + pos0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = ok ? *reinterpret_cast<const float4*>(src + 4 * q)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                xx[i][t][2 * q] = make_float2(v.x, v.y);
+                xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
+            }
+        }
     }
     __syncthreads();
 
     const int G = p.K / kGroup;
     const int64_t rowbytes = (int64_t)G * 16 * BITS;
-    const int64_t ntiles = (p.N + kRows - 1) / kRows;
-    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-    const float* mylut = lut + lane;
-
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
-        const int64_t row0 = tile * kRows;
+    const int tile_rows = kRows * p.rg;
+    const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
+    const float2* mylut = lut2 + lane;
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
+        // L2 prefetch of this warp's rows of the next tile (one lane per row and segment)
+        if (busy && lane < kRows * SPW) {
+            const int r = lane % kRows, i = lane / kRows;
+            const int seg = slot + i * kWarps2;
+            const int64_t nrow = row0 + (int64_t)gridDim.x * tile_rows + r;
+            if (seg < p.nseg && nrow < p.N) {
+                const int bytes = min(128 * BITS, (int)((p.K - seg * kSeg) / 8 * BITS));
+                prefetch_l2(p.packed + nrow * rowbytes + (int64_t)seg * (128 * BITS), (uint32_t)bytes);
+            }
+        }
         float acc[TB][kRows];
 #pragma unroll
         for (int t = 0; t < TB; ++t)
 #pragma unroll
             for (int r = 0; r < kRows; ++r) acc[t][r] = 0.0f;
-
-        for (int seg = 0; seg < p.nseg; ++seg) {
-            const int pos0 = seg * kSeg + lane * 32;
-            const bool active = pos0 < p.K;
-            uint32_t w[kRows][BITS];
-            float nrm[kRows];
+        if (busy) {
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-                const int64_t row = row0 + r;
-                if (active && row < p.N) {
-                    load_packed<BITS>(w[r], p.packed + row * rowbytes +
-                                                (int64_t)seg * (128 * BITS) + lane * (4 * BITS));
-                    nrm[r] = f16_bits_to_f32(__ldg(p.norms + row * G + seg * 8 + (lane >> 2)));
-                } else {
+            for (int i = 0; i < SPW; ++i) {
+                const int seg = slot + i * kWarps2;
+                if (seg >= p.nseg) break;
+                const bool active = seg * kSeg + lane * 32 < p.K;
+                uint32_t wd[kRows][BITS];
+                float nrm[kRows];
 #pragma unroll
-                    for (int k = 0; k < BITS; ++k) w[r][k] = 0u;
-                    nrm[r] = 0.0f;
-                }
-            }
-            float x[TB][32];
+                for (int r = 0; r < kRows; ++r) {
+                    const int64_t row = row0 + r;
+                    if (active && row < p.N) {
+                        load_packed<BITS>(wd[r], p.packed + row * rowbytes +
+                                                     (int64_t)seg * (128 * BITS) + lane * (4 * BITS));
+                        nrm[r] = f16_bits_to_f32(__ldg(p.norms + row * G + seg * 8 + (lane >> 2)));
+                    } else {
 #pragma unroll
-            for (int t = 0; t < TB; ++t)
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(xs + t * segK + pos0 + i);
-                    x[t][i] = v.x; x[t][i + 1] = v.y; x[t][i + 2] = v.z; x[t][i + 3] = v.w;
+                        for (int k = 0; k < BITS; ++k) wd[r][k] = 0u;
+                        nrm[r] = 0.0f;
+                    }
                 }
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-                float dot[TB];
+                for (int r = 0; r < kRows; ++r) {
+                    float2 d2[TB];
 #pragma unroll
-                for (int t = 0; t < TB; ++t) dot[t] = 0.0f;
+                    for (int t = 0; t < TB; ++t) d2[t] = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float cw = mylut[extract_idx<BITS>(w[r], i) << 5];
+                    for (int q = 0; q < 16; ++q) {
+                        const float2 c = mylut[extract_bits<2 * BITS>(wd[r], q) << 5];
 #pragma unroll
-                    for (int t = 0; t < TB; ++t) dot[t] = fmaf(cw, x[t][i], dot[t]);
+                        for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][q], d2[t]);
+                    }
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(nrm[r], d2[t].x + d2[t].y, acc[t][r]);
                 }
-#pragma unroll
-                for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(nrm[r], dot[t], acc[t][r]);
             }
         }
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            const float v = reduce_rows8(acc[t], lane);
-            const int64_t row = row0 + ((lane >> 2) & 7);
-            if ((lane & 3) == 0 && t < p.ntok && row < p.N) {
-                const int tok = p.t0 + t;
-                p.Y[(int64_t)tok * p.N + row] = v * (p.scale[tok] * (1.0f / 128.0f));
-            }
-        }
+        tile_reduce<TB>(rd, acc, it, w, lane, nsl, tile_rows, p.ntok, p.err,
+                        [&](int t, int rr, float sum) {
+                            const int64_t row = tile * tile_rows + rr;
+                            if (row < p.N) {
+                                const int tok = p.t0 + t;
+                                p.Y[(int64_t)tok * p.N + row] = sum * (p.scale[tok] * (1.0f / 128.0f));
+                            }
+                        });
     }
 }
 
 // ---------------------------------------------------------------------------------
-// A8: Q4_0 GEMV.  Lane l of a segment owns block (32 seg + l) of every row; the 18-byte
-// blocks of a row segment are staged through shared memory with 16-byte loads.
+// A8: Q4_0 GEMV.  Same persistent layout; lane l of a segment owns block 32 seg + l of
+// every row.  The 18-byte blocks of a row segment are staged in the warp's shared
+// buffer - by double-buffered bulk copies (cp.async.bulk, one per row) when rows and
+// segments are 16-byte aligned, else by guarded 16-byte loads - and each lane reads its
+// block with five aligned 32-bit loads.  A nibble pair is decoded without a table: moved
+// into the mantissa of 256.0f (low nibble) and 16.0f (high nibble), giving exactly
+// 256 + lo and 16 + hi, multiplied by the activation pair with one fp32x2 FMA; the
+// constant offsets (and the -8 of the format) are removed per block with a precomputed
+// sum of the activations.
 // ---------------------------------------------------------------------------------
 struct Q40GemvParams {
     const uint8_t* blocks;
     const float* X;       // [B][K]
     float* Y;             // [B][N]
+    unsigned int* err;
     int64_t N;
     int K;
     int nblk;             // ceil(K / 32)
     int nseg;             // ceil(nblk / 32)
+    int rg;
     int64_t total_bytes;  // N * nblk * 18
-    int t0, ntok, B;
+    int t0, ntok;
 };
 
-constexpr int kStage = 608;  // >= 37 chunks of 16 B, per row, per warp
+constexpr int kStage = 608;  // >= 37 chunks of 16 B, per row
 
 template <int TB>
-__global__ void __launch_bounds__(kThreads) q4_0_gemv_kernel(const Q40GemvParams p) {
-    extern __shared__ __align__(16) float smem[];
-    const int segK = p.nseg * kSeg;
-    float* xs = smem;                                                      // [TB][segK]
-    uint8_t* stage = reinterpret_cast<uint8_t*>(smem + TB * segK);         // [8 warps][kRows][kStage]
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < TB * segK; i += kThreads) {
-        const int t = i / segK, k = i - t * segK;
-        xs[i] = (t < p.ntok && k < p.K) ? p.X[(int64_t)(p.t0 + t) * p.K + k] : 0.0f;
+__device__ __forceinline__ void q4_block(const uint8_t* rowbuf, int o, const float2 (&xx)[TB][16],
+                                         const float (&cblk)[TB], float (&accr)[TB]) {
+    // the block starts at byte o (even) of the staged row; read the aligned words
+    // covering it and shift the nibble bytes into place
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowbuf + (o & ~3));
+    const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2], w3 = wp[3], w4 = wp[4];
+    const uint32_t sh = (uint32_t)(o & 3) * 8u;          // 0 or 16
+    const uint32_t dbits = (sh == 0u) ? (w0 & 0xFFFFu) : (w0 >> 16);
+    const float d = f16_bits_to_f32((uint16_t)dbits);
+    const uint32_t nw[4] = {__funnelshift_rc(w0, w1, sh + 16u), __funnelshift_rc(w1, w2, sh + 16u),
+                            __funnelshift_rc(w2, w3, sh + 16u), __funnelshift_rc(w3, w4, sh + 16u)};
+    float2 s2[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) s2[t] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // byte j of the word to bits 15..22
+            const uint32_t tb = (j == 0) ? (nw[k] << 15) : (j == 1) ? (nw[k] << 7)
+                              : (j == 2) ? (nw[k] >> 1) : (nw[k] >> 9);
+            const float2 f = make_float2(__uint_as_float((tb & 0x00078000u) | 0x43800000u),
+                                         __uint_as_float((tb & 0x00780000u) | 0x41800000u));
+#pragma unroll
+            for (int t = 0; t < TB; ++t) s2[t] = __ffma2_rn(f, xx[t][4 * k + j], s2[t]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TB; ++t) accr[t] = fmaf(d, (s2[t].x + s2[t].y) - cblk[t], accr[t]);
+}
+
+template <int TB, int SPW, bool BULK>
+__global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_kernel(const Q40GemvParams p) {
+    extern __shared__ __align__(16) uint8_t smem_q[];
+    constexpr int kBufs = BULK ? 2 : 1;
+    uint8_t* stage = smem_q;                                              // [16][kBufs][8][608]
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kBufs * kRows * kStage);  // [16][2]
+    Reduce rd;
+    rd.part = reinterpret_cast<float*>(tma_bar + 2 * kWarps2);
+    rd.full = reinterpret_cast<uint64_t*>(rd.part + kSlots * kWarps2 * TB * kRows);
+    rd.empty = rd.full + kSlots;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) {
+        init_reduce_bars(rd);
+        for (int i = 0; i < 2 * kWarps2; ++i) mbar_init(&tma_bar[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
+    const int slot = w % nsl, rgi = w / nsl;
+    const bool busy = rgi < p.rg;
+    float2 xx[SPW][TB][16];
+    float cblk[SPW][TB];
+#pragma unroll
+    for (int i = 0; i < SPW; ++i) {
+        const int seg = slot + i * kWarps2;
+        const int blk = seg * 32 + lane;
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            const bool ok = busy && seg < p.nseg && blk < p.nblk && t < p.ntok;
+            const float* src = p.X + (int64_t)(p.t0 + t) * p.K;
+            float se = 0.0f, so = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int k0 = blk * 32 + 2 * q;
+                const float a = (ok && k0 < p.K) ? src[k0] : 0.0f;
+                const float b = (ok && k0 + 1 < p.K) ? src[k0 + 1] : 0.0f;
+                xx[i][t][q] = make_float2(a, b);
+                se += a;
+                so += b;
+            }
+            cblk[i][t] = 264.0f * se + 24.0f * so;
+        }
     }
     __syncthreads();
-    uint8_t* mystage = stage + wid * (kRows * kStage);
+
+    uint8_t* mystage = stage + w * (kBufs * kRows * kStage);
+    uint64_t* mybar = tma_bar + 2 * w;
     const int64_t rowbytes = (int64_t)p.nblk * 18;
-    const int64_t ntiles = (p.N + kRows - 1) / kRows;
-    const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int tile_rows = kRows * p.rg;
+    const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
     const uintptr_t base_addr = reinterpret_cast<uintptr_t>(p.blocks);
     const uintptr_t end_addr = base_addr + (uintptr_t)p.total_bytes;
 
-    for (int64_t tile = warp; tile < ntiles; tile += nwarps) {
-        const int64_t row0 = tile * kRows;
+    // bulk staging: unit u = (tile number, owned segment i) in order; buffer u % 2
+    auto issue_bulk = [&](int64_t tile, int i, int bufi) {
+        const int seg = slot + i * kWarps2;
+        const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
+        const int nb = min(32, p.nblk - seg * 32);
+        int nrows = 0;
+        for (int r = 0; r < kRows; ++r) nrows += (row0 + r < p.N) ? 1 : 0;
+        if (lane == 0) mbar_arrive_tx(&mybar[bufi], (uint32_t)(nrows * nb * 18));
+        __syncwarp();
+        if (lane < nrows) {
+            const uint8_t* src = p.blocks + (row0 + lane) * rowbytes + (int64_t)seg * 576;
+            uint8_t* dst = mystage + (bufi * kRows + lane) * kStage;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(dst)),
+                "l"(src), "r"((uint32_t)(nb * 18)), "r"(smem_u32(&mybar[bufi]))
+                : "memory");
+        }
+    };
+    int units_total = 0;   // per-warp count of bulk units issued (for buffer parity)
+    int it = 0;
+    if (BULK && busy && blockIdx.x < ntiles) {
+        if (slot < p.nseg) { issue_bulk(blockIdx.x, 0, 0); }
+    }
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
         float acc[TB][kRows];
 #pragma unroll
         for (int t = 0; t < TB; ++t)
 #pragma unroll
             for (int r = 0; r < kRows; ++r) acc[t][r] = 0.0f;
-
-        for (int seg = 0; seg < p.nseg; ++seg) {
-            const int nb = min(32, p.nblk - seg * 32);
-            int offs[kRows];
-            __syncwarp();
+        if (busy) {
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) {
-                const int64_t row = row0 + r;
-                offs[r] = 0;
-                if (row >= p.N) continue;
-                const uintptr_t a = base_addr + (uintptr_t)(row * rowbytes + (int64_t)seg * 576);
-                const uintptr_t start = a & ~(uintptr_t)15;
-                offs[r] = (int)(a - start);
-                const int chunks = (int)((a + (uintptr_t)nb * 18 - start + 15) >> 4);
-                for (int c = lane; c < chunks; c += 32) {
-                    const uintptr_t q = start + (uintptr_t)c * 16;
-                    uint4 v;
-                    if (q + 16 <= end_addr) {
-                        v = __ldcs(reinterpret_cast<const uint4*>(q));
-                    } else {
-                        uint8_t tmp[16];
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            tmp[k] = (q + k < end_addr) ? *reinterpret_cast<const uint8_t*>(q + k) : 0;
-                        v = make_uint4(tmp[0] | tmp[1] << 8 | tmp[2] << 16 | (uint32_t)tmp[3] << 24,
-                                       tmp[4] | tmp[5] << 8 | tmp[6] << 16 | (uint32_t)tmp[7] << 24,
-                                       tmp[8] | tmp[9] << 8 | tmp[10] << 16 | (uint32_t)tmp[11] << 24,
-                                       tmp[12] | tmp[13] << 8 | tmp[14] << 16 | (uint32_t)tmp[15] << 24);
+            for (int i = 0; i < SPW; ++i) {
+                const int seg = slot + i * kWarps2;
+                if (seg >= p.nseg) break;
+                const int nb = min(32, p.nblk - seg * 32);
+                const uint8_t* rowbufs;
+                int offs[kRows];
+                if constexpr (BULK) {
+                    const int bufi = units_total & 1;
+                    const uint32_t par = (uint32_t)((units_total >> 1) & 1);
+                    // issue the next unit into the other buffer before waiting for this one
+                    {
+                        int ni = i + 1;
+                        int64_t nt = tile;
+                        if (ni >= SPW || slot + ni * kWarps2 >= p.nseg) { ni = 0; nt = tile + gridDim.x; }
+                        __syncwarp();
+                        if (nt < ntiles) issue_bulk(nt, ni, bufi ^ 1);
                     }
-                    *reinterpret_cast<uint4*>(mystage + r * kStage + c * 16) = v;
-                }
-            }
-            __syncwarp();
-            if (lane < nb) {
-                const int pos0 = seg * kSeg + lane * 32;
-                float x[TB][32];
+                    mbar_wait(&mybar[bufi], par, p.err);
+                    rowbufs = mystage + bufi * kRows * kStage;
 #pragma unroll
-                for (int t = 0; t < TB; ++t)
+                    for (int r = 0; r < kRows; ++r) offs[r] = 0;
+                    ++units_total;
+                } else {
+                    __syncwarp();
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(xs + t * segK + pos0 + i);
-                        x[t][i] = v.x; x[t][i + 1] = v.y; x[t][i + 2] = v.z; x[t][i + 3] = v.w;
-                    }
+                    for (int r = 0; r < kRows; ++r) {
+                        const int64_t row = row0 + r;
+                        offs[r] = 0;
+                        if (row >= p.N) continue;
+                        const uintptr_t a = base_addr + (uintptr_t)(row * rowbytes + (int64_t)seg * 576);
+                        const uintptr_t start = a & ~(uintptr_t)15;
+                        offs[r] = (int)(a - start);
+                        const int chunks = (int)((a + (uintptr_t)nb * 18 - start + 15) >> 4);
+                        for (int c = lane; c < chunks; c += 32) {
+                            const uintptr_t q = start + (uintptr_t)c * 16;
+                            uint4 v;
+                            if (q + 16 <= end_addr) {
+                                v = __ldcs(reinterpret_cast<const uint4*>(q));
+                            } else {
+                                uint8_t tmp[16];
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    if (row0 + r >= p.N) continue;
-                    const uint8_t* blk = mystage + r * kStage + offs[r] + lane * 18;
-                    const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
-                    const float d = f16_bits_to_f32(h[0]);
-                    float s[TB];
-#pragma unroll
-                    for (int t = 0; t < TB; ++t) s[t] = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t two = h[1 + k];   // bytes 2k, 2k+1 -> 4 nibbles
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t nib = (two >> (4 * j)) & 15u;
-                            // (nib - 8) exactly: 2^23 + nib as a float, minus 2^23 + 8
-                            const float wv = __uint_as_float(0x4B000000u | nib) - 8388616.0f;
-#pragma unroll
-                            for (int t = 0; t < TB; ++t) s[t] = fmaf(wv, x[t][4 * k + j], s[t]);
+                                for (int k = 0; k < 16; ++k)
+                                    tmp[k] = (q + k < end_addr) ? *reinterpret_cast<const uint8_t*>(q + k) : 0;
+                                v = make_uint4(tmp[0] | tmp[1] << 8 | tmp[2] << 16 | (uint32_t)tmp[3] << 24,
+                                               tmp[4] | tmp[5] << 8 | tmp[6] << 16 | (uint32_t)tmp[7] << 24,
+                                               tmp[8] | tmp[9] << 8 | tmp[10] << 16 | (uint32_t)tmp[11] << 24,
+                                               tmp[12] | tmp[13] << 8 | tmp[14] << 16 | (uint32_t)tmp[15] << 24);
+                            }
+                            *reinterpret_cast<uint4*>(mystage + r * kStage + c * 16) = v;
                         }
                     }
+                    __syncwarp();
+                    rowbufs = mystage;
+                }
+                if (lane < nb) {
+                    float accr[TB];
 #pragma unroll
-                    for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(d, s[t], acc[t][r]);
+                    for (int r = 0; r < kRows; ++r) {
+                        if (row0 + r >= p.N) continue;
+#pragma unroll
+                        for (int t = 0; t < TB; ++t) accr[t] = acc[t][r];
+                        q4_block<TB>(rowbufs + r * kStage, offs[r] + lane * 18, xx[i], cblk[i], accr);
+#pragma unroll
+                        for (int t = 0; t < TB; ++t) acc[t][r] = accr[t];
+                    }
                 }
             }
         }
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            const float v = reduce_rows8(acc[t], lane);
-            const int64_t row = row0 + ((lane >> 2) & 7);
-            if ((lane & 3) == 0 && t < p.ntok && row < p.N)
-                p.Y[(int64_t)(p.t0 + t) * p.N + row] = v;
-        }
+        tile_reduce<TB>(rd, acc, it, w, lane, nsl, tile_rows, p.ntok, p.err,
+                        [&](int t, int rr, float sum) {
+                            const int64_t row = tile * tile_rows + rr;
+                            if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
+                        });
     }
-}
-
-// Persistent grid: as many CTAs as fit, capped by the number of warp tiles.
-int grid_for(const void* kern, size_t smem, int64_t ntiles) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
-        per_sm < 1)
-        return -1;
-    int64_t want = (ntiles + (kThreads / 32) - 1) / (kThreads / 32);
-    int64_t grid = (int64_t)per_sm * sm_count();
-    if (want < grid) grid = want;
-    return (int)(grid < 1 ? 1 : grid);
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
-template <int BITS, int TB>
-cq_status run_cq_gemv(CqGemvParams p, cudaStream_t st) {
-    static bool attr = false;
-    auto kern = cq_gemv_kernel<BITS, TB>;
-    const size_t smem = (size_t)(16 * 32 + TB * p.nseg * kSeg) * sizeof(float);
-    if (smem > kMaxSmem) return CQ_ERR_UNSUPPORTED;
-    if (!attr) {
+static __device__ unsigned int g_gemv_err;
+std::mutex g_err_mu;
+unsigned int* g_gemv_err_ptr[64] = {nullptr};
+
+// Cached device address of this unit's error word on the current device.
+cq_status device_error_word(unsigned int** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+    if (dev < 0 || dev >= 64) return CQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_err_mu);
+    if (!g_gemv_err_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_gemv_err);
+        if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+        g_gemv_err_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_gemv_err_ptr[dev];
+    return CQ_OK;
+}
+
+template <typename Kern>
+cq_status launch_once(Kern kern, size_t smem, int64_t ntiles, cudaStream_t st, bool* attr,
+                      int* grid_out) {
+    if (!*attr) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=
             cudaSuccess)
             return check_launch();
-        attr = true;
+        *attr = true;
     }
-    const int64_t ntiles = (p.N + kRows - 1) / kRows;
-    const int grid = grid_for((const void*)kern, smem, ntiles);
-    if (grid < 0) return check_launch() == CQ_OK ? CQ_ERR_UNSUPPORTED : CQ_ERR_CUDA;
-    kern<<<grid, kThreads, smem, st>>>(p);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps2 * 32, smem) != cudaSuccess)
+        return check_launch();
+    if (per_sm < 1) return CQ_ERR_UNSUPPORTED;
+    int64_t grid = (int64_t)per_sm * sm_count();
+    if (ntiles < grid) grid = ntiles;
+    *grid_out = (int)(grid < 1 ? 1 : grid);
+    return CQ_OK;
+}
+
+// segment ownership: row groups when K has fewer segments than warps
+inline int row_groups(int nseg) { return nseg >= kWarps2 ? 1 : kWarps2 / nseg; }
+
+template <int BITS, int TB, int SPW>
+cq_status run_cq_gemv(CqGemvParams p, cudaStream_t st) {
+    static bool attr = false;
+    auto kern = cq_gemv_kernel<BITS, TB, SPW>;
+    const size_t smem = (size_t)(1 << (2 * BITS)) * 32 * sizeof(float2) + reduce_bytes(TB);
+    const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
+    int grid = 0;
+    const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
+    if (s != CQ_OK) return s;
+    kern<<<grid, kWarps2 * 32, smem, st>>>(p);
     return check_launch();
 }
 
-template <int TB>
+template <int TB, int SPW, bool BULK>
 cq_status run_q4_0_gemv(Q40GemvParams p, cudaStream_t st) {
     static bool attr = false;
-    auto kern = q4_0_gemv_kernel<TB>;
-    const size_t smem = (size_t)TB * p.nseg * kSeg * sizeof(float) + (size_t)8 * kRows * kStage;
-    if (smem > kMaxSmem) return CQ_ERR_UNSUPPORTED;
-    if (!attr) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=
-            cudaSuccess)
-            return check_launch();
-        attr = true;
-    }
-    const int64_t ntiles = (p.N + kRows - 1) / kRows;
-    const int grid = grid_for((const void*)kern, smem, ntiles);
-    if (grid < 0) return check_launch() == CQ_OK ? CQ_ERR_UNSUPPORTED : CQ_ERR_CUDA;
-    kern<<<grid, kThreads, smem, st>>>(p);
+    auto kern = q4_0_gemv_kernel<TB, SPW, BULK>;
+    const size_t smem = (size_t)kWarps2 * (BULK ? 2 : 1) * kRows * kStage +
+                        2 * kWarps2 * sizeof(uint64_t) + reduce_bytes(TB);
+    const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
+    int grid = 0;
+    const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
+    if (s != CQ_OK) return s;
+    kern<<<grid, kWarps2 * 32, smem, st>>>(p);
     return check_launch();
+}
+
+template <int BITS>
+cq_status dispatch_cq(CqGemvParams p, int tb, int spw, cudaStream_t st) {
+    if (spw == 2) return run_cq_gemv<BITS, 1, 2>(p, st);
+    if (tb == 2) return run_cq_gemv<BITS, 2, 1>(p, st);
+    return run_cq_gemv<BITS, 1, 1>(p, st);
 }
 
 }  // namespace
+
+unsigned int* gemv_error_word(int dev) {
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(g_err_mu);
+    return g_gemv_err_ptr[dev];
+}
+
 }  // namespace cq
 
 using namespace cq;
@@ -403,6 +683,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         return CQ_ERR_ALIGNMENT;
     if (!workspace || workspace_bytes < cq_gemv_workspace_bytes(B, K)) return CQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return CQ_ERR_ALIGNMENT;
+    if (K > 2 * kWarps2 * kSeg) return CQ_ERR_UNSUPPORTED;   // at most 2 segments per warp
     cudaStream_t st = as_stream(stream);
     float* xr = reinterpret_cast<float*>(workspace);
     const int64_t groups = B * (K / kGroup);
@@ -415,6 +696,12 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         if (s != CQ_OK) return s;
     }
     CqGemvParams p;
+    {
+        unsigned int* err = nullptr;
+        const cq_status se = device_error_word(&err);
+        if (se != CQ_OK) return se;
+        p.err = err;
+    }
     p.packed = packed; p.norms = norms; p.xr = xr; p.scale = scale; p.Y = Y;
     p.N = N; p.K = (int)K; p.nseg = (int)((K + kSeg - 1) / kSeg);
     for (int t = 0; t < 16; ++t) p.lv[t] = 0.0f;
@@ -425,26 +712,20 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
         for (int t = 0; t < (1 << b); ++t) p.lv[t] = cbk->cb[off + t];
     }
-    // tokens per pass: 2 when the activations of two tokens fit in shared memory
-    const int tb = ((size_t)2 * p.nseg * kSeg * sizeof(float) + 2048 <= kMaxSmem && B > 1) ? 2 : 1;
+    // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
+    // tokens per pass when each warp owns a single segment
+    const int spw = (p.nseg + kWarps2 - 1) / kWarps2;
+    p.rg = row_groups(p.nseg);
+    const int tb = (spw == 1 && B > 1) ? 2 : 1;
     for (int64_t t0 = 0; t0 < B; t0 += tb) {
         p.t0 = (int)t0;
         p.ntok = (int)((B - t0) < tb ? (B - t0) : tb);
         cq_status s;
-        if (tb == 2) {
-            switch (b) {
-                case 1: s = run_cq_gemv<1, 2>(p, st); break;
-                case 2: s = run_cq_gemv<2, 2>(p, st); break;
-                case 3: s = run_cq_gemv<3, 2>(p, st); break;
-                default: s = run_cq_gemv<4, 2>(p, st); break;
-            }
-        } else {
-            switch (b) {
-                case 1: s = run_cq_gemv<1, 1>(p, st); break;
-                case 2: s = run_cq_gemv<2, 1>(p, st); break;
-                case 3: s = run_cq_gemv<3, 1>(p, st); break;
-                default: s = run_cq_gemv<4, 1>(p, st); break;
-            }
+        switch (b) {
+            case 1: s = dispatch_cq<1>(p, tb, spw, st); break;
+            case 2: s = dispatch_cq<2>(p, tb, spw, st); break;
+            case 3: s = dispatch_cq<3>(p, tb, spw, st); break;
+            default: s = dispatch_cq<4>(p, tb, spw, st); break;
         }
         if (s != CQ_OK) return s;
     }
@@ -454,21 +735,36 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
 extern "C" cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X,
                                int64_t B, float* Y, void* stream) {
     if (!blocks || !X || !Y || N < 1 || K < 1 || B < 1) return CQ_ERR_INVALID_ARG;
-    if (K > (1 << 24) || N > ((int64_t)1 << 40)) return CQ_ERR_UNSUPPORTED;
+    if (K > 2 * kWarps2 * kSeg || N > ((int64_t)1 << 40)) return CQ_ERR_UNSUPPORTED;
     if (!aligned16(blocks) || !aligned16(X) || !aligned16(Y)) return CQ_ERR_ALIGNMENT;
     Q40GemvParams p;
     p.blocks = blocks; p.X = X; p.Y = Y; p.N = N; p.K = (int)K;
     p.nblk = (int)((K + 31) / 32);
     p.nseg = (p.nblk + 31) / 32;
     p.total_bytes = N * (int64_t)p.nblk * 18;
-    p.B = (int)B;
     cudaStream_t st = as_stream(stream);
-    const size_t stage = (size_t)8 * kRows * kStage;
-    const int tb = ((size_t)2 * p.nseg * kSeg * sizeof(float) + stage <= kMaxSmem && B > 1) ? 2 : 1;
+    unsigned int* err = nullptr;
+    {
+        const cq_status se = device_error_word(&err);
+        if (se != CQ_OK) return se;
+    }
+    p.err = err;
+    // bulk-copy staging needs 16-byte aligned row segments: 8 | nblk
+    const bool bulk = (p.nblk % 8) == 0;
+    const int spw = (p.nseg + kWarps2 - 1) / kWarps2;
+    p.rg = row_groups(p.nseg);
+    const int tb = (spw == 1 && B > 1) ? 2 : 1;
     for (int64_t t0 = 0; t0 < B; t0 += tb) {
         p.t0 = (int)t0;
         p.ntok = (int)((B - t0) < tb ? (B - t0) : tb);
-        const cq_status s = (tb == 2) ? run_q4_0_gemv<2>(p, st) : run_q4_0_gemv<1>(p, st);
+        cq_status s;
+        if (bulk) {
+            s = (spw == 2) ? run_q4_0_gemv<1, 2, true>(p, st)
+              : (tb == 2) ? run_q4_0_gemv<2, 1, true>(p, st) : run_q4_0_gemv<1, 1, true>(p, st);
+        } else {
+            s = (spw == 2) ? run_q4_0_gemv<1, 2, false>(p, st)
+              : (tb == 2) ? run_q4_0_gemv<2, 1, false>(p, st) : run_q4_0_gemv<1, 1, false>(p, st);
+        }
         if (s != CQ_OK) return s;
     }
     return CQ_OK;

@@ -25,8 +25,7 @@
  *  - Arguments are validated before anything is launched; a failed check returns an
  *    error status and launches nothing.
  *  - Row-major layouts; sizes are element counts unless named *_bytes.
- *  - Pointers must be 16-byte aligned (CQ_ERR_ALIGNMENT otherwise), except the
- *    Q4_0 block array, which needs no alignment.
+ *  - Pointers must be 16-byte aligned (CQ_ERR_ALIGNMENT otherwise).
  *  - CQ_ERR_CUDA means a CUDA runtime call or launch failed; cq_last_cuda_error()
  *    returns its cudaError_t code.
  */
@@ -115,7 +114,9 @@ cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* Xq, float* s
  *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
  *   Y  [B][N] float32
  *   workspace      device scratch of at least cq_gemv_workspace_bytes(B, K) bytes
- * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, CUDA. */
+ * K is limited to 32768 (CQ_ERR_UNSUPPORTED above).  Deterministic: the same inputs give
+ * bit-identical outputs.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
 size_t cq_gemv_workspace_bytes(int64_t B, int64_t K);
 cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
                   int g, int b, const cq_codebook* cbk, const int8_t* Xq,
@@ -160,9 +161,9 @@ cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, int64_t M, in
                           const cq_codebook* cbk, void* workspace, size_t workspace_bytes,
                           void* stream);
 
-/* Reports (and clears) the device error flag raised by a bounded wait that timed out in
- * a GEMM launch on the current device: CQ_ERR_DEVICE_TIMEOUT if raised, else CQ_OK.
- * Synchronises `stream`. */
+/* Reports (and clears) the device error flags raised by a bounded wait that timed out
+ * (2 s) in a GEMM or GEMV launch on the current device: CQ_ERR_DEVICE_TIMEOUT if any
+ * was raised, else CQ_OK.  Synchronises `stream`. */
 cq_status cq_device_error(void* stream);
 
 /* ---- cq_gemv without a workspace (the paper has no counterpart to this entry point:
@@ -194,8 +195,9 @@ cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks, v
 /* ---- A8: Q4_0 decode GEMV (KMCU page, §2, §3: fixed-length 32 inner loop over
  * row-aligned blocks).  Y[t][o] = sum_blocks fp32(d) * sum_k (nib - 8) * X[t][k],
  * float32 accumulation; padding columns are skipped.
- *   blocks [N][ceil(K/32) * 18] uint8 (any alignment), X [B][K] float32, Y [B][N] float32
- * Errors: INVALID_ARG, ALIGNMENT (X, Y), CUDA. */
+ *   blocks [N][ceil(K/32) * 18] uint8, X [B][K] float32, Y [B][N] float32 (all 16-byte
+ *   aligned); K is limited to 32768 (CQ_ERR_UNSUPPORTED above).
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA. */
 cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t B,
                     float* Y, void* stream);
 

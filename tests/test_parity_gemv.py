@@ -121,7 +121,8 @@ def test_q4_0_gemv_minueza(m, B):
     assert max_rel_err(Y, ref) < TOL
 
 
-@pytest.mark.parametrize("N,K,B", [(1, 1, 1), (3, 33, 2), (9, 1000, 3), (70, 2080, 1)])
+@pytest.mark.parametrize("N,K,B", [(1, 1, 1), (3, 33, 2), (9, 1000, 3), (70, 2080, 1), (40, 2048, 3),
+                                   (333, 8448, 1)])
 def test_q4_0_gemv_ragged(N, K, B):
     Y, ref = _q4_case(N, K, B, N + K, K + B)
     assert max_rel_err(Y, ref) < TOL
