@@ -288,6 +288,8 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     const int tile_rows = kRows * p.rg;
     const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
     const float2* mylut = lut2 + lane;
+    const char* lut_bytes = reinterpret_cast<const char*>(lut2);
+    const uint32_t lane8 = (uint32_t)lane << 3;
     int it = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
@@ -332,11 +334,29 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                     float2 d2[TB];
 #pragma unroll
                     for (int t = 0; t < TB; ++t) d2[t] = make_float2(0.0f, 0.0f);
+                    if constexpr (BITS == 4) {
+                        // byte j of a word -> table offset (byte << 8) | (lane << 3): the
+                        // lane's own copy of entry `byte`, one LOP3 (plus a shift for j != 1)
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
-                        const float2 c = mylut[extract_bits<2 * BITS>(wd[r], q) << 5];
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t wv = wd[r][k];
+                            const uint32_t off[4] = {((wv << 8) & 0xFF00u) | lane8, (wv & 0xFF00u) | lane8,
+                                                     ((wv >> 8) & 0xFF00u) | lane8,
+                                                     ((wv >> 16) & 0xFF00u) | lane8};
 #pragma unroll
-                        for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][q], d2[t]);
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 c = *reinterpret_cast<const float2*>(lut_bytes + off[j]);
+#pragma unroll
+                                for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][4 * k + j], d2[t]);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            const float2 c = mylut[extract_bits<2 * BITS>(wd[r], q) << 5];
+#pragma unroll
+                            for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][q], d2[t]);
+                        }
                     }
 #pragma unroll
                     for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(nrm[r], d2[t].x + d2[t].y, acc[t][r]);
@@ -359,11 +379,10 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
 // every row.  The 18-byte blocks of a row segment are staged in the warp's shared
 // buffer - by double-buffered bulk copies (cp.async.bulk, one per row) when rows and
 // segments are 16-byte aligned, else by guarded 16-byte loads - and each lane reads its
-// block with five aligned 32-bit loads.  A nibble pair is decoded without a table: moved
-// into the mantissa of 256.0f (low nibble) and 16.0f (high nibble), giving exactly
-// 256 + lo and 16 + hi, multiplied by the activation pair with one fp32x2 FMA; the
-// constant offsets (and the -8 of the format) are removed per block with a precomputed
-// sum of the activations.
+// block with five aligned 32-bit loads.  A nibble is decoded without a table: one byte
+// permute drops it into the mantissa of 128.0f, giving exactly 128 + nib; an even/odd
+// pair multiplies the activation pair with one fp32x2 FMA; the constant 128 (and the -8
+// of the format) is removed per block with a precomputed sum of the activations.
 // ---------------------------------------------------------------------------------
 struct Q40GemvParams {
     const uint8_t* blocks;
@@ -382,35 +401,37 @@ struct Q40GemvParams {
 constexpr int kStage = 608;  // >= 37 chunks of 16 B, per row
 
 template <int TB>
-__device__ __forceinline__ void q4_block(const uint8_t* rowbuf, int o, const float2 (&xx)[TB][16],
-                                         const float (&cblk)[TB], float (&accr)[TB]) {
-    // the block starts at byte o (even) of the staged row; read the aligned words
-    // covering it and shift the nibble bytes into place
-    const uint32_t* wp = reinterpret_cast<const uint32_t*>(rowbuf + (o & ~3));
+__device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint32_t nsh,
+                                         const float2 (&xx)[TB][16], const float (&cblk)[TB],
+                                         float (&acc)[TB][kRows], int r) {
+    // wp: the aligned words covering the block; dsh: bit offset of the fp16 scale in
+    // word 0 (0 or 16); nsh = dsh + 16: funnel shift that aligns the nibble bytes
     const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2], w3 = wp[3], w4 = wp[4];
-    const uint32_t sh = (uint32_t)(o & 3) * 8u;          // 0 or 16
-    const uint32_t dbits = (sh == 0u) ? (w0 & 0xFFFFu) : (w0 >> 16);
-    const float d = f16_bits_to_f32((uint16_t)dbits);
-    const uint32_t nw[4] = {__funnelshift_rc(w0, w1, sh + 16u), __funnelshift_rc(w1, w2, sh + 16u),
-                            __funnelshift_rc(w2, w3, sh + 16u), __funnelshift_rc(w3, w4, sh + 16u)};
+    const float d = f16_bits_to_f32((uint16_t)(w0 >> dsh));
+    const uint32_t nw[4] = {__funnelshift_rc(w0, w1, nsh), __funnelshift_rc(w1, w2, nsh),
+                            __funnelshift_rc(w2, w3, nsh), __funnelshift_rc(w3, w4, nsh)};
     float2 s2[TB];
 #pragma unroll
     for (int t = 0; t < TB; ++t) s2[t] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
+        // even-index nibbles (low halves of the bytes) and odd-index nibbles, one per byte
+        const uint32_t ev = nw[k] & 0x0F0F0F0Fu, od = (nw[k] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            // byte j of the word to bits 15..22
-            const uint32_t tb = (j == 0) ? (nw[k] << 15) : (j == 1) ? (nw[k] << 7)
-                              : (j == 2) ? (nw[k] >> 1) : (nw[k] >> 9);
-            const float2 f = make_float2(__uint_as_float((tb & 0x00078000u) | 0x43800000u),
-                                         __uint_as_float((tb & 0x00780000u) | 0x41800000u));
+            // byte j -> byte 2 of 0x43000000: the float 2^7 * (1 + nib / 2^7) = 128 + nib
+            const uint32_t sel = 0x7044u | ((uint32_t)j << 8);
+            uint32_t fe, fo;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fe) : "r"(ev), "r"(0x43000000u), "r"(sel));
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fo) : "r"(od), "r"(0x43000000u), "r"(sel));
+            const float2 f = make_float2(__uint_as_float(fe), __uint_as_float(fo));
 #pragma unroll
             for (int t = 0; t < TB; ++t) s2[t] = __ffma2_rn(f, xx[t][4 * k + j], s2[t]);
         }
     }
+    // sum (nib - 8) x = sum (128 + nib) x - 136 sum x
 #pragma unroll
-    for (int t = 0; t < TB; ++t) accr[t] = fmaf(d, (s2[t].x + s2[t].y) - cblk[t], accr[t]);
+    for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(d, (s2[t].x + s2[t].y) - cblk[t], acc[t][r]);
 }
 
 template <int TB, int SPW, bool BULK>
@@ -452,7 +473,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_kernel(const Q40Gem
                 se += a;
                 so += b;
             }
-            cblk[i][t] = 264.0f * se + 24.0f * so;
+            cblk[i][t] = 136.0f * (se + so);
         }
     }
     __syncthreads();
@@ -553,15 +574,24 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_kernel(const Q40Gem
                     rowbufs = mystage;
                 }
                 if (lane < nb) {
-                    float accr[TB];
+                    if constexpr (BULK) {
+                        // every staged row starts at byte 0: per-lane word offset and shifts
+                        const int o = lane * 18;
+                        const uint32_t dsh = (uint32_t)(o & 3) * 8u;
+                        const uint32_t* wl = reinterpret_cast<const uint32_t*>(rowbufs) + (o >> 2);
 #pragma unroll
-                    for (int r = 0; r < kRows; ++r) {
-                        if (row0 + r >= p.N) continue;
+                        for (int r = 0; r < kRows; ++r)
+                            if (row0 + r < p.N)
+                                q4_block<TB>(wl + r * (kStage / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, r);
+                    } else {
 #pragma unroll
-                        for (int t = 0; t < TB; ++t) accr[t] = acc[t][r];
-                        q4_block<TB>(rowbufs + r * kStage, offs[r] + lane * 18, xx[i], cblk[i], accr);
-#pragma unroll
-                        for (int t = 0; t < TB; ++t) acc[t][r] = accr[t];
+                        for (int r = 0; r < kRows; ++r) {
+                            if (row0 + r >= p.N) continue;
+                            const int o = offs[r] + lane * 18;
+                            const uint32_t dsh = (uint32_t)(o & 3) * 8u;
+                            const uint32_t* wl = reinterpret_cast<const uint32_t*>(rowbufs + r * kStage) + (o >> 2);
+                            q4_block<TB>(wl, dsh, dsh + 16u, xx[i], cblk[i], acc, r);
+                        }
                     }
                 }
             }
