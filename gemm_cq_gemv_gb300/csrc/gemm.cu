@@ -5,21 +5,27 @@
 // xr = Hu @ q (the rotated int8 activations, exact integers) the product is
 //   Y[t][o] = s_t / 128 * sum_k xr[t][k] * cb[idx[o][k]] * norm[o][k / 128]
 // and both factors of the contraction are fed to tcgen05.mma as bf16:
-//   A = bf16(xr)                [M tokens][K]      - rotated once per call, TMA-loaded
-//   B = bf16(cb[idx] * norm)    [N out-rows][K]    - dequantised in shared memory
-// with fp32 accumulation in tensor memory and a bf16 epilogue.
+//   A = bf16(cb[idx] * norm)        [N out-rows][K]  - dequantised into TENSOR memory
+//   B = bf16(xr * s_t / 128)        [M tokens][K]    - rotated once per call, TMA-loaded
+// D[o][t] accumulates in fp32 in tensor memory; the epilogue rounds to bf16 and stores
+// the transposed tile.  Keeping the dequantised weights in tensor memory means shared
+// memory only carries the activation tile (TMA write + one MMA read) and the packed
+// nibbles, which is what lets the MMA rate approach the tensor-core peak.
 //
-// One CTA per SM (persistent), tile = 256 tokens x 128 out-rows, K in chunks of 64 (one
-// 128-byte swizzle atom of bf16), 4 stages; the two fp32 accumulators of a tile (one per
-// 128-token half) are double-buffered in tensor memory so the epilogue of a tile runs
-// under the main loop of the next.
+// One CTA per SM (persistent), tile = 128 out-rows x 192 tokens, K in chunks of 64.
+// Tensor memory (512 columns): 4 A stages of 32 columns (64 bf16 per row) and two
+// 192-column fp32 accumulators (the epilogue of a tile overlaps the next main loop).
 // Warp roles:
-//   warp 0      TMA producer: per stage the two 128-token A tiles and the packed 4-bit
-//               weight tile (128 rows x 32 bytes)
-//   warp 1      MMA issuer (one thread): 2 x 4 tcgen05.mma (M=128, N=128, K=16) per stage
-//   warps 2-9   epilogue: tcgen05.ld of the two accumulators (two warps per TMEM lane
-//               quarter, 64 columns each), scale, bf16, store
-//   warps 10-17 dequant: packed tile (shared) -> bf16 B tile in the SWIZZLE_128B layout
+//   warp 0      TMA producer: per stage the activation tile (128-byte
+//               swizzle) and the packed 4-bit weight tile (128 rows x 32 bytes)
+//   warp 1      MMA issuer (one thread): 4 tcgen05.mma (M=128, N=192, K=16) per stage,
+//               A from tensor memory, B from shared memory
+//   warps 2-9   epilogue: tcgen05.ld (two warps per TMEM lane quarter, 96 tokens each,
+//               16-column pieces),
+//               bf16, store
+//   warps 10-17 dequant: packed tile -> codeword pairs from a per-lane shared table,
+//               scaled by the group norm, bf16, tcgen05.st into the A stage (two warps
+//               per lane quarter, 32 k each)
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a device error
 // flag, stops issuing work, frees its tensor memory and returns.
 
@@ -34,22 +40,24 @@
 namespace cq {
 namespace {
 
-constexpr int kBM = 256;                 // tokens per tile (two M=128 MMAs)
-constexpr int kBN = 128;                 // out-rows per tile (MMA N)
+constexpr int kBO = 128;                 // out-rows per tile (MMA M, TMEM lanes)
+constexpr int kBT = 192;                 // tokens per tile (MMA N)
 constexpr int kBK = 64;                  // K per stage (128 bytes of bf16)
 constexpr int kStages = 4;
 constexpr int kThreadsGemm = 576;        // 18 warps
 constexpr int kEpiWarp0 = 2;             // warps 2..9: two per TMEM lane quarter
 constexpr int kEpiWarps = 8;
 constexpr int kDequantWarp0 = kEpiWarp0 + kEpiWarps;
-constexpr int kDequantThreads = 256;     // warps 10..17
-constexpr int kATileBytes = 128 * kBK * 2;           // 16 KB
-constexpr int kBTileBytes = kBN * kBK * 2;           // 16 KB
-constexpr int kPTileBytes = kBN * kBK / 2;           // 4 KB of packed nibbles
-constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes + kPTileBytes;
-constexpr int kTmemCols = 512;                       // 2 buffers x 2 halves x 128 columns
+constexpr int kDequantWarps = 8;         // warps 10..17: two per TMEM lane quarter
+constexpr int kXTileBytes = kBT * kBK * 2;            // 24 KB of bf16 activations
+constexpr int kPTileBytes = kBO * kBK / 2;            // 4 KB of packed nibbles
+constexpr int kStageBytes = kXTileBytes + kPTileBytes;
+constexpr int kTmemCols = 512;
+constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
+constexpr int kDCol0 = kStages * kACols;              // accumulators start at column 128
 constexpr int kMaxProblems = 120;
 constexpr int kMaxActs = 8;
+static_assert(kDCol0 + 2 * kBT <= kTmemCols, "tensor memory budget");
 
 struct GemmProblem {
     CUtensorMap pmap;        // packed bytes as [N][K/2] uint8, box 32 x 128
@@ -99,11 +107,13 @@ __device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
 }
 __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
     uint32_t ok;
+    // with a suspend-time hint the waiting thread sleeps until the phase completes (or
+    // the hint elapses) instead of spinning and taking issue slots from working warps
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
+        : "r"(smem_u32(b)), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -152,13 +162,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
            ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -184,27 +187,17 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
           "=r"(r[31])
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// scale the first `valid` (0, 16 or 32) of 32 fp32 accumulator columns, round to bf16
-// and store them contiguously
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&r)[32], float sc,
-                                            int valid) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (8 * q >= valid) break;
-        uint4 o;
-        uint32_t* w = &o.x;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[8 * q + 2 * j]) * sc,
-                                                     __uint_as_float(r[8 * q + 2 * j + 1]) * sc);
-            w[j] = *reinterpret_cast<uint32_t*>(&v);
-        }
-        *reinterpret_cast<uint4*>(dst + 8 * q) = o;
-    }
 }
 
 __device__ __forceinline__ int find_problem(const GemmParams& p, int tile) {
@@ -217,11 +210,13 @@ __device__ __forceinline__ int find_problem(const GemmParams& p, int tile) {
 }
 
 // ---------------------------------------------------------------------------------
-// xr = bf16(Hu @ q) per 128-group; one warp per (token, group).  The fp32 butterfly is
-// exact (integers below 2^24); the single rounding is the bf16 conversion.
+// B = bf16(Hu @ q * s_t / 128) per 128-group; one warp per (token, group).  The fp32
+// butterfly is exact (integers below 2^24); the product with s_t / 128 and the bf16
+// conversion are the only roundings.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
-rotate_act_bf16_kernel(const int8_t* __restrict__ Xq, int64_t groups, __nv_bfloat16* __restrict__ out) {
+rotate_act_bf16_kernel(const int8_t* __restrict__ Xq, const float* __restrict__ scale,
+                       int64_t groups, int64_t groups_per_token, __nv_bfloat16* __restrict__ out) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * 256) >> 5;
@@ -242,8 +237,9 @@ rotate_act_bf16_kernel(const int8_t* __restrict__ Xq, int64_t groups, __nv_bfloa
             v2 = upper ? (p2 - v2) : (v2 + p2);
             v3 = upper ? (p3 - v3) : (v3 + p3);
         }
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v0, v1);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v2, v3);
+        const float sc = __ldg(scale + gi / groups_per_token) * (1.0f / 128.0f);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v0 * sc, v1 * sc);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v2 * sc, v3 * sc);
         uint2 pk;
         pk.x = *reinterpret_cast<uint32_t*>(&lo);
         pk.y = *reinterpret_cast<uint32_t*>(&hi);
@@ -274,16 +270,33 @@ __device__ __forceinline__ float load_norm(const GemmProblem& pr, int o, int kc)
     return f16_bits_to_f32(__ldg(pr.norms + (int64_t)o * G + (kc * kBK) / kGroup));
 }
 
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~(uintptr_t)1023);
-    // stage s: [A half 0 | A half 1 | B (bf16, swizzled) | P (packed, 32 B per row)]
+    // stage s: [X (bf16, swizzled, 192 rows) | P (packed, 32 B per out-row)]
     uint8_t* stage_base = smem;
-    float* lut = reinterpret_cast<float*>(smem + kStages * kStageBytes);        // [16][32]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(lut + 16 * 32);
-    uint64_t* full_a = bars;                      // TMA: A tiles + packed tile landed
-    uint64_t* full_b = bars + kStages;            // dequant: B tile written
+    float2* lut2 = reinterpret_cast<float2*>(smem + kStages * kStageBytes);   // [256][32]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(lut2 + 256 * 32);
+    uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
+    uint64_t* full_b = bars + kStages;            // dequant: A stage written to TMEM
     uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
     uint64_t* acc_full = bars + 3 * kStages;      // [2] accumulator buffer ready
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator buffer drained
@@ -292,17 +305,21 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    for (int i = tid; i < 16 * 32; i += kThreadsGemm) {
-        const int t = i >> 5;
-        float v = 0.0f;
+    // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]), one copy per lane
+    for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
+        const int e = i >> 5;
+        float a = 0.0f, b = 0.0f;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) v = (u == t) ? p.lv[u] : v;
-        lut[i] = v;
+        for (int u = 0; u < 16; ++u) {
+            a = (u == (e & 15)) ? p.lv[u] : a;
+            b = (u == (e >> 4)) ? p.lv[u] : b;
+        }
+        lut2[i] = make_float2(a, b);
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_a[s], 1);
-            mbar_init(&full_b[s], kDequantThreads / 32);
+            mbar_init(&full_b[s], kDequantWarps);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -332,15 +349,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
                 const TileRef tr = tile_ref(p, tile);
                 const GemmProblem& pr = p.prob[tr.prob];
-                const CUtensorMap* amap = &p.tmap[pr.act];
+                const CUtensorMap* xmap = &p.tmap[pr.act];
                 for (int kc = 0; kc < pr.K / kBK; ++kc) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p)) { ok = false; break; }
                     uint8_t* st = stage_base + s * kStageBytes;
-                    mbar_arrive_tx(&full_a[s], 2 * kATileBytes + kPTileBytes);
-                    tma_load_2d(st, amap, kc * kBK, tr.mt * kBM, &full_a[s]);
-                    tma_load_2d(st + kATileBytes, amap, kc * kBK, tr.mt * kBM + 128, &full_a[s]);
-                    tma_load_2d(st + 2 * kATileBytes + kBTileBytes, &pr.pmap, kc * (kBK / 2),
-                                tr.nt * kBN, &full_a[s]);
+                    mbar_arrive_tx(&full_a[s], kXTileBytes + kPTileBytes);
+                    tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
+                    tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK / 2), tr.nt * kBO, &full_a[s]);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
@@ -349,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(128, kBN);
+            constexpr uint32_t idesc = idesc_bf16(kBO, kBT);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -360,24 +375,20 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 const uint32_t aph = (uint32_t)((it >> 1) & 1);
                 if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, p)) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + (uint32_t)(buf * 2 * kBN);
+                const uint32_t d = tmem_base + (uint32_t)(kDCol0 + buf * kBT);
                 const int nk = pr.K / kBK;
                 for (int kc = 0; kc < nk; ++kc) {
                     if (!mbar_wait(&full_a[s], ph, abort_flag, p) ||
                         !mbar_wait(&full_b[s], ph, abort_flag, p)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t st = smem_u32(stage_base + s * kStageBytes);
-                    const uint64_t bdesc0 = smem_desc_sw128(st + 2 * kATileBytes);
+                    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(stage_base + s * kStageBytes));
+                    const uint32_t a0 = tmem_base + (uint32_t)(s * kACols);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t adesc0 = smem_desc_sw128(st + h * kATileBytes);
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            // +32 bytes along K inside the swizzle atom = +2 in the
-                            // 16-byte-unit start address field
-                            umma_bf16(d0 + (uint32_t)(h * kBN), adesc0 + 2u * kk, bdesc0 + 2u * kk,
-                                      idesc, (kc > 0 || kk > 0) ? 1u : 0u);
-                        }
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // A: 8 TMEM columns (16 bf16) per K step; B: +32 bytes along K
+                        // inside the swizzle atom = +2 in the 16-byte-unit address field
+                        umma_bf16_tmem_a(d, a0 + (uint32_t)(8 * kk), bdesc0 + 2u * kk, idesc,
+                                         (kc > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -389,11 +400,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         __syncwarp();
     } else if (warp < kDequantWarp0) {
         // ------------------------------ epilogue ----------------------------------
-        // warp -> TMEM lane quarter q (tokens 32q..32q+31 of each half) and a 64-column
-        // half ch of the tile; four 32-column loads per tile, each issued before the
-        // previous one is converted and stored
+        // warp -> TMEM lane quarter q (out-rows 32q..32q+31) and token half th (96 tokens);
+        // three 32-column loads per tile, each issued before the previous one is stored
         const int q = warp & 3;
-        const int ch = (warp - kEpiWarp0) >> 2;
+        const int th = (warp - kEpiWarp0) >> 2;
         int it = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
             const TileRef tr = tile_ref(p, tile);
@@ -401,41 +411,44 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             const int buf = it & 1;
             if (!mbar_wait(&acc_full[buf], (uint32_t)((it >> 1) & 1), abort_flag, p)) break;
             tc_fence_after();
-            const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (uint32_t)(buf * 2 * kBN + ch * 64);
-            const int tok0 = tr.mt * kBM + q * 32 + lane;
-            const int tok1 = tok0 + 128;
-            const float sc0 = (tok0 < p.M) ? __ldg(pr.scale + tok0) * (1.0f / 128.0f) : 0.0f;
-            const float sc1 = (tok1 < p.M) ? __ldg(pr.scale + tok1) * (1.0f / 128.0f) : 0.0f;
-            const int col = tr.nt * kBN + ch * 64;
-            __nv_bfloat16* y0 = pr.Y + (int64_t)tok0 * pr.N + col;
-            __nv_bfloat16* y1 = pr.Y + (int64_t)tok1 * pr.N + col;
-            // valid columns of each 32-column piece (N is a multiple of 16)
-            const int v0 = min(32, max(0, pr.N - col)), v1 = min(32, max(0, pr.N - col - 32));
-            uint32_t ra[32], rb[32];
-            tmem_ld32_async(lane_base, ra);                         // half 0, cols 0..31
-            tmem_wait_ld();
-            tmem_ld32_async(lane_base + 32, rb);                    // half 0, cols 32..63
-            if (tok0 < p.M) store_row32(y0, ra, sc0, v0);
-            tmem_wait_ld();
-            tmem_ld32_async(lane_base + kBN, ra);                   // half 1, cols 0..31
-            if (tok0 < p.M) store_row32(y0 + 32, rb, sc0, v1);
-            tmem_wait_ld();
-            tmem_ld32_async(lane_base + kBN + 32, rb);              // half 1, cols 32..63
-            if (tok1 < p.M) store_row32(y1, ra, sc1, v0);
-            tmem_wait_ld();
-            if (tok1 < p.M) store_row32(y1 + 32, rb, sc1, v1);
+            const uint32_t col0 = tmem_base + ((uint32_t)(q * 32) << 16) +
+                                  (uint32_t)(kDCol0 + buf * kBT + th * (kBT / 2));
+            const int o = tr.nt * kBO + q * 32 + lane;
+            const int t0 = tr.mt * kBT + th * (kBT / 2);
+            const bool ook = o < pr.N;
+            __nv_bfloat16* ycol = pr.Y + o;
+            // 16-column pieces, each load issued before the previous piece is stored
+            constexpr int kPieces = (kBT / 2) / 16;
+            uint32_t rr[2][16];
+            auto store16 = [&](const uint32_t (&r)[16], int tb) {
+                if (!ook) return;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = tb + j;
+                    if (t < p.M) ycol[(int64_t)t * pr.N] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                }
+            };
+            tmem_ld16_async(col0, rr[0]);
+#pragma unroll
+            for (int pc = 0; pc < kPieces; ++pc) {
+                tmem_wait_ld();
+                if (pc + 1 < kPieces) tmem_ld16_async(col0 + 16 * (pc + 1), rr[(pc + 1) & 1]);
+                store16(rr[pc & 1], t0 + 16 * pc);
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
     } else {
         // ------------------------------ dequant -----------------------------------
-        // thread dt owns row r = dt / 2 and k-half hf = dt % 2 of every B tile: 32 nibbles
-        // (16 bytes of the staged packed tile) -> four 16-byte chunks of the swizzled tile
-        const int dt = tid - kDequantWarp0 * 32;    // 0..255
-        const int r = dt >> 1, hf = dt & 1;
-        const float* mylut = lut + lane;
+        // warp -> TMEM lane quarter q (out-rows 32q..32q+31) and k half kh (32 of the 64 k
+        // of a stage); lane -> one row: 16 packed bytes -> 16 codeword pairs (one table
+        // lookup each) x norm -> bf16 pairs -> tcgen05.st of 16 columns
+        const int q = warp & 3;
+        const int kh = (warp - kDequantWarp0) >> 2;
+        const int r = q * 32 + lane;
+        const char* lut_bytes = reinterpret_cast<const char*>(lut2);
+        const uint32_t lane8 = (uint32_t)lane << 3;
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -443,7 +456,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         float nrm = 0.0f;
         if (tile < p.total_tiles) {
             const TileRef tr = tile_ref(p, tile);
-            nrm = load_norm(p.prob[tr.prob], tr.nt * kBN + r, 0);
+            nrm = load_norm(p.prob[tr.prob], tr.nt * kBO + r, 0);
         }
         for (; ok && tile < p.total_tiles; tile += gridDim.x) {
             const TileRef tr = tile_ref(p, tile);
@@ -453,34 +466,33 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 // prefetch the norm of the next chunk (or of the next tile's first chunk)
                 float nrm_next = 0.0f;
                 if (kc + 1 < nk) {
-                    nrm_next = load_norm(pr, tr.nt * kBN + r, kc + 1);
+                    nrm_next = load_norm(pr, tr.nt * kBO + r, kc + 1);
                 } else if (tile + (int)gridDim.x < p.total_tiles) {
                     const TileRef tn = tile_ref(p, tile + gridDim.x);
-                    nrm_next = load_norm(p.prob[tn.prob], tn.nt * kBN + r, 0);
+                    nrm_next = load_norm(p.prob[tn.prob], tn.nt * kBO + r, 0);
                 }
                 if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
-                uint8_t* st = stage_base + s * kStageBytes;
-                uint8_t* bt = st + 2 * kATileBytes;
-                const uint4 w = *reinterpret_cast<const uint4*>(st + 2 * kATileBytes + kBTileBytes +
-                                                                r * 32 + hf * 16);
+                const uint4 w = *reinterpret_cast<const uint4*>(stage_base + s * kStageBytes +
+                                                                kXTileBytes + r * 32 + kh * 16);
                 const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                const float2 n2 = make_float2(nrm, nrm);
+                uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {      // 8 k values -> one 16-byte chunk
-                    uint32_t pk[4];
+                for (int k = 0; k < 4; ++k) {
+                    // byte j -> offset (byte << 8) | (lane << 3) of the lane's own table copy
+                    const uint32_t off[4] = {((wv[k] << 8) & 0xFF00u) | lane8, (wv[k] & 0xFF00u) | lane8,
+                                             ((wv[k] >> 8) & 0xFF00u) | lane8,
+                                             ((wv[k] >> 16) & 0xFF00u) | lane8};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t i0 = (wv[j] >> (8 * e)) & 15u;
-                        const uint32_t i1 = (wv[j] >> (8 * e + 4)) & 15u;
-                        __nv_bfloat162 v = __floats2bfloat162_rn(mylut[i0 << 5] * nrm,
-                                                                 mylut[i1 << 5] * nrm);
-                        pk[e] = *reinterpret_cast<uint32_t*>(&v);
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 c = __fmul2_rn(*reinterpret_cast<const float2*>(lut_bytes + off[j]), n2);
+                        __nv_bfloat162 v = __floats2bfloat162_rn(c.x, c.y);
+                        pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
                     }
-                    const int c = hf * 4 + j;
-                    *reinterpret_cast<uint4*>(bt + r * 128 + ((c ^ (r & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
-                // make the generic-proxy writes visible to the tensor cores, then arrive
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full_b[s]);
                 if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -531,7 +543,7 @@ cq_status host_setup(unsigned int** err) {
         g_err_ptr[dev] = static_cast<unsigned int*>(pe);
     }
     if (!g_attr_done[dev]) {
-        const size_t smem = (size_t)kStages * kStageBytes + 16 * 32 * 4 + 256 + 1024;  // + align slack
+        const size_t smem = (size_t)kStages * kStageBytes + 256 * 32 * 8 + 256 + 1024;  // + align slack
         e = cudaFuncSetAttribute(cq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
         g_attr_done[dev] = true;
@@ -543,7 +555,7 @@ cq_status host_setup(unsigned int** err) {
 cq_status make_packed_map(CUtensorMap* map, const void* base, int64_t N, int64_t K) {
     cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    cuuint32_t box[2] = {(cuuint32_t)(kBK / 2), (cuuint32_t)kBN};
+    cuuint32_t box[2] = {(cuuint32_t)(kBK / 2), (cuuint32_t)kBO};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -556,7 +568,7 @@ cq_status make_packed_map(CUtensorMap* map, const void* base, int64_t N, int64_t
 cq_status make_act_map(CUtensorMap* map, const void* base, int64_t M, int64_t K) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBT};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -651,7 +663,8 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
             const int64_t cap = (int64_t)sm_count() * 16;
             if (grid > cap) grid = cap;
             rotate_act_bf16_kernel<<<(unsigned)grid, 256, 0, cs>>>(
-                probs[i].Xq, groups, reinterpret_cast<__nv_bfloat16*>(ws + off));
+                probs[i].Xq, probs[i].scale, groups, probs[i].K / kGroup,
+                reinterpret_cast<__nv_bfloat16*>(ws + off));
             st = check_launch();
             if (st != CQ_OK) return st;
             off += ((size_t)M * (size_t)probs[i].K * 2u + 255u) & ~(size_t)255u;
@@ -677,7 +690,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
         int map_of_act[1024];
         for (int a = 0; a < nact; ++a) map_of_act[a] = -1;
         int nmaps = 0, np = 0, tiles = 0;
-        const int tiles_m = (int)((M + kBM - 1) / kBM);
+        const int tiles_m = (int)((M + kBT - 1) / kBT);
         while (i0 < count && np < kMaxProblems) {
             const int pi = order[i0];
             const int a = act_of[pi];
@@ -694,7 +707,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
             gp.N = (int)q.N; gp.K = (int)q.K; gp.act = map_of_act[a];
             st = make_packed_map(&gp.pmap, q.packed, q.N, q.K);
             if (st != CQ_OK) return st;
-            gp.tiles_n = (int)((q.N + kBN - 1) / kBN);
+            gp.tiles_n = (int)((q.N + kBO - 1) / kBO);
             gp.tile_begin = tiles;
             tiles += gp.tiles_n * tiles_m;
             ++i0;
@@ -706,7 +719,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
         fill_levels(prm.lv, b, cbk);
         prm.err = err;
         prm.timeout_ns = 2000000000ull;   // 2 s per wait
-        const size_t smem = (size_t)kStages * kStageBytes + 16 * 32 * 4 + 256 + 1024;  // + align slack
+        const size_t smem = (size_t)kStages * kStageBytes + 256 * 32 * 8 + 256 + 1024;  // + align slack
         const int grid = tiles < sm_count() ? tiles : sm_count();
         cq_gemm_kernel<<<grid, kThreadsGemm, smem, cs>>>(prm);
         st = check_launch();

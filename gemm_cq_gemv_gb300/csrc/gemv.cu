@@ -107,11 +107,13 @@ __device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
 }
 __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
     uint32_t ok;
+    // with a suspend-time hint the waiting thread sleeps until the phase completes (or
+    // the hint elapses) instead of spinning and taking issue slots from working warps
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
+        : "r"(smem_u32(b)), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
