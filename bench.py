@@ -443,10 +443,12 @@ def cpu_baseline(rows):
     cb = load_codebook()
     state = oracle_state(rows, cb, synth, oracle)
     oracle_sample_step(rows, cb, synth, oracle, state)
-    reps, nbytes = 4, 0
+    # repeat the sample for about ten seconds of CPU work
+    reps, nbytes = 0, 0
     a = time.perf_counter()
-    for _ in range(reps):
+    while reps == 0 or time.perf_counter() - a < 10.0:
         nbytes += oracle_sample_step(rows, cb, synth, oracle, state)
+        reps += 1
     dt = time.perf_counter() - a
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
             "kind": "oracle",

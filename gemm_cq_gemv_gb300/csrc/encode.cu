@@ -168,16 +168,32 @@ __global__ void __launch_bounds__(kEncThreads) cq_encode_kernel(const EncodePara
 // ---------------------------------------------------------------------------------
 // A3: per-token symmetric int8.  One CTA per token.
 // ---------------------------------------------------------------------------------
-constexpr int kA8Threads = 256;
+constexpr int kA8Threads = 512;
 
+__device__ __forceinline__ int8_t a8_code(float x, float s) {
+    const float q = fminf(fmaxf(rintf(__fdiv_rn(x, s)), -127.0f), 127.0f);
+    return (int8_t)(int)q;
+}
+
+// One CTA per token; 16-byte loads / 4-byte stores when the row allows it (K % 4 == 0).
 __global__ void __launch_bounds__(kA8Threads)
 a8_quantize_kernel(const float* __restrict__ X, int64_t K, int8_t* __restrict__ Xq,
                    float* __restrict__ scale) {
     __shared__ float red[kA8Threads / 32];
     const int64_t t = blockIdx.x;
     const float* x = X + t * K;
+    int8_t* xq = Xq + t * K;
+    const bool vec = (K & 3) == 0;
     float amax = 0.0f;
-    for (int64_t k = threadIdx.x; k < K; k += kA8Threads) amax = fmaxf(amax, fabsf(x[k]));
+    if (vec) {
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        for (int64_t k = threadIdx.x; k < K / 4; k += kA8Threads) {
+            const float4 v = x4[k];
+            amax = fmaxf(fmaxf(amax, fmaxf(fabsf(v.x), fabsf(v.y))), fmaxf(fabsf(v.z), fabsf(v.w)));
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < K; k += kA8Threads) amax = fmaxf(amax, fabsf(x[k]));
+    }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
@@ -185,10 +201,15 @@ a8_quantize_kernel(const float* __restrict__ X, int64_t K, int8_t* __restrict__ 
     amax = 0.0f;
     for (int w = 0; w < kA8Threads / 32; ++w) amax = fmaxf(amax, red[w]);
     const float s = (amax > 0.0f) ? __fdiv_rn(amax, 127.0f) : 1.0f;
-    for (int64_t k = threadIdx.x; k < K; k += kA8Threads) {
-        float q = rintf(__fdiv_rn(x[k], s));
-        q = fminf(fmaxf(q, -127.0f), 127.0f);
-        Xq[t * K + k] = (int8_t)(int)q;
+    if (vec) {
+        const float4* x4 = reinterpret_cast<const float4*>(x);
+        char4* q4 = reinterpret_cast<char4*>(xq);
+        for (int64_t k = threadIdx.x; k < K / 4; k += kA8Threads) {
+            const float4 v = x4[k];
+            q4[k] = make_char4(a8_code(v.x, s), a8_code(v.y, s), a8_code(v.z, s), a8_code(v.w, s));
+        }
+    } else {
+        for (int64_t k = threadIdx.x; k < K; k += kA8Threads) xq[k] = a8_code(x[k], s);
     }
     if (threadIdx.x == 0) scale[t] = s;
 }
