@@ -83,12 +83,13 @@ __device__ __forceinline__ float reduce_rows8(const float (&a)[kRows], int lane)
 // slice is loaded into registers once per kernel; when K has fewer segments than warps
 // the warps sharing a segment split the tile into row groups of 8.  Every tile therefore
 // needs a cross-warp sum: each warp drops its per-row partials into one of kSlots
-// shared slots and arrives on the slot's mbarrier; the warp whose turn it is (tile
-// index mod 16) waits for all 16 arrivals, adds the partials in warp order
-// (deterministic) and frees the slot.  No CTA-wide barrier stalls the streaming warps.
+// shared slots and counts itself in with an atomic add on the slot's counter; the warp
+// that arrives last adds the partials in warp order (deterministic), writes the rows
+// and frees the slot.  A warp waits only when it runs kSlots tiles ahead of the slowest
+// one, so no warp stalls the streaming of the others.
 // ---------------------------------------------------------------------------------
 constexpr int kWarps2 = 16;
-constexpr int kSlots = 4;
+constexpr int kSlots = 16;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -138,16 +139,25 @@ __device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned
 
 struct Reduce {
     float* part;        // [kSlots][16][TB][8]
-    uint64_t* full;     // [kSlots]
-    uint64_t* empty;    // [kSlots]
+    uint32_t* count;    // [kSlots] arrivals (cumulative)
+    uint64_t* empty;    // [kSlots] completes when the slot's tile has been reduced
 };
 
-// Stores this warp's row partials of tile number `it` and, on its turn, reduces the tile.
-// `fin(t, rr, sum)` receives the sum for token t of tile row rr.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_shared(uint32_t* a, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "r"(smem_u32(a)), "r"(v)
+                 : "memory");
+    return old;
+}
+
+// Stores this warp's row partials of tile number `it`; the last of the `nbusy` warps to
+// arrive reduces the tile.  `fin(t, rr, sum)` receives the sum for token t of tile row rr.
 template <int TB, typename Fin>
 __device__ __forceinline__ void tile_reduce(const Reduce& rd, const float (&acc)[TB][kRows], int it,
-                                            int w, int lane, int nsl, int tile_rows, int ntok,
-                                            unsigned int* err, Fin fin) {
+                                            int w, int lane, int nsl, uint32_t nbusy, int tile_rows,
+                                            int ntok, unsigned int* err, Fin fin) {
     const int slot = it % kSlots;
     const uint32_t ph = (uint32_t)((it / kSlots) & 1);
     float v[TB];
@@ -160,9 +170,11 @@ __device__ __forceinline__ void tile_reduce(const Reduce& rd, const float (&acc)
             rd.part[((slot * kWarps2 + w) * TB + t) * kRows + ((lane >> 2) & 7)] = v[t];
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&rd.full[slot]);
-    if (w == it % kWarps2) {
-        mbar_wait(&rd.full[slot], ph, err);
+    uint32_t old = 0;
+    if (lane == 0) old = atomic_add_acq_rel_shared(&rd.count[slot], 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old % nbusy == nbusy - 1u) {
+        __syncwarp();
         for (int idx = lane; idx < TB * tile_rows; idx += 32) {
             const int t = idx / tile_rows, rr = idx % tile_rows;
             const int g = rr / kRows, r = rr % kRows;
@@ -178,24 +190,73 @@ __device__ __forceinline__ void tile_reduce(const Reduce& rd, const float (&acc)
     }
 }
 
-__device__ __forceinline__ void init_reduce_bars(const Reduce& rd) {
+__device__ __forceinline__ void init_reduce(const Reduce& rd) {
     for (int s = 0; s < kSlots; ++s) {
-        mbar_init(&rd.full[s], kWarps2);
+        rd.count[s] = 0u;
         mbar_init(&rd.empty[s], 1);
     }
 }
 
-constexpr size_t reduce_bytes(int tb) {
-    return (size_t)kSlots * kWarps2 * tb * kRows * sizeof(float) + 2 * kSlots * sizeof(uint64_t);
+// bytes of the reduction area: partials, then the barriers (8-byte aligned), then counters
+__host__ __device__ constexpr size_t reduce_bytes(int tb) {
+    return (size_t)kSlots * kWarps2 * tb * kRows * sizeof(float) + kSlots * sizeof(uint64_t) +
+           kSlots * sizeof(uint32_t);
 }
+
+__device__ __forceinline__ Reduce carve_reduce(void* base, int tb) {
+    Reduce rd;
+    rd.part = reinterpret_cast<float*>(base);
+    rd.empty = reinterpret_cast<uint64_t*>(rd.part + kSlots * kWarps2 * tb * kRows);
+    rd.count = reinterpret_cast<uint32_t*>(rd.empty + kSlots);
+    return rd;
+}
+
+// ---------------------------------------------------------------------------------
+// Per-warp staging ring.  Each warp streams its own rows through kRing slots of shared
+// memory, one slot per unit of kUnitRows rows (half a warp tile) of one owned segment,
+// filled by bulk copies (cp.async.bulk, one per row) that complete on the slot's
+// mbarrier.  While a unit is decoded the next kRing - 1 are in flight, so the load
+// latency overlaps the decode instead of following it.
+// ---------------------------------------------------------------------------------
+constexpr int kUnitRows = 4;
+constexpr int kRing = 4;
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// orders this thread's earlier shared-memory reads before later bulk copies into them
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bump allocator over (at most) two free ranges of the shared window; every thread runs
+// it identically, so all agree on the layout.
+struct SmemCarve {
+    uint32_t a, a_end, b, b_end;
+    bool ok;
+    __device__ __forceinline__ uint32_t take(uint32_t size, uint32_t align) {
+        const uint32_t pa = (a + align - 1) & ~(align - 1);
+        if (pa + size <= a_end) { a = pa + size; return pa; }
+        const uint32_t pb = (b + align - 1) & ~(align - 1);
+        if (pb + size <= b_end) { b = pb + size; return pb; }
+        ok = false;
+        return b;
+    }
+};
 
 // ---------------------------------------------------------------------------------
 // A5: CQ GEMV.  Y[t][o] = s_t / 128 * sum_j norm[o][j] * sum_i cb[idx] * xr[t][128 j + i]
 // Codewords come from a shared-memory table indexed by two consecutive indices (2b
 // bits): entry e = (cb[e mod 2^b], cb[e / 2^b]), replicated once per bank so every lane
 // reads its own copy (conflict-free 64-bit loads); the pair multiplies a pair of
-// activations with one packed fp32x2 FMA.  The packed rows of the next tile are
-// prefetched into L2 while the current one is decoded.
+// activations with one packed fp32x2 FMA.  For 4-bit indices the table sits at a 64 KB
+// boundary of the shared window, so the address of (entry e, lane l), base | e << 8 |
+// l << 3, is one byte permute of an index byte into the lane's base.  The packed rows
+// and their group norms arrive through the warp's staging ring.
 // ---------------------------------------------------------------------------------
 struct CqGemvParams {
     const uint8_t* packed;
@@ -210,6 +271,7 @@ struct CqGemvParams {
     int rg;               // row groups per tile
     int t0;               // first token of this pass
     int ntok;             // tokens in this pass (<= TB)
+    uint32_t smem_bytes;  // dynamic shared memory of the launch
     float lv[16];
 };
 
@@ -223,34 +285,87 @@ __device__ __forceinline__ uint32_t extract_bits(const uint32_t* w, int p) {
     return v & ((1u << NB) - 1u);
 }
 
+// this lane's 4 b bytes of a staged row segment
 template <int BITS>
-__device__ __forceinline__ void load_packed(uint32_t (&w)[BITS], const uint8_t* p) {
+__device__ __forceinline__ void lds_packed(uint32_t (&w)[BITS], const uint8_t* p) {
     if constexpr (BITS == 4) {
-        const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
         w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     } else if constexpr (BITS == 2) {
-        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(p));
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
         w[0] = v.x; w[1] = v.y;
     } else {
 #pragma unroll
-        for (int k = 0; k < BITS; ++k) w[k] = __ldcs(reinterpret_cast<const uint32_t*>(p) + k);
+        for (int k = 0; k < BITS; ++k) w[k] = reinterpret_cast<const uint32_t*>(p)[k];
     }
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+template <int J>
+__device__ __forceinline__ uint32_t pair_addr(uint32_t wv, uint32_t lb) {
+    uint32_t a;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(wv), "r"(lb), "n"(0x7604 | (J << 4)));
+    return a;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
+// Shared-memory plan of the CQ kernel: pair table, reduction area, ring barriers and one
+// ring per warp (a slot holds kUnitRows packed row segments, then their 16-byte norm runs).
+template <int BITS>
+struct CqPlan {
+    static constexpr uint32_t seg = 128 * BITS;
+    static constexpr uint32_t slot = kUnitRows * (seg + 16);
+    static constexpr uint32_t ring = kRing * slot;
+    static constexpr uint32_t table = (1u << (2 * BITS)) * 32 * 8;
+};
+
+template <int BITS>
+size_t cq_smem_bytes(int tb) {
+    using P = CqPlan<BITS>;
+    const size_t rest = reduce_bytes(tb) + 16 + kWarps2 * kRing * 8 + 8 + (size_t)kWarps2 * (P::ring + 128);
+    // 4-bit: the table is 64 KB aligned; the space below it may be too small to use
+    if (BITS == 4) return 227 * 1024;
+    return P::table + 16 + rest;
 }
 
 template <int BITS, int TB, int SPW>
 __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvParams p) {
+    using P = CqPlan<BITS>;
     constexpr int L = 1 << BITS;
     constexpr int E = 1 << (2 * BITS);
-    extern __shared__ __align__(16) float2 lut2[];                      // [E][32]
-    Reduce rd;
-    rd.part = reinterpret_cast<float*>(lut2 + E * 32);
-    rd.full = reinterpret_cast<uint64_t*>(rd.part + kSlots * kWarps2 * TB * kRows);
-    rd.empty = rd.full + kSlots;
+    extern __shared__ __align__(128) unsigned char smem_c[];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const uint32_t sbase = smem_u32(smem_c), send = sbase + p.smem_bytes;
+    uint32_t tbase;
+    SmemCarve cv;
+    cv.ok = true;
+    if (BITS == 4) {
+        tbase = (sbase + 65535u) & ~65535u;
+        cv.a = sbase; cv.a_end = tbase; cv.b = tbase + P::table; cv.b_end = send;
+    } else {
+        tbase = (sbase + 15u) & ~15u;
+        cv.a = cv.a_end = tbase + P::table; cv.b = cv.a; cv.b_end = send;
+    }
+    if (tbase + P::table > send) cv.ok = false;
+    const uint32_t red_at = cv.take((uint32_t)reduce_bytes(TB), 16);
+    const uint32_t bar_at = cv.take(kWarps2 * kRing * 8, 8);
+    uint32_t ring_at = 0;
+    for (int v = 0; v < kWarps2; ++v) {
+        const uint32_t at = cv.take(P::ring, 128);
+        if (v == w) ring_at = at;
+    }
+    if (!cv.ok) {   // the launch's shared memory cannot hold the plan (host sizing error)
+        if (tid == 0) atomicOr(p.err, 4u);
+        return;
+    }
+    auto gen = [&](uint32_t a) { return smem_c + (a - sbase); };
+    float2* lut2 = reinterpret_cast<float2*>(gen(tbase));                 // [E][32]
+    const Reduce rd = carve_reduce(gen(red_at), TB);
+    uint64_t* rfull = reinterpret_cast<uint64_t*>(gen(bar_at)) + w * kRing;
+    uint8_t* ring = gen(ring_at);
     for (int i = tid; i < E * 32; i += kWarps2 * 32) {
         const int e = i >> 5;
         float a = 0.0f, b = 0.0f;
@@ -261,10 +376,15 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
         }
         lut2[i] = make_float2(a, b);
     }
-    if (tid == 0) init_reduce_bars(rd);
+    if (tid == 0) {
+        init_reduce(rd);
+        uint64_t* all = reinterpret_cast<uint64_t*>(gen(bar_at));
+        for (int i = 0; i < kWarps2 * kRing; ++i) mbar_init(&all[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
     const int slot = w % nsl, rgi = w / nsl;
-    const bool busy = rgi < p.rg;
+    const uint32_t nbusy = (uint32_t)(nsl * p.rg);
     float2 xx[SPW][TB][16];
 #pragma unroll
     for (int i = 0; i < SPW; ++i) {
@@ -272,7 +392,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
         const int pos0 = seg * kSeg + lane * 32;
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
-            const bool ok = busy && seg < p.nseg && pos0 < p.K && t < p.ntok;
+            const bool ok = rgi < p.rg && seg < p.nseg && pos0 < p.K && t < p.ntok;
             const float* src = p.xr + (int64_t)(p.t0 + t) * p.K + pos0;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -284,88 +404,120 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
         }
     }
     __syncthreads();
+    if (rgi >= p.rg) return;   // warps left over when the segments do not divide 16
 
     const int G = p.K / kGroup;
     const int64_t rowbytes = (int64_t)G * 16 * BITS;
     const int tile_rows = kRows * p.rg;
     const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
+    const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int nown = (SPW == 2 && slot + kWarps2 < p.nseg) ? 2 : 1;   // owned segments
+    const int upt = 2 * nown;                                           // units per tile
+    const int64_t U = ntk * upt;
+    const bool nbulk = (p.K % kSeg) == 0;   // a segment's norms are 16 aligned bytes
     const float2* mylut = lut2 + lane;
-    const char* lut_bytes = reinterpret_cast<const char*>(lut2);
-    const uint32_t lane8 = (uint32_t)lane << 3;
-    int it = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-        const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
-        // L2 prefetch of this warp's rows of the next tile (one lane per row and segment)
-        if (busy && lane < kRows * SPW) {
-            const int r = lane % kRows, i = lane / kRows;
-            const int seg = slot + i * kWarps2;
-            const int64_t nrow = row0 + (int64_t)gridDim.x * tile_rows + r;
-            if (seg < p.nseg && nrow < p.N) {
-                const int bytes = min(128 * BITS, (int)((p.K - seg * kSeg) / 8 * BITS));
-                prefetch_l2(p.packed + nrow * rowbytes + (int64_t)seg * (128 * BITS), (uint32_t)bytes);
-            }
+    const uint32_t lb = tbase | ((uint32_t)lane << 3);
+
+    auto issue = [&](int64_t u) {
+        const int64_t k = u / upt;
+        const int rem = (int)(u - k * upt);
+        const int seg = slot + (rem >> 1) * kWarps2;
+        const int64_t row0 = (blockIdx.x + k * gridDim.x) * tile_rows + (int64_t)rgi * kRows +
+                             (rem & 1) * kUnitRows;
+        const int64_t left = p.N - row0;
+        const int nr = left >= kUnitRows ? kUnitRows : (left > 0 ? (int)left : 0);
+        const uint32_t bytes = min(P::seg, (uint32_t)((p.K - seg * kSeg) / 8 * BITS));
+        const int d = (int)(u % kRing);
+        uint8_t* sp = ring + d * P::slot;
+        if (lane == 0) mbar_arrive_tx(&rfull[d], (uint32_t)nr * (bytes + (nbulk ? 16u : 0u)));
+        __syncwarp();
+        if (lane < nr) {
+            bulk_g2s(sp + lane * P::seg, p.packed + (row0 + lane) * rowbytes + (int64_t)seg * P::seg,
+                     bytes, &rfull[d]);
+        } else if (nbulk && lane >= 8 && lane < 8 + nr) {
+            const int r = lane - 8;
+            bulk_g2s(sp + kUnitRows * P::seg + r * 16, p.norms + (row0 + r) * G + seg * 8, 16u,
+                     &rfull[d]);
         }
+    };
+    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue(u);
+
+    int64_t u = 0;
+    for (int64_t k = 0; k < ntk; ++k) {
+        const int64_t tile = blockIdx.x + k * gridDim.x;
         float acc[TB][kRows];
 #pragma unroll
         for (int t = 0; t < TB; ++t)
 #pragma unroll
             for (int r = 0; r < kRows; ++r) acc[t][r] = 0.0f;
-        if (busy) {
 #pragma unroll
-            for (int i = 0; i < SPW; ++i) {
-                const int seg = slot + i * kWarps2;
-                if (seg >= p.nseg) break;
-                const bool active = seg * kSeg + lane * 32 < p.K;
-                uint32_t wd[kRows][BITS];
-                float nrm[kRows];
+        for (int i = 0; i < SPW; ++i) {
+            if (i >= nown) break;
+            const int seg = slot + i * kWarps2;
+            const bool active = seg * kSeg + lane * 32 < p.K;
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) {
-                    const int64_t row = row0 + r;
-                    if (active && row < p.N) {
-                        load_packed<BITS>(wd[r], p.packed + row * rowbytes +
-                                                     (int64_t)seg * (128 * BITS) + lane * (4 * BITS));
-                        nrm[r] = f16_bits_to_f32(__ldg(p.norms + row * G + seg * 8 + (lane >> 2)));
-                    } else {
+            for (int h = 0; h < 2; ++h, ++u) {
+                if (u + kRing - 1 < U) {
+                    fence_proxy_async();   // reads of the slot about to be refilled are done
+                    __syncwarp();
+                    issue(u + kRing - 1);
+                }
+                const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows + h * kUnitRows;
+                const int d = (int)(u % kRing);
+                const uint8_t* sp = ring + d * P::slot;
+                float nrm[kUnitRows];
+                if (!nbulk) {
 #pragma unroll
-                        for (int k = 0; k < BITS; ++k) wd[r][k] = 0u;
-                        nrm[r] = 0.0f;
-                    }
+                    for (int r = 0; r < kUnitRows; ++r)
+                        nrm[r] = (active && row0 + r < p.N)
+                                     ? f16_bits_to_f32(__ldg(p.norms + (row0 + r) * G + seg * 8 + (lane >> 2)))
+                                     : 0.0f;
+                }
+                mbar_wait(&rfull[d], (uint32_t)((u / kRing) & 1), p.err);
+                if (nbulk) {
+                    const uint16_t* sn = reinterpret_cast<const uint16_t*>(sp + kUnitRows * P::seg);
+#pragma unroll
+                    for (int r = 0; r < kUnitRows; ++r)
+                        nrm[r] = (active && row0 + r < p.N) ? f16_bits_to_f32(sn[r * 8 + (lane >> 2)]) : 0.0f;
                 }
 #pragma unroll
-                for (int r = 0; r < kRows; ++r) {
+                for (int r = 0; r < kUnitRows; ++r) {
+                    uint32_t wd[BITS];
+                    lds_packed<BITS>(wd, sp + r * P::seg + lane * (4 * BITS));
                     float2 d2[TB];
 #pragma unroll
                     for (int t = 0; t < TB; ++t) d2[t] = make_float2(0.0f, 0.0f);
                     if constexpr (BITS == 4) {
-                        // byte j of a word -> table offset (byte << 8) | (lane << 3): the
-                        // lane's own copy of entry `byte`, one LOP3 (plus a shift for j != 1)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t wv = wd[r][k];
-                            const uint32_t off[4] = {((wv << 8) & 0xFF00u) | lane8, (wv & 0xFF00u) | lane8,
-                                                     ((wv >> 8) & 0xFF00u) | lane8,
-                                                     ((wv >> 16) & 0xFF00u) | lane8};
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint32_t wv = wd[kk];
+                            const float2 c0 = lds_f2(pair_addr<0>(wv, lb));
+                            const float2 c1 = lds_f2(pair_addr<1>(wv, lb));
+                            const float2 c2 = lds_f2(pair_addr<2>(wv, lb));
+                            const float2 c3 = lds_f2(pair_addr<3>(wv, lb));
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float2 c = *reinterpret_cast<const float2*>(lut_bytes + off[j]);
-#pragma unroll
-                                for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][4 * k + j], d2[t]);
+                            for (int t = 0; t < TB; ++t) {
+                                d2[t] = __ffma2_rn(c0, xx[i][t][4 * kk], d2[t]);
+                                d2[t] = __ffma2_rn(c1, xx[i][t][4 * kk + 1], d2[t]);
+                                d2[t] = __ffma2_rn(c2, xx[i][t][4 * kk + 2], d2[t]);
+                                d2[t] = __ffma2_rn(c3, xx[i][t][4 * kk + 3], d2[t]);
                             }
                         }
                     } else {
 #pragma unroll
                         for (int q = 0; q < 16; ++q) {
-                            const float2 c = mylut[extract_bits<2 * BITS>(wd[r], q) << 5];
+                            const float2 c = mylut[extract_bits<2 * BITS>(wd, q) << 5];
 #pragma unroll
                             for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][q], d2[t]);
                         }
                     }
 #pragma unroll
-                    for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(nrm[r], d2[t].x + d2[t].y, acc[t][r]);
+                    for (int t = 0; t < TB; ++t)
+                        acc[t][h * kUnitRows + r] = fmaf(nrm[r], d2[t].x + d2[t].y, acc[t][h * kUnitRows + r]);
                 }
             }
         }
-        tile_reduce<TB>(rd, acc, it, w, lane, nsl, tile_rows, p.ntok, p.err,
+        tile_reduce<TB>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
                         [&](int t, int rr, float sum) {
                             const int64_t row = tile * tile_rows + rr;
                             if (row < p.N) {
@@ -378,13 +530,13 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
 
 // ---------------------------------------------------------------------------------
 // A8: Q4_0 GEMV.  Same persistent layout; lane l of a segment owns block 32 seg + l of
-// every row.  The 18-byte blocks of a row segment are staged in the warp's shared
-// buffer - by double-buffered bulk copies (cp.async.bulk, one per row) when rows and
-// segments are 16-byte aligned, else by guarded 16-byte loads - and each lane reads its
-// block with five aligned 32-bit loads.  A nibble is decoded without a table: one byte
-// permute drops it into the mantissa of 128.0f, giving exactly 128 + nib; an even/odd
-// pair multiplies the activation pair with one fp32x2 FMA; the constant 128 (and the -8
-// of the format) is removed per block with a precomputed sum of the activations.
+// every row.  The 18-byte blocks of a row segment are staged in shared memory - through
+// the warp's ring when rows and segments are 16-byte aligned, else by guarded 16-byte
+// loads into one buffer per warp - and each lane reads its block with five aligned
+// 32-bit loads.  A nibble is decoded without a table: one byte permute drops it into
+// the mantissa of 128.0f, giving exactly 128 + nib; an even/odd pair multiplies the
+// activation pair with one fp32x2 FMA; the constant 128 (and the -8 of the format) is
+// removed per block with a precomputed sum of the activations.
 // ---------------------------------------------------------------------------------
 struct Q40GemvParams {
     const uint8_t* blocks;
@@ -400,7 +552,8 @@ struct Q40GemvParams {
     int t0, ntok;
 };
 
-constexpr int kStage = 608;  // >= 37 chunks of 16 B, per row
+constexpr int kStage = 608;     // >= 37 chunks of 16 B, per row (unaligned staging)
+constexpr int kQSeg = 576;      // 32 blocks of 18 B (ring staging)
 
 template <int TB>
 __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint32_t nsh,
@@ -436,27 +589,10 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
     for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(d, (s2[t].x + s2[t].y) - cblk[t], acc[t][r]);
 }
 
-template <int TB, int SPW, bool BULK>
-__global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_kernel(const Q40GemvParams p) {
-    extern __shared__ __align__(16) uint8_t smem_q[];
-    constexpr int kBufs = BULK ? 2 : 1;
-    uint8_t* stage = smem_q;                                              // [16][kBufs][8][608]
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kBufs * kRows * kStage);  // [16][2]
-    Reduce rd;
-    rd.part = reinterpret_cast<float*>(tma_bar + 2 * kWarps2);
-    rd.full = reinterpret_cast<uint64_t*>(rd.part + kSlots * kWarps2 * TB * kRows);
-    rd.empty = rd.full + kSlots;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (tid == 0) {
-        init_reduce_bars(rd);
-        for (int i = 0; i < 2 * kWarps2; ++i) mbar_init(&tma_bar[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
-    const int slot = w % nsl, rgi = w / nsl;
-    const bool busy = rgi < p.rg;
-    float2 xx[SPW][TB][16];
-    float cblk[SPW][TB];
+// Activation pairs of this lane's blocks and their block sums (x 136), zero outside K.
+template <int TB, int SPW>
+__device__ __forceinline__ void q4_load_x(const Q40GemvParams& p, int slot, bool busy, int lane,
+                                          float2 (&xx)[SPW][TB][16], float (&cblk)[SPW][TB]) {
 #pragma unroll
     for (int i = 0; i < SPW; ++i) {
         const int seg = slot + i * kWarps2;
@@ -478,40 +614,129 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_kernel(const Q40Gem
             cblk[i][t] = 136.0f * (se + so);
         }
     }
-    __syncthreads();
+}
 
-    uint8_t* mystage = stage + w * (kBufs * kRows * kStage);
-    uint64_t* mybar = tma_bar + 2 * w;
+// Ring-staged Q4_0 GEMV: needs 16-byte aligned row segments (nblk a multiple of 8).
+template <int TB, int SPW>
+__global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q40GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem_q[];
+    constexpr int kSlotB = kUnitRows * kQSeg;
+    uint8_t* rings = smem_q;                                                   // [16][kRing][4][576]
+    uint64_t* rbar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kRing * kSlotB);  // [16][kRing]
+    const Reduce rd = carve_reduce(rbar + kWarps2 * kRing, TB);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) {
+        init_reduce(rd);
+        for (int i = 0; i < kWarps2 * kRing; ++i) mbar_init(&rbar[i], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
+    const int slot = w % nsl, rgi = w / nsl;
+    const bool busy = rgi < p.rg;
+    const uint32_t nbusy = (uint32_t)(nsl * p.rg);
+    float2 xx[SPW][TB][16];
+    float cblk[SPW][TB];
+    q4_load_x<TB, SPW>(p, slot, busy, lane, xx, cblk);
+    __syncthreads();
+    if (!busy) return;   // warps left over when the segments do not divide 16
+
+    uint8_t* ring = rings + w * (kRing * kSlotB);
+    uint64_t* rfull = rbar + w * kRing;
+    const int64_t rowbytes = (int64_t)p.nblk * 18;
+    const int tile_rows = kRows * p.rg;
+    const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
+    const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int nown = (SPW == 2 && slot + kWarps2 < p.nseg) ? 2 : 1;
+    const int upt = 2 * nown;
+    const int64_t U = ntk * upt;
+
+    auto issue = [&](int64_t u) {
+        const int64_t k = u / upt;
+        const int rem = (int)(u - k * upt);
+        const int seg = slot + (rem >> 1) * kWarps2;
+        const int64_t row0 = (blockIdx.x + k * gridDim.x) * tile_rows + (int64_t)rgi * kRows +
+                             (rem & 1) * kUnitRows;
+        const int64_t left = p.N - row0;
+        const int nr = left >= kUnitRows ? kUnitRows : (left > 0 ? (int)left : 0);
+        const int nb = min(32, p.nblk - seg * 32);
+        const int d = (int)(u % kRing);
+        if (lane == 0) mbar_arrive_tx(&rfull[d], (uint32_t)(nr * nb * 18));
+        __syncwarp();
+        if (lane < nr)
+            bulk_g2s(ring + d * kSlotB + lane * kQSeg, p.blocks + (row0 + lane) * rowbytes + (int64_t)seg * kQSeg,
+                     (uint32_t)(nb * 18), &rfull[d]);
+    };
+    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue(u);
+
+    // every staged row starts at byte 0: per-lane word offset and shifts
+    const int o = lane * 18;
+    const uint32_t dsh = (uint32_t)(o & 3) * 8u;
+    int64_t u = 0;
+    for (int64_t k = 0; k < ntk; ++k) {
+        const int64_t tile = blockIdx.x + k * gridDim.x;
+        float acc[TB][kRows];
+#pragma unroll
+        for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) acc[t][r] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < SPW; ++i) {
+            if (i >= nown) break;
+            const int seg = slot + i * kWarps2;
+            const int nb = min(32, p.nblk - seg * 32);
+#pragma unroll
+            for (int h = 0; h < 2; ++h, ++u) {
+                if (u + kRing - 1 < U) {
+                    fence_proxy_async();   // reads of the slot about to be refilled are done
+                    __syncwarp();
+                    issue(u + kRing - 1);
+                }
+                const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows + h * kUnitRows;
+                const int d = (int)(u % kRing);
+                mbar_wait(&rfull[d], (uint32_t)((u / kRing) & 1), p.err);
+                if (lane < nb) {
+                    const uint32_t* wl = reinterpret_cast<const uint32_t*>(ring + d * kSlotB) + (o >> 2);
+#pragma unroll
+                    for (int r = 0; r < kUnitRows; ++r)
+                        if (row0 + r < p.N)
+                            q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, h * kUnitRows + r);
+                }
+            }
+        }
+        tile_reduce<TB>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
+                        [&](int t, int rr, float sum) {
+                            const int64_t row = tile * tile_rows + rr;
+                            if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
+                        });
+    }
+}
+
+// Q4_0 GEMV for rows that are not 16-byte aligned: guarded 16-byte loads into one
+// staging buffer of kRows rows per warp.
+template <int TB, int SPW>
+__global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_rows_kernel(const Q40GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem_q[];
+    uint8_t* stage = smem_q;                                              // [16][8][608]
+    const Reduce rd = carve_reduce(smem_q + kWarps2 * kRows * kStage, TB);
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) init_reduce(rd);
+    const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
+    const int slot = w % nsl, rgi = w / nsl;
+    const bool busy = rgi < p.rg;
+    const uint32_t nbusy = (uint32_t)(nsl * p.rg);
+    float2 xx[SPW][TB][16];
+    float cblk[SPW][TB];
+    q4_load_x<TB, SPW>(p, slot, busy, lane, xx, cblk);
+    __syncthreads();
+    if (!busy) return;
+
+    uint8_t* mystage = stage + w * (kRows * kStage);
     const int64_t rowbytes = (int64_t)p.nblk * 18;
     const int tile_rows = kRows * p.rg;
     const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
     const uintptr_t base_addr = reinterpret_cast<uintptr_t>(p.blocks);
     const uintptr_t end_addr = base_addr + (uintptr_t)p.total_bytes;
-
-    // bulk staging: unit u = (tile number, owned segment i) in order; buffer u % 2
-    auto issue_bulk = [&](int64_t tile, int i, int bufi) {
-        const int seg = slot + i * kWarps2;
-        const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
-        const int nb = min(32, p.nblk - seg * 32);
-        int nrows = 0;
-        for (int r = 0; r < kRows; ++r) nrows += (row0 + r < p.N) ? 1 : 0;
-        if (lane == 0) mbar_arrive_tx(&mybar[bufi], (uint32_t)(nrows * nb * 18));
-        __syncwarp();
-        if (lane < nrows) {
-            const uint8_t* src = p.blocks + (row0 + lane) * rowbytes + (int64_t)seg * 576;
-            uint8_t* dst = mystage + (bufi * kRows + lane) * kStage;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    smem_u32(dst)),
-                "l"(src), "r"((uint32_t)(nb * 18)), "r"(smem_u32(&mybar[bufi]))
-                : "memory");
-        }
-    };
-    int units_total = 0;   // per-warp count of bulk units issued (for buffer parity)
     int it = 0;
-    if (BULK && busy && blockIdx.x < ntiles) {
-        if (slot < p.nseg) { issue_bulk(blockIdx.x, 0, 0); }
-    }
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
         const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows;
         float acc[TB][kRows];
@@ -519,86 +744,53 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_kernel(const Q40Gem
         for (int t = 0; t < TB; ++t)
 #pragma unroll
             for (int r = 0; r < kRows; ++r) acc[t][r] = 0.0f;
-        if (busy) {
 #pragma unroll
-            for (int i = 0; i < SPW; ++i) {
-                const int seg = slot + i * kWarps2;
-                if (seg >= p.nseg) break;
-                const int nb = min(32, p.nblk - seg * 32);
-                const uint8_t* rowbufs;
-                int offs[kRows];
-                if constexpr (BULK) {
-                    const int bufi = units_total & 1;
-                    const uint32_t par = (uint32_t)((units_total >> 1) & 1);
-                    // issue the next unit into the other buffer before waiting for this one
-                    {
-                        int ni = i + 1;
-                        int64_t nt = tile;
-                        if (ni >= SPW || slot + ni * kWarps2 >= p.nseg) { ni = 0; nt = tile + gridDim.x; }
-                        __syncwarp();
-                        if (nt < ntiles) issue_bulk(nt, ni, bufi ^ 1);
-                    }
-                    mbar_wait(&mybar[bufi], par, p.err);
-                    rowbufs = mystage + bufi * kRows * kStage;
+        for (int i = 0; i < SPW; ++i) {
+            const int seg = slot + i * kWarps2;
+            if (seg >= p.nseg) break;
+            const int nb = min(32, p.nblk - seg * 32);
+            int offs[kRows];
+            __syncwarp();
 #pragma unroll
-                    for (int r = 0; r < kRows; ++r) offs[r] = 0;
-                    ++units_total;
-                } else {
-                    __syncwarp();
-#pragma unroll
-                    for (int r = 0; r < kRows; ++r) {
-                        const int64_t row = row0 + r;
-                        offs[r] = 0;
-                        if (row >= p.N) continue;
-                        const uintptr_t a = base_addr + (uintptr_t)(row * rowbytes + (int64_t)seg * 576);
-                        const uintptr_t start = a & ~(uintptr_t)15;
-                        offs[r] = (int)(a - start);
-                        const int chunks = (int)((a + (uintptr_t)nb * 18 - start + 15) >> 4);
-                        for (int c = lane; c < chunks; c += 32) {
-                            const uintptr_t q = start + (uintptr_t)c * 16;
-                            uint4 v;
-                            if (q + 16 <= end_addr) {
-                                v = __ldcs(reinterpret_cast<const uint4*>(q));
-                            } else {
-                                uint8_t tmp[16];
-#pragma unroll
-                                for (int k = 0; k < 16; ++k)
-                                    tmp[k] = (q + k < end_addr) ? *reinterpret_cast<const uint8_t*>(q + k) : 0;
-                                v = make_uint4(tmp[0] | tmp[1] << 8 | tmp[2] << 16 | (uint32_t)tmp[3] << 24,
-                                               tmp[4] | tmp[5] << 8 | tmp[6] << 16 | (uint32_t)tmp[7] << 24,
-                                               tmp[8] | tmp[9] << 8 | tmp[10] << 16 | (uint32_t)tmp[11] << 24,
-                                               tmp[12] | tmp[13] << 8 | tmp[14] << 16 | (uint32_t)tmp[15] << 24);
-                            }
-                            *reinterpret_cast<uint4*>(mystage + r * kStage + c * 16) = v;
-                        }
-                    }
-                    __syncwarp();
-                    rowbufs = mystage;
-                }
-                if (lane < nb) {
-                    if constexpr (BULK) {
-                        // every staged row starts at byte 0: per-lane word offset and shifts
-                        const int o = lane * 18;
-                        const uint32_t dsh = (uint32_t)(o & 3) * 8u;
-                        const uint32_t* wl = reinterpret_cast<const uint32_t*>(rowbufs) + (o >> 2);
-#pragma unroll
-                        for (int r = 0; r < kRows; ++r)
-                            if (row0 + r < p.N)
-                                q4_block<TB>(wl + r * (kStage / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, r);
+            for (int r = 0; r < kRows; ++r) {
+                const int64_t row = row0 + r;
+                offs[r] = 0;
+                if (row >= p.N) continue;
+                const uintptr_t a = base_addr + (uintptr_t)(row * rowbytes + (int64_t)seg * kQSeg);
+                const uintptr_t start = a & ~(uintptr_t)15;
+                offs[r] = (int)(a - start);
+                const int chunks = (int)((a + (uintptr_t)nb * 18 - start + 15) >> 4);
+                for (int c = lane; c < chunks; c += 32) {
+                    const uintptr_t q = start + (uintptr_t)c * 16;
+                    uint4 v;
+                    if (q + 16 <= end_addr) {
+                        v = __ldcs(reinterpret_cast<const uint4*>(q));
                     } else {
+                        uint8_t tmp[16];
 #pragma unroll
-                        for (int r = 0; r < kRows; ++r) {
-                            if (row0 + r >= p.N) continue;
-                            const int o = offs[r] + lane * 18;
-                            const uint32_t dsh = (uint32_t)(o & 3) * 8u;
-                            const uint32_t* wl = reinterpret_cast<const uint32_t*>(rowbufs + r * kStage) + (o >> 2);
-                            q4_block<TB>(wl, dsh, dsh + 16u, xx[i], cblk[i], acc, r);
-                        }
+                        for (int kk = 0; kk < 16; ++kk)
+                            tmp[kk] = (q + kk < end_addr) ? *reinterpret_cast<const uint8_t*>(q + kk) : 0;
+                        v = make_uint4(tmp[0] | tmp[1] << 8 | tmp[2] << 16 | (uint32_t)tmp[3] << 24,
+                                       tmp[4] | tmp[5] << 8 | tmp[6] << 16 | (uint32_t)tmp[7] << 24,
+                                       tmp[8] | tmp[9] << 8 | tmp[10] << 16 | (uint32_t)tmp[11] << 24,
+                                       tmp[12] | tmp[13] << 8 | tmp[14] << 16 | (uint32_t)tmp[15] << 24);
                     }
+                    *reinterpret_cast<uint4*>(mystage + r * kStage + c * 16) = v;
+                }
+            }
+            __syncwarp();
+            if (lane < nb) {
+#pragma unroll
+                for (int r = 0; r < kRows; ++r) {
+                    if (row0 + r >= p.N) continue;
+                    const int o = offs[r] + lane * 18;
+                    const uint32_t dsh = (uint32_t)(o & 3) * 8u;
+                    const uint32_t* wl = reinterpret_cast<const uint32_t*>(mystage + r * kStage) + (o >> 2);
+                    q4_block<TB>(wl, dsh, dsh + 16u, xx[i], cblk[i], acc, r);
                 }
             }
         }
-        tile_reduce<TB>(rd, acc, it, w, lane, nsl, tile_rows, p.ntok, p.err,
+        tile_reduce<TB>(rd, acc, it, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
                         [&](int t, int rr, float sum) {
                             const int64_t row = tile * tile_rows + rr;
                             if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
@@ -655,7 +847,8 @@ template <int BITS, int TB, int SPW>
 cq_status run_cq_gemv(CqGemvParams p, cudaStream_t st) {
     static bool attr = false;
     auto kern = cq_gemv_kernel<BITS, TB, SPW>;
-    const size_t smem = (size_t)(1 << (2 * BITS)) * 32 * sizeof(float2) + reduce_bytes(TB);
+    const size_t smem = cq_smem_bytes<BITS>(TB);
+    p.smem_bytes = (uint32_t)smem;
     const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int grid = 0;
     const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
@@ -664,12 +857,12 @@ cq_status run_cq_gemv(CqGemvParams p, cudaStream_t st) {
     return check_launch();
 }
 
-template <int TB, int SPW, bool BULK>
+template <int TB, int SPW, bool RING>
 cq_status run_q4_0_gemv(Q40GemvParams p, cudaStream_t st) {
     static bool attr = false;
-    auto kern = q4_0_gemv_kernel<TB, SPW, BULK>;
-    const size_t smem = (size_t)kWarps2 * (BULK ? 2 : 1) * kRows * kStage +
-                        2 * kWarps2 * sizeof(uint64_t) + reduce_bytes(TB);
+    auto kern = RING ? q4_0_gemv_ring_kernel<TB, SPW> : q4_0_gemv_rows_kernel<TB, SPW>;
+    const size_t smem = RING ? (size_t)kWarps2 * kRing * kUnitRows * kQSeg + kWarps2 * kRing * 8 + reduce_bytes(TB)
+                             : (size_t)kWarps2 * kRows * kStage + reduce_bytes(TB);
     const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int grid = 0;
     const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
@@ -781,7 +974,7 @@ extern "C" cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, cons
         if (se != CQ_OK) return se;
     }
     p.err = err;
-    // bulk-copy staging needs 16-byte aligned row segments: 8 | nblk
+    // ring staging by bulk copies needs 16-byte aligned row segments: 8 | nblk
     const bool bulk = (p.nblk % 8) == 0;
     const int spw = (p.nseg + kWarps2 - 1) / kWarps2;
     p.rg = row_groups(p.nseg);
