@@ -325,7 +325,8 @@ struct CqPlan {
 template <int BITS>
 size_t cq_smem_bytes(int tb) {
     using P = CqPlan<BITS>;
-    const size_t rest = reduce_bytes(tb) + 16 + kWarps2 * kRing * 8 + 8 + (size_t)kWarps2 * (P::ring + 128);
+    const size_t rest = reduce_bytes(tb) + 16 + kWarps2 * kRing * 8 + 8 + 64 + 16 +
+                        (size_t)kWarps2 * (P::ring + 128);
     // 4-bit: the table is 64 KB aligned; the space below it may be too small to use
     if (BITS == 4) return 227 * 1024;
     return P::table + 16 + rest;
@@ -352,6 +353,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     if (tbase + P::table > send) cv.ok = false;
     const uint32_t red_at = cv.take((uint32_t)reduce_bytes(TB), 16);
     const uint32_t bar_at = cv.take(kWarps2 * kRing * 8, 8);
+    const uint32_t lv_at = cv.take(16 * sizeof(float), 16);
     uint32_t ring_at = 0;
     for (int v = 0; v < kWarps2; ++v) {
         const uint32_t at = cv.take(P::ring, 128);
@@ -365,47 +367,26 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     float2* lut2 = reinterpret_cast<float2*>(gen(tbase));                 // [E][32]
     const Reduce rd = carve_reduce(gen(red_at), TB);
     uint64_t* rfull = reinterpret_cast<uint64_t*>(gen(bar_at)) + w * kRing;
+    float* slv = reinterpret_cast<float*>(gen(lv_at));
     uint8_t* ring = gen(ring_at);
-    for (int i = tid; i < E * 32; i += kWarps2 * 32) {
-        const int e = i >> 5;
-        float a = 0.0f, b = 0.0f;
-#pragma unroll
-        for (int u = 0; u < L; ++u) {
-            a = (u == (e & (L - 1))) ? p.lv[u] : a;
-            b = (u == (e >> BITS)) ? p.lv[u] : b;
-        }
-        lut2[i] = make_float2(a, b);
-    }
     if (tid == 0) {
         init_reduce(rd);
         uint64_t* all = reinterpret_cast<uint64_t*>(gen(bar_at));
         for (int i = 0; i < kWarps2 * kRing; ++i) mbar_init(&all[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (tid < 16) {   // the levels, by an unrolled select (no indexed parameter access)
+        float v = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v = (u == tid) ? p.lv[u] : v;
+        slv[tid] = v;
+    }
+    __syncthreads();
+
     const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
     const int slot = w % nsl, rgi = w / nsl;
     const uint32_t nbusy = (uint32_t)(nsl * p.rg);
-    float2 xx[SPW][TB][16];
-#pragma unroll
-    for (int i = 0; i < SPW; ++i) {
-        const int seg = slot + i * kWarps2;
-        const int pos0 = seg * kSeg + lane * 32;
-#pragma unroll
-        for (int t = 0; t < TB; ++t) {
-            const bool ok = rgi < p.rg && seg < p.nseg && pos0 < p.K && t < p.ntok;
-            const float* src = p.xr + (int64_t)(p.t0 + t) * p.K + pos0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = ok ? *reinterpret_cast<const float4*>(src + 4 * q)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                xx[i][t][2 * q] = make_float2(v.x, v.y);
-                xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
-            }
-        }
-    }
-    __syncthreads();
-    if (rgi >= p.rg) return;   // warps left over when the segments do not divide 16
-
+    const bool busy = rgi < p.rg;
     const int G = p.K / kGroup;
     const int64_t rowbytes = (int64_t)G * 16 * BITS;
     const int tile_rows = kRows * p.rg;
@@ -413,10 +394,8 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int nown = (SPW == 2 && slot + kWarps2 < p.nseg) ? 2 : 1;   // owned segments
     const int upt = 2 * nown;                                           // units per tile
-    const int64_t U = ntk * upt;
+    const int64_t U = busy ? ntk * upt : 0;
     const bool nbulk = (p.K % kSeg) == 0;   // a segment's norms are 16 aligned bytes
-    const float2* mylut = lut2 + lane;
-    const uint32_t lb = tbase | ((uint32_t)lane << 3);
 
     auto issue = [&](int64_t u) {
         const int64_t k = u / upt;
@@ -440,8 +419,36 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                      &rfull[d]);
         }
     };
+    // the first units are in flight while the table and the activations are set up
     for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue(u);
 
+    for (int i = tid; i < E * 32; i += kWarps2 * 32) {
+        const int e = i >> 5;
+        lut2[i] = make_float2(slv[e & (L - 1)], slv[e >> BITS]);
+    }
+    float2 xx[SPW][TB][16];
+#pragma unroll
+    for (int i = 0; i < SPW; ++i) {
+        const int seg = slot + i * kWarps2;
+        const int pos0 = seg * kSeg + lane * 32;
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            const bool ok = busy && seg < p.nseg && pos0 < p.K && t < p.ntok;
+            const float* src = p.xr + (int64_t)(p.t0 + t) * p.K + pos0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 v = ok ? *reinterpret_cast<const float4*>(src + 4 * q)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                xx[i][t][2 * q] = make_float2(v.x, v.y);
+                xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
+            }
+        }
+    }
+    __syncthreads();
+    if (!busy) return;   // warps left over when the segments do not divide 16
+
+    const float2* mylut = lut2 + lane;
+    const uint32_t lb = tbase | ((uint32_t)lane << 3);
     int64_t u = 0;
     for (int64_t k = 0; k < ntk; ++k) {
         const int64_t tile = blockIdx.x + k * gridDim.x;
@@ -589,7 +596,8 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
     for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(d, (s2[t].x + s2[t].y) - cblk[t], acc[t][r]);
 }
 
-// Activation pairs of this lane's blocks and their block sums (x 136), zero outside K.
+// Activation pairs of this lane's blocks and their block sums (x 136), zero outside K;
+// 16-byte loads where the block lies inside K and rows of X are 16-byte aligned.
 template <int TB, int SPW>
 __device__ __forceinline__ void q4_load_x(const Q40GemvParams& p, int slot, bool busy, int lane,
                                           float2 (&xx)[SPW][TB][16], float (&cblk)[SPW][TB]) {
@@ -600,16 +608,27 @@ __device__ __forceinline__ void q4_load_x(const Q40GemvParams& p, int slot, bool
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
             const bool ok = busy && seg < p.nseg && blk < p.nblk && t < p.ntok;
-            const float* src = p.X + (int64_t)(p.t0 + t) * p.K;
+            const float* src = p.X + (int64_t)(p.t0 + t) * p.K + blk * 32;
             float se = 0.0f, so = 0.0f;
+            if (ok && (p.K & 3) == 0 && blk * 32 + 32 <= p.K) {
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const int k0 = blk * 32 + 2 * q;
-                const float a = (ok && k0 < p.K) ? src[k0] : 0.0f;
-                const float b = (ok && k0 + 1 < p.K) ? src[k0 + 1] : 0.0f;
-                xx[i][t][q] = make_float2(a, b);
-                se += a;
-                so += b;
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(src) + q);
+                    xx[i][t][2 * q] = make_float2(v.x, v.y);
+                    xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
+                    se += v.x + v.z;
+                    so += v.y + v.w;
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int k0 = blk * 32 + 2 * q;
+                    const float a = (ok && k0 < p.K) ? src[2 * q] : 0.0f;
+                    const float b = (ok && k0 + 1 < p.K) ? src[2 * q + 1] : 0.0f;
+                    xx[i][t][q] = make_float2(a, b);
+                    se += a;
+                    so += b;
+                }
             }
             cblk[i][t] = 136.0f * (se + so);
         }
@@ -630,15 +649,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q
         for (int i = 0; i < kWarps2 * kRing; ++i) mbar_init(&rbar[i], 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
     const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
     const int slot = w % nsl, rgi = w / nsl;
-    const bool busy = rgi < p.rg;
+    if (rgi >= p.rg) return;   // warps left over when the segments do not divide 16
     const uint32_t nbusy = (uint32_t)(nsl * p.rg);
-    float2 xx[SPW][TB][16];
-    float cblk[SPW][TB];
-    q4_load_x<TB, SPW>(p, slot, busy, lane, xx, cblk);
-    __syncthreads();
-    if (!busy) return;   // warps left over when the segments do not divide 16
 
     uint8_t* ring = rings + w * (kRing * kSlotB);
     uint64_t* rfull = rbar + w * kRing;
@@ -666,7 +681,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q
             bulk_g2s(ring + d * kSlotB + lane * kQSeg, p.blocks + (row0 + lane) * rowbytes + (int64_t)seg * kQSeg,
                      (uint32_t)(nb * 18), &rfull[d]);
     };
+    // the first units are in flight while the activations are loaded
     for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue(u);
+    float2 xx[SPW][TB][16];
+    float cblk[SPW][TB];
+    q4_load_x<TB, SPW>(p, slot, true, lane, xx, cblk);
 
     // every staged row starts at byte 0: per-lane word offset and shifts
     const int o = lane * 18;
