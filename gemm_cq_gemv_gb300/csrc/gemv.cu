@@ -219,7 +219,8 @@ __device__ __forceinline__ Reduce carve_reduce(void* base, int tb) {
 // latency overlaps the decode instead of following it.
 // ---------------------------------------------------------------------------------
 constexpr int kUnitRows = 4;
-constexpr int kRing = 4;
+constexpr int kRing = 4;       // a power of two (slot = unit & 3, phase = unit >> 2)
+static_assert(kRing == 4, "ring slot and phase arithmetic assume 4 slots");
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -397,16 +398,15 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     const int64_t U = busy ? ntk * upt : 0;
     const bool nbulk = (p.K % kSeg) == 0;   // a segment's norms are 16 aligned bytes
 
-    auto issue = [&](int64_t u) {
-        const int64_t k = u / upt;
-        const int rem = (int)(u - k * upt);
-        const int seg = slot + (rem >> 1) * kWarps2;
-        const int64_t row0 = (blockIdx.x + k * gridDim.x) * tile_rows + (int64_t)rgi * kRows +
-                             (rem & 1) * kUnitRows;
+    // cursor of the next unit to issue (units go out strictly in order)
+    int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;   // its tile's first row
+    int nx_rem = 0;                                                             // unit within the tile
+    auto issue = [&](int d) {
+        const int seg = slot + (nx_rem >> 1) * kWarps2;
+        const int64_t row0 = nx_base + (nx_rem & 1) * kUnitRows;
         const int64_t left = p.N - row0;
         const int nr = left >= kUnitRows ? kUnitRows : (left > 0 ? (int)left : 0);
         const uint32_t bytes = min(P::seg, (uint32_t)((p.K - seg * kSeg) / 8 * BITS));
-        const int d = (int)(u % kRing);
         uint8_t* sp = ring + d * P::slot;
         if (lane == 0) mbar_arrive_tx(&rfull[d], (uint32_t)nr * (bytes + (nbulk ? 16u : 0u)));
         __syncwarp();
@@ -418,9 +418,13 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
             bulk_g2s(sp + kUnitRows * P::seg + r * 16, p.norms + (row0 + r) * G + seg * 8, 16u,
                      &rfull[d]);
         }
+        if (++nx_rem == upt) {
+            nx_rem = 0;
+            nx_base += (int64_t)gridDim.x * tile_rows;
+        }
     };
     // the first units are in flight while the table and the activations are set up
-    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue(u);
+    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
 
     for (int i = tid; i < E * 32; i += kWarps2 * 32) {
         const int e = i >> 5;
@@ -467,33 +471,35 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                 if (u + kRing - 1 < U) {
                     fence_proxy_async();   // reads of the slot about to be refilled are done
                     __syncwarp();
-                    issue(u + kRing - 1);
+                    issue((int)((u + kRing - 1) & (kRing - 1)));
                 }
                 const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows + h * kUnitRows;
-                const int d = (int)(u % kRing);
+                const int64_t left = p.N - row0;
+                const int nv = !active ? 0 : (left >= kUnitRows ? kUnitRows : (int)left);   // rows to add
+                const int d = (int)(u & (kRing - 1));
                 const uint8_t* sp = ring + d * P::slot;
                 float nrm[kUnitRows];
                 if (!nbulk) {
 #pragma unroll
                     for (int r = 0; r < kUnitRows; ++r)
-                        nrm[r] = (active && row0 + r < p.N)
-                                     ? f16_bits_to_f32(__ldg(p.norms + (row0 + r) * G + seg * 8 + (lane >> 2)))
-                                     : 0.0f;
+                        nrm[r] = r < nv ? f16_bits_to_f32(__ldg(p.norms + (row0 + r) * G + seg * 8 + (lane >> 2)))
+                                        : 0.0f;
                 }
-                mbar_wait(&rfull[d], (uint32_t)((u / kRing) & 1), p.err);
+                mbar_wait(&rfull[d], (uint32_t)(u >> 2) & 1u, p.err);
                 if (nbulk) {
                     const uint16_t* sn = reinterpret_cast<const uint16_t*>(sp + kUnitRows * P::seg);
 #pragma unroll
                     for (int r = 0; r < kUnitRows; ++r)
-                        nrm[r] = (active && row0 + r < p.N) ? f16_bits_to_f32(sn[r * 8 + (lane >> 2)]) : 0.0f;
+                        nrm[r] = r < nv ? f16_bits_to_f32(sn[r * 8 + (lane >> 2)]) : 0.0f;
                 }
 #pragma unroll
                 for (int r = 0; r < kUnitRows; ++r) {
                     uint32_t wd[BITS];
                     lds_packed<BITS>(wd, sp + r * P::seg + lane * (4 * BITS));
-                    float2 d2[TB];
+                    // two independent accumulator chains per token
+                    float2 d2[TB][2];
 #pragma unroll
-                    for (int t = 0; t < TB; ++t) d2[t] = make_float2(0.0f, 0.0f);
+                    for (int t = 0; t < TB; ++t) d2[t][0] = d2[t][1] = make_float2(0.0f, 0.0f);
                     if constexpr (BITS == 4) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -504,10 +510,10 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                             const float2 c3 = lds_f2(pair_addr<3>(wv, lb));
 #pragma unroll
                             for (int t = 0; t < TB; ++t) {
-                                d2[t] = __ffma2_rn(c0, xx[i][t][4 * kk], d2[t]);
-                                d2[t] = __ffma2_rn(c1, xx[i][t][4 * kk + 1], d2[t]);
-                                d2[t] = __ffma2_rn(c2, xx[i][t][4 * kk + 2], d2[t]);
-                                d2[t] = __ffma2_rn(c3, xx[i][t][4 * kk + 3], d2[t]);
+                                d2[t][0] = __ffma2_rn(c0, xx[i][t][4 * kk], d2[t][0]);
+                                d2[t][1] = __ffma2_rn(c1, xx[i][t][4 * kk + 1], d2[t][1]);
+                                d2[t][0] = __ffma2_rn(c2, xx[i][t][4 * kk + 2], d2[t][0]);
+                                d2[t][1] = __ffma2_rn(c3, xx[i][t][4 * kk + 3], d2[t][1]);
                             }
                         }
                     } else {
@@ -515,12 +521,13 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                         for (int q = 0; q < 16; ++q) {
                             const float2 c = mylut[extract_bits<2 * BITS>(wd, q) << 5];
 #pragma unroll
-                            for (int t = 0; t < TB; ++t) d2[t] = __ffma2_rn(c, xx[i][t][q], d2[t]);
+                            for (int t = 0; t < TB; ++t) d2[t][q & 1] = __ffma2_rn(c, xx[i][t][q], d2[t][q & 1]);
                         }
                     }
 #pragma unroll
                     for (int t = 0; t < TB; ++t)
-                        acc[t][h * kUnitRows + r] = fmaf(nrm[r], d2[t].x + d2[t].y, acc[t][h * kUnitRows + r]);
+                        acc[t][h * kUnitRows + r] =
+                            fmaf(nrm[r], (d2[t][0].x + d2[t][1].x) + (d2[t][0].y + d2[t][1].y), acc[t][h * kUnitRows + r]);
                 }
             }
         }
@@ -572,9 +579,9 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
     const float d = f16_bits_to_f32((uint16_t)(w0 >> dsh));
     const uint32_t nw[4] = {__funnelshift_rc(w0, w1, nsh), __funnelshift_rc(w1, w2, nsh),
                             __funnelshift_rc(w2, w3, nsh), __funnelshift_rc(w3, w4, nsh)};
-    float2 s2[TB];
+    float2 s2[TB][2];   // two independent accumulator chains per token
 #pragma unroll
-    for (int t = 0; t < TB; ++t) s2[t] = make_float2(0.0f, 0.0f);
+    for (int t = 0; t < TB; ++t) s2[t][0] = s2[t][1] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         // even-index nibbles (low halves of the bytes) and odd-index nibbles, one per byte
@@ -588,12 +595,13 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
             asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fo) : "r"(od), "r"(0x43000000u), "r"(sel));
             const float2 f = make_float2(__uint_as_float(fe), __uint_as_float(fo));
 #pragma unroll
-            for (int t = 0; t < TB; ++t) s2[t] = __ffma2_rn(f, xx[t][4 * k + j], s2[t]);
+            for (int t = 0; t < TB; ++t) s2[t][j & 1] = __ffma2_rn(f, xx[t][4 * k + j], s2[t][j & 1]);
         }
     }
     // sum (nib - 8) x = sum (128 + nib) x - 136 sum x
 #pragma unroll
-    for (int t = 0; t < TB; ++t) acc[t][r] = fmaf(d, (s2[t].x + s2[t].y) - cblk[t], acc[t][r]);
+    for (int t = 0; t < TB; ++t)
+        acc[t][r] = fmaf(d, ((s2[t][0].x + s2[t][1].x) + (s2[t][0].y + s2[t][1].y)) - cblk[t], acc[t][r]);
 }
 
 // Activation pairs of this lane's blocks and their block sums (x 136), zero outside K;
@@ -665,24 +673,26 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q
     const int upt = 2 * nown;
     const int64_t U = ntk * upt;
 
-    auto issue = [&](int64_t u) {
-        const int64_t k = u / upt;
-        const int rem = (int)(u - k * upt);
-        const int seg = slot + (rem >> 1) * kWarps2;
-        const int64_t row0 = (blockIdx.x + k * gridDim.x) * tile_rows + (int64_t)rgi * kRows +
-                             (rem & 1) * kUnitRows;
+    int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;
+    int nx_rem = 0;
+    auto issue = [&](int d) {
+        const int seg = slot + (nx_rem >> 1) * kWarps2;
+        const int64_t row0 = nx_base + (nx_rem & 1) * kUnitRows;
         const int64_t left = p.N - row0;
         const int nr = left >= kUnitRows ? kUnitRows : (left > 0 ? (int)left : 0);
         const int nb = min(32, p.nblk - seg * 32);
-        const int d = (int)(u % kRing);
         if (lane == 0) mbar_arrive_tx(&rfull[d], (uint32_t)(nr * nb * 18));
         __syncwarp();
         if (lane < nr)
             bulk_g2s(ring + d * kSlotB + lane * kQSeg, p.blocks + (row0 + lane) * rowbytes + (int64_t)seg * kQSeg,
                      (uint32_t)(nb * 18), &rfull[d]);
+        if (++nx_rem == upt) {
+            nx_rem = 0;
+            nx_base += (int64_t)gridDim.x * tile_rows;
+        }
     };
     // the first units are in flight while the activations are loaded
-    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue(u);
+    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
     float2 xx[SPW][TB][16];
     float cblk[SPW][TB];
     q4_load_x<TB, SPW>(p, slot, true, lane, xx, cblk);
@@ -708,18 +718,17 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q
                 if (u + kRing - 1 < U) {
                     fence_proxy_async();   // reads of the slot about to be refilled are done
                     __syncwarp();
-                    issue(u + kRing - 1);
+                    issue((int)((u + kRing - 1) & (kRing - 1)));
                 }
-                const int64_t row0 = tile * tile_rows + (int64_t)rgi * kRows + h * kUnitRows;
-                const int d = (int)(u % kRing);
-                mbar_wait(&rfull[d], (uint32_t)((u / kRing) & 1), p.err);
-                if (lane < nb) {
-                    const uint32_t* wl = reinterpret_cast<const uint32_t*>(ring + d * kSlotB) + (o >> 2);
+                const int64_t left = p.N - (tile * tile_rows + (int64_t)rgi * kRows + h * kUnitRows);
+                const int nv = lane >= nb ? 0 : (left >= kUnitRows ? kUnitRows : (int)left);   // rows to add
+                const int d = (int)(u & (kRing - 1));
+                mbar_wait(&rfull[d], (uint32_t)(u >> 2) & 1u, p.err);
+                const uint32_t* wl = reinterpret_cast<const uint32_t*>(ring + d * kSlotB) + (o >> 2);
 #pragma unroll
-                    for (int r = 0; r < kUnitRows; ++r)
-                        if (row0 + r < p.N)
-                            q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, h * kUnitRows + r);
-                }
+                for (int r = 0; r < kUnitRows; ++r)
+                    if (r < nv)
+                        q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, h * kUnitRows + r);
             }
         }
         tile_reduce<TB>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
