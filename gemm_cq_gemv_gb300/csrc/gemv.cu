@@ -11,6 +11,9 @@
 //   * warps are persistent (grid-stride over tiles) and the activations of the call
 //     sit in shared memory, loaded once per CTA.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -214,20 +217,27 @@ __device__ __forceinline__ Reduce carve_reduce(void* base, int tb) {
 // ---------------------------------------------------------------------------------
 // Per-warp staging ring.  Each warp streams its own rows through kRing slots of shared
 // memory, one slot per unit of kUnitRows rows (half a warp tile) of one owned segment,
-// filled by bulk copies (cp.async.bulk, one per row) that complete on the slot's
-// mbarrier.  While a unit is decoded the next kRing - 1 are in flight, so the load
-// latency overlaps the decode instead of following it.
+// filled by one 2-D tensor copy (cp.async.bulk.tensor, issued by one lane) that
+// completes on the slot's mbarrier.  While a unit is decoded the next kRing - 1 are in
+// flight, so the load latency overlaps the decode instead of following it.
 // ---------------------------------------------------------------------------------
 constexpr int kUnitRows = 4;
+// row coordinates of the tensor copies are 32-bit (with a tile of slack past N)
+constexpr int64_t kMaxGemvRows = ((int64_t)1 << 31) - 1024;
 constexpr int kRing = 4;       // a power of two (slot = unit & 3, phase = unit >> 2)
 static_assert(kRing == 4, "ring slot and phase arithmetic assume 4 slots");
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+// 2-D tensor copy of one box (rows outside the tensor and columns past its end read as
+// zero and still count toward the transaction bytes)
+__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 // orders this thread's earlier shared-memory reads before later bulk copies into them
 __device__ __forceinline__ void fence_proxy_async() {
@@ -254,12 +264,14 @@ struct SmemCarve {
 // Codewords come from a shared-memory table indexed by two consecutive indices (2b
 // bits): entry e = (cb[e mod 2^b], cb[e / 2^b]), replicated once per bank so every lane
 // reads its own copy (conflict-free 64-bit loads); the pair multiplies a pair of
-// activations with one packed fp32x2 FMA.  For 4-bit indices the table sits at a 64 KB
+// activations with two scalar FMAs.  For 4-bit indices the table sits at a 64 KB
 // boundary of the shared window, so the address of (entry e, lane l), base | e << 8 |
 // l << 3, is one byte permute of an index byte into the lane's base.  The packed rows
 // and their group norms arrive through the warp's staging ring.
 // ---------------------------------------------------------------------------------
 struct CqGemvParams {
+    CUtensorMap pmap;     // packed rows as [N][rowbytes / 4] uint32, box 32 b x kUnitRows
+    CUtensorMap nmap;     // norms as [N][K / 128] fp16, box 8 x kUnitRows (when K % 1024 == 0)
     const uint8_t* packed;
     const uint16_t* norms;
     const float* xr;      // [B][K] rotated activations
@@ -314,11 +326,13 @@ __device__ __forceinline__ float2 lds_f2(uint32_t addr) {
 }
 
 // Shared-memory plan of the CQ kernel: pair table, reduction area, ring barriers and one
-// ring per warp (a slot holds kUnitRows packed row segments, then their 16-byte norm runs).
+// ring per warp (a slot holds the kUnitRows x segment box of packed rows, then the
+// kUnitRows x 8 box of their group norms; slots are 128-byte aligned for the copies).
 template <int BITS>
 struct CqPlan {
-    static constexpr uint32_t seg = 128 * BITS;
-    static constexpr uint32_t slot = kUnitRows * (seg + 16);
+    static constexpr uint32_t seg = 128 * BITS;                        // bytes of a row segment
+    static constexpr uint32_t norms = kUnitRows * seg;                  // offset of the norm box
+    static constexpr uint32_t slot = (norms + kUnitRows * 16 + 127) / 128 * 128;
     static constexpr uint32_t ring = kRing * slot;
     static constexpr uint32_t table = (1u << (2 * BITS)) * 32 * 8;
 };
@@ -334,7 +348,7 @@ size_t cq_smem_bytes(int tb) {
 }
 
 template <int BITS, int TB, int SPW>
-__global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvParams p) {
+__global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_constant__ CqGemvParams p) {
     using P = CqPlan<BITS>;
     constexpr int L = 1 << BITS;
     constexpr int E = 1 << (2 * BITS);
@@ -371,11 +385,15 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     float* slv = reinterpret_cast<float*>(gen(lv_at));
     uint8_t* ring = gen(ring_at);
     if (tid == 0) {
-        init_reduce(rd);
-        uint64_t* all = reinterpret_cast<uint64_t*>(gen(bar_at));
-        for (int i = 0; i < kWarps2 * kRing; ++i) mbar_init(&all[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&p.pmap);
+        if (p.K % kSeg == 0) prefetch_tensormap(&p.nmap);
     }
+    if (lane < kRing) mbar_init(&rfull[lane], 1);   // each warp its own ring barriers
+    if (tid < kSlots) {
+        rd.count[tid] = 0u;
+        mbar_init(&rd.empty[tid], 1);
+    }
+    if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (tid < 16) {   // the levels, by an unrolled select (no indexed parameter access)
         float v = 0.0f;
 #pragma unroll
@@ -389,7 +407,6 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     const uint32_t nbusy = (uint32_t)(nsl * p.rg);
     const bool busy = rgi < p.rg;
     const int G = p.K / kGroup;
-    const int64_t rowbytes = (int64_t)G * 16 * BITS;
     const int tile_rows = kRows * p.rg;
     const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
     const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -401,22 +418,15 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
     // cursor of the next unit to issue (units go out strictly in order)
     int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;   // its tile's first row
     int nx_rem = 0;                                                             // unit within the tile
+    constexpr uint32_t kBoxBytes = kUnitRows * P::seg;
     auto issue = [&](int d) {
-        const int seg = slot + (nx_rem >> 1) * kWarps2;
-        const int64_t row0 = nx_base + (nx_rem & 1) * kUnitRows;
-        const int64_t left = p.N - row0;
-        const int nr = left >= kUnitRows ? kUnitRows : (left > 0 ? (int)left : 0);
-        const uint32_t bytes = min(P::seg, (uint32_t)((p.K - seg * kSeg) / 8 * BITS));
-        uint8_t* sp = ring + d * P::slot;
-        if (lane == 0) mbar_arrive_tx(&rfull[d], (uint32_t)nr * (bytes + (nbulk ? 16u : 0u)));
-        __syncwarp();
-        if (lane < nr) {
-            bulk_g2s(sp + lane * P::seg, p.packed + (row0 + lane) * rowbytes + (int64_t)seg * P::seg,
-                     bytes, &rfull[d]);
-        } else if (nbulk && lane >= 8 && lane < 8 + nr) {
-            const int r = lane - 8;
-            bulk_g2s(sp + kUnitRows * P::seg + r * 16, p.norms + (row0 + r) * G + seg * 8, 16u,
-                     &rfull[d]);
+        if (lane == 0) {
+            const int seg = slot + (nx_rem >> 1) * kWarps2;
+            const int y = (int)(nx_base + (nx_rem & 1) * kUnitRows);
+            uint8_t* sp = ring + d * P::slot;
+            mbar_arrive_tx(&rfull[d], kBoxBytes + (nbulk ? kUnitRows * 16u : 0u));
+            tma_box(sp, &p.pmap, seg * (P::seg / 4), y, &rfull[d]);
+            if (nbulk) tma_box(sp + P::norms, &p.nmap, seg * 8, y, &rfull[d]);
         }
         if (++nx_rem == upt) {
             nx_rem = 0;
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                 }
                 mbar_wait(&rfull[d], (uint32_t)(u >> 2) & 1u, p.err);
                 if (nbulk) {
-                    const uint16_t* sn = reinterpret_cast<const uint16_t*>(sp + kUnitRows * P::seg);
+                    const uint16_t* sn = reinterpret_cast<const uint16_t*>(sp + P::norms);
 #pragma unroll
                     for (int r = 0; r < kUnitRows; ++r)
                         nrm[r] = r < nv ? f16_bits_to_f32(sn[r * 8 + (lane >> 2)]) : 0.0f;
@@ -496,10 +506,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                 for (int r = 0; r < kUnitRows; ++r) {
                     uint32_t wd[BITS];
                     lds_packed<BITS>(wd, sp + r * P::seg + lane * (4 * BITS));
-                    // two independent accumulator chains per token
-                    float2 d2[TB][2];
+                    // scalar FMAs on four independent chains per token: the FMA pipe has room,
+                    // the integer pipe (byte permutes, moves) is the one that binds
+                    float a4[TB][4];
 #pragma unroll
-                    for (int t = 0; t < TB; ++t) d2[t][0] = d2[t][1] = make_float2(0.0f, 0.0f);
+                    for (int t = 0; t < TB; ++t) a4[t][0] = a4[t][1] = a4[t][2] = a4[t][3] = 0.0f;
                     if constexpr (BITS == 4) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -510,10 +521,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                             const float2 c3 = lds_f2(pair_addr<3>(wv, lb));
 #pragma unroll
                             for (int t = 0; t < TB; ++t) {
-                                d2[t][0] = __ffma2_rn(c0, xx[i][t][4 * kk], d2[t][0]);
-                                d2[t][1] = __ffma2_rn(c1, xx[i][t][4 * kk + 1], d2[t][1]);
-                                d2[t][0] = __ffma2_rn(c2, xx[i][t][4 * kk + 2], d2[t][0]);
-                                d2[t][1] = __ffma2_rn(c3, xx[i][t][4 * kk + 3], d2[t][1]);
+                                const float2* xq = &xx[i][t][4 * kk];
+                                a4[t][0] = fmaf(c0.x, xq[0].x, a4[t][0]); a4[t][1] = fmaf(c0.y, xq[0].y, a4[t][1]);
+                                a4[t][2] = fmaf(c1.x, xq[1].x, a4[t][2]); a4[t][3] = fmaf(c1.y, xq[1].y, a4[t][3]);
+                                a4[t][0] = fmaf(c2.x, xq[2].x, a4[t][0]); a4[t][1] = fmaf(c2.y, xq[2].y, a4[t][1]);
+                                a4[t][2] = fmaf(c3.x, xq[3].x, a4[t][2]); a4[t][3] = fmaf(c3.y, xq[3].y, a4[t][3]);
                             }
                         }
                     } else {
@@ -521,13 +533,16 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
                         for (int q = 0; q < 16; ++q) {
                             const float2 c = mylut[extract_bits<2 * BITS>(wd, q) << 5];
 #pragma unroll
-                            for (int t = 0; t < TB; ++t) d2[t][q & 1] = __ffma2_rn(c, xx[i][t][q], d2[t][q & 1]);
+                            for (int t = 0; t < TB; ++t) {
+                                a4[t][2 * (q & 1)] = fmaf(c.x, xx[i][t][q].x, a4[t][2 * (q & 1)]);
+                                a4[t][2 * (q & 1) + 1] = fmaf(c.y, xx[i][t][q].y, a4[t][2 * (q & 1) + 1]);
+                            }
                         }
                     }
 #pragma unroll
                     for (int t = 0; t < TB; ++t)
                         acc[t][h * kUnitRows + r] =
-                            fmaf(nrm[r], (d2[t][0].x + d2[t][1].x) + (d2[t][0].y + d2[t][1].y), acc[t][h * kUnitRows + r]);
+                            fmaf(nrm[r], (a4[t][0] + a4[t][2]) + (a4[t][1] + a4[t][3]), acc[t][h * kUnitRows + r]);
                 }
             }
         }
@@ -549,10 +564,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const CqGemvPa
 // loads into one buffer per warp - and each lane reads its block with five aligned
 // 32-bit loads.  A nibble is decoded without a table: one byte permute drops it into
 // the mantissa of 128.0f, giving exactly 128 + nib; an even/odd pair multiplies the
-// activation pair with one fp32x2 FMA; the constant 128 (and the -8 of the format) is
+// activation pair with two scalar FMAs; the constant 128 (and the -8 of the format) is
 // removed per block with a precomputed sum of the activations.
 // ---------------------------------------------------------------------------------
 struct Q40GemvParams {
+    CUtensorMap bmap;     // blocks as [N][nblk * 18 / 4] uint32, box 144 x kUnitRows (nblk % 8 == 0)
     const uint8_t* blocks;
     const float* X;       // [B][K]
     float* Y;             // [B][N]
@@ -579,9 +595,10 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
     const float d = f16_bits_to_f32((uint16_t)(w0 >> dsh));
     const uint32_t nw[4] = {__funnelshift_rc(w0, w1, nsh), __funnelshift_rc(w1, w2, nsh),
                             __funnelshift_rc(w2, w3, nsh), __funnelshift_rc(w3, w4, nsh)};
-    float2 s2[TB][2];   // two independent accumulator chains per token
+    // scalar FMAs on four chains per token (the integer pipe, not the FMA pipe, binds)
+    float a4[TB][4];
 #pragma unroll
-    for (int t = 0; t < TB; ++t) s2[t][0] = s2[t][1] = make_float2(0.0f, 0.0f);
+    for (int t = 0; t < TB; ++t) a4[t][0] = a4[t][1] = a4[t][2] = a4[t][3] = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         // even-index nibbles (low halves of the bytes) and odd-index nibbles, one per byte
@@ -593,15 +610,17 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
             uint32_t fe, fo;
             asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fe) : "r"(ev), "r"(0x43000000u), "r"(sel));
             asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fo) : "r"(od), "r"(0x43000000u), "r"(sel));
-            const float2 f = make_float2(__uint_as_float(fe), __uint_as_float(fo));
 #pragma unroll
-            for (int t = 0; t < TB; ++t) s2[t][j & 1] = __ffma2_rn(f, xx[t][4 * k + j], s2[t][j & 1]);
+            for (int t = 0; t < TB; ++t) {
+                a4[t][2 * (j & 1)] = fmaf(__uint_as_float(fe), xx[t][4 * k + j].x, a4[t][2 * (j & 1)]);
+                a4[t][2 * (j & 1) + 1] = fmaf(__uint_as_float(fo), xx[t][4 * k + j].y, a4[t][2 * (j & 1) + 1]);
+            }
         }
     }
     // sum (nib - 8) x = sum (128 + nib) x - 136 sum x
 #pragma unroll
     for (int t = 0; t < TB; ++t)
-        acc[t][r] = fmaf(d, ((s2[t][0].x + s2[t][1].x) + (s2[t][0].y + s2[t][1].y)) - cblk[t], acc[t][r]);
+        acc[t][r] = fmaf(d, ((a4[t][0] + a4[t][2]) + (a4[t][1] + a4[t][3])) - cblk[t], acc[t][r]);
 }
 
 // Activation pairs of this lane's blocks and their block sums (x 136), zero outside K;
@@ -645,18 +664,20 @@ __device__ __forceinline__ void q4_load_x(const Q40GemvParams& p, int slot, bool
 
 // Ring-staged Q4_0 GEMV: needs 16-byte aligned row segments (nblk a multiple of 8).
 template <int TB, int SPW>
-__global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q40GemvParams p) {
+__global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const __grid_constant__ Q40GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem_q[];
     constexpr int kSlotB = kUnitRows * kQSeg;
     uint8_t* rings = smem_q;                                                   // [16][kRing][4][576]
     uint64_t* rbar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kRing * kSlotB);  // [16][kRing]
     const Reduce rd = carve_reduce(rbar + kWarps2 * kRing, TB);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (tid == 0) {
-        init_reduce(rd);
-        for (int i = 0; i < kWarps2 * kRing; ++i) mbar_init(&rbar[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (tid == 0) prefetch_tensormap(&p.bmap);
+    if (lane < kRing) mbar_init(&rbar[w * kRing + lane], 1);   // each warp its own ring barriers
+    if (tid < kSlots) {
+        rd.count[tid] = 0u;
+        mbar_init(&rd.empty[tid], 1);
     }
+    if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
     const int slot = w % nsl, rgi = w / nsl;
@@ -665,7 +686,6 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q
 
     uint8_t* ring = rings + w * (kRing * kSlotB);
     uint64_t* rfull = rbar + w * kRing;
-    const int64_t rowbytes = (int64_t)p.nblk * 18;
     const int tile_rows = kRows * p.rg;
     const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
     const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -676,16 +696,12 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const Q
     int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;
     int nx_rem = 0;
     auto issue = [&](int d) {
-        const int seg = slot + (nx_rem >> 1) * kWarps2;
-        const int64_t row0 = nx_base + (nx_rem & 1) * kUnitRows;
-        const int64_t left = p.N - row0;
-        const int nr = left >= kUnitRows ? kUnitRows : (left > 0 ? (int)left : 0);
-        const int nb = min(32, p.nblk - seg * 32);
-        if (lane == 0) mbar_arrive_tx(&rfull[d], (uint32_t)(nr * nb * 18));
-        __syncwarp();
-        if (lane < nr)
-            bulk_g2s(ring + d * kSlotB + lane * kQSeg, p.blocks + (row0 + lane) * rowbytes + (int64_t)seg * kQSeg,
-                     (uint32_t)(nb * 18), &rfull[d]);
+        if (lane == 0) {
+            const int seg = slot + (nx_rem >> 1) * kWarps2;
+            const int y = (int)(nx_base + (nx_rem & 1) * kUnitRows);
+            mbar_arrive_tx(&rfull[d], (uint32_t)kSlotB);
+            tma_box(ring + d * kSlotB, &p.bmap, seg * (kQSeg / 4), y, &rfull[d]);
+        }
         if (++nx_rem == upt) {
             nx_rem = 0;
             nx_base += (int64_t)gridDim.x * tile_rows;
@@ -849,6 +865,37 @@ cq_status device_error_word(unsigned int** out) {
     return CQ_OK;
 }
 
+// cuTensorMapEncodeTiled from the driver (cached; no link against libcuda)
+std::mutex g_enc_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+
+cq_status encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                     uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+    {
+        std::lock_guard<std::mutex> lock(g_enc_mu);
+        if (!g_enc) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            const cudaError_t e =
+                cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+                set_last_cuda_error((int)e);
+                return CQ_ERR_UNSUPPORTED;
+            }
+            g_enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = g_enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { set_last_cuda_error((int)r); return CQ_ERR_CUDA; }
+    return CQ_OK;
+}
+
 template <typename Kern>
 cq_status launch_once(Kern kern, size_t smem, int64_t ntiles, cudaStream_t st, bool* attr,
                       int* grid_out) {
@@ -930,7 +977,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     if (!packed || !norms || !cbk || !Xq || !scale || !Y || N < 1 || K < 1 || B < 1)
         return CQ_ERR_INVALID_ARG;
     if (g != kGroup || K % kGroup != 0 || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
-    if (K > (1 << 24) || N > ((int64_t)1 << 40)) return CQ_ERR_UNSUPPORTED;
+    if (K > (1 << 24) || N > kMaxGemvRows) return CQ_ERR_UNSUPPORTED;
     if (!aligned16(packed) || !aligned16(norms) || !aligned16(Xq) || !aligned16(scale) ||
         !aligned16(Y))
         return CQ_ERR_ALIGNMENT;
@@ -957,6 +1004,18 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     }
     p.packed = packed; p.norms = norms; p.xr = xr; p.scale = scale; p.Y = Y;
     p.N = N; p.K = (int)K; p.nseg = (int)((K + kSeg - 1) / kSeg);
+    {
+        // packed rows as 32-bit words (rows are 16 b-byte groups long, so 16-byte strides)
+        const uint64_t rowbytes = (uint64_t)(K / kGroup) * 16u * (uint64_t)b;
+        cq_status se = encode_map(&p.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, packed, rowbytes / 4,
+                                  (uint64_t)N, rowbytes, 32u * (uint32_t)b, kUnitRows);
+        if (se != CQ_OK) return se;
+        if (K % kSeg == 0) {   // norm rows of 8-group segments: 16-byte strides and boxes
+            se = encode_map(&p.nmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, norms, (uint64_t)(K / kGroup),
+                            (uint64_t)N, (uint64_t)(K / kGroup) * 2u, 8u, kUnitRows);
+            if (se != CQ_OK) return se;
+        }
+    }
     for (int t = 0; t < 16; ++t) p.lv[t] = 0.0f;
     if (b == 1) {
         const float c = 0.797884560802865355879892119868763737f;  // sqrt(2/pi)
@@ -988,7 +1047,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
 extern "C" cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X,
                                int64_t B, float* Y, void* stream) {
     if (!blocks || !X || !Y || N < 1 || K < 1 || B < 1) return CQ_ERR_INVALID_ARG;
-    if (K > 2 * kWarps2 * kSeg || N > ((int64_t)1 << 40)) return CQ_ERR_UNSUPPORTED;
+    if (K > 2 * kWarps2 * kSeg || N > kMaxGemvRows) return CQ_ERR_UNSUPPORTED;
     if (!aligned16(blocks) || !aligned16(X) || !aligned16(Y)) return CQ_ERR_ALIGNMENT;
     Q40GemvParams p;
     p.blocks = blocks; p.X = X; p.Y = Y; p.N = N; p.K = (int)K;
@@ -1002,8 +1061,14 @@ extern "C" cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, cons
         if (se != CQ_OK) return se;
     }
     p.err = err;
-    // ring staging by bulk copies needs 16-byte aligned row segments: 8 | nblk
+    // ring staging by tensor copies needs 16-byte row strides: 8 | nblk
     const bool bulk = (p.nblk % 8) == 0;
+    if (bulk) {
+        const uint64_t rowbytes = (uint64_t)p.nblk * 18u;
+        const cq_status se = encode_map(&p.bmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, blocks, rowbytes / 4,
+                                        (uint64_t)N, rowbytes, kQSeg / 4, kUnitRows);
+        if (se != CQ_OK) return se;
+    }
     const int spw = (p.nseg + kWarps2 - 1) / kWarps2;
     p.rg = row_groups(p.nseg);
     const int tb = (spw == 1 && B > 1) ? 2 : 1;

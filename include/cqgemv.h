@@ -114,7 +114,7 @@ cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* Xq, float* s
  *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
  *   Y  [B][N] float32
  *   workspace      device scratch of at least cq_gemv_workspace_bytes(B, K) bytes
- * K is limited to 32768 (CQ_ERR_UNSUPPORTED above).  Deterministic: the same inputs give
+ * K is limited to 32768 and N to 2^31 - 1024 (CQ_ERR_UNSUPPORTED above).  Deterministic: the same inputs give
  * bit-identical outputs.
  * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
 size_t cq_gemv_workspace_bytes(int64_t B, int64_t K);
@@ -196,7 +196,7 @@ cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks, v
  * row-aligned blocks).  Y[t][o] = sum_blocks fp32(d) * sum_k (nib - 8) * X[t][k],
  * float32 accumulation; padding columns are skipped.
  *   blocks [N][ceil(K/32) * 18] uint8, X [B][K] float32, Y [B][N] float32 (all 16-byte
- *   aligned); K is limited to 32768 (CQ_ERR_UNSUPPORTED above).
+ *   aligned); K is limited to 32768 and N to 2^31 - 1024 (CQ_ERR_UNSUPPORTED above).
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA. */
 cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t B,
                     float* Y, void* stream);
