@@ -274,7 +274,8 @@ struct CqGemvParams {
     CUtensorMap nmap;     // norms as [N][K / 128] fp16, box 8 x kUnitRows (when K % 1024 == 0)
     const uint8_t* packed;
     const uint16_t* norms;
-    const float* xr;      // [B][K] rotated activations
+    const float* xr;      // [B][K] rotated activations (multi-pass calls), or
+    const int8_t* xq;     // [B][K] int8 activations, rotated in the prologue (single pass)
     const float* scale;   // [B]
     float* Y;             // [B][N]
     unsigned int* err;    // device error flag
@@ -345,6 +346,31 @@ size_t cq_smem_bytes(int tb) {
     // 4-bit: the table is 64 KB aligned; the space below it may be too small to use
     if (BITS == 4) return 227 * 1024;
     return P::table + 16 + rest;
+}
+
+// xr = Hu @ q for this lane's 32 positions of a 128-group held by lanes 4g..4g+3: five
+// butterfly stages inside the lane, the strides of 32 and 64 across lanes (xor 1, 2).
+// The values are integers below 2^24, exact in fp32 in any order, so this equals the
+// separate rotation kernel bit for bit.
+__device__ __forceinline__ void rotate32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if ((j & h) == 0) {
+                const float a = v[j], b = v[j + h];
+                v[j] = a + b;
+                v[j + h] = a - b;
+            }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float q = __shfl_xor_sync(0xffffffffu, v[j], m);
+            v[j] = upper ? (q - v[j]) : (v[j] + q);
+        }
+    }
 }
 
 template <int BITS, int TB, int SPW>
@@ -447,14 +473,30 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
         const int pos0 = seg * kSeg + lane * 32;
 #pragma unroll
         for (int t = 0; t < TB; ++t) {
+            // whole 128-groups lie inside or outside K, so the four lanes of a group agree
             const bool ok = busy && seg < p.nseg && pos0 < p.K && t < p.ntok;
-            const float* src = p.xr + (int64_t)(p.t0 + t) * p.K + pos0;
+            if (p.xq) {
+                float v[32];
+                const int8_t* src = p.xq + (int64_t)(p.t0 + t) * p.K + pos0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 v = ok ? *reinterpret_cast<const float4*>(src + 4 * q)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                xx[i][t][2 * q] = make_float2(v.x, v.y);
-                xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
+                for (int h = 0; h < 2; ++h) {
+                    const int4 c = ok ? *reinterpret_cast<const int4*>(src + 16 * h) : make_int4(0, 0, 0, 0);
+                    const int wv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[16 * h + q] = (float)(int8_t)(wv[q >> 2] >> (8 * (q & 3)));
+                }
+                rotate32(v, lane);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) xx[i][t][q] = make_float2(v[2 * q], v[2 * q + 1]);
+            } else {
+                const float* src = p.xr + (int64_t)(p.t0 + t) * p.K + pos0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 v = ok ? *reinterpret_cast<const float4*>(src + 4 * q)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    xx[i][t][2 * q] = make_float2(v.x, v.y);
+                    xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
+                }
             }
         }
     }
@@ -985,9 +1027,17 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     if (!aligned16(workspace)) return CQ_ERR_ALIGNMENT;
     if (K > 2 * kWarps2 * kSeg) return CQ_ERR_UNSUPPORTED;   // at most 2 segments per warp
     cudaStream_t st = as_stream(stream);
+    // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
+    // tokens per pass when each warp owns a single segment
+    const int nseg = (int)((K + kSeg - 1) / kSeg);
+    const int spw = (nseg + kWarps2 - 1) / kWarps2;
+    const int tb = (spw == 1 && B > 1) ? 2 : 1;
+    // a single pass rotates the activations in its prologue; several passes share one
+    // rotation kernel's output in the workspace
+    const bool fused = B <= tb;
     float* xr = reinterpret_cast<float*>(workspace);
-    const int64_t groups = B * (K / kGroup);
-    {
+    if (!fused) {
+        const int64_t groups = B * (K / kGroup);
         int64_t grid = (groups + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
         if (grid > cap) grid = cap;
@@ -1002,8 +1052,10 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         if (se != CQ_OK) return se;
         p.err = err;
     }
-    p.packed = packed; p.norms = norms; p.xr = xr; p.scale = scale; p.Y = Y;
-    p.N = N; p.K = (int)K; p.nseg = (int)((K + kSeg - 1) / kSeg);
+    p.packed = packed; p.norms = norms; p.scale = scale; p.Y = Y;
+    p.xr = fused ? nullptr : xr;
+    p.xq = fused ? Xq : nullptr;
+    p.N = N; p.K = (int)K; p.nseg = nseg;
     {
         // packed rows as 32-bit words (rows are 16 b-byte groups long, so 16-byte strides)
         const uint64_t rowbytes = (uint64_t)(K / kGroup) * 16u * (uint64_t)b;
@@ -1024,11 +1076,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
         for (int t = 0; t < (1 << b); ++t) p.lv[t] = cbk->cb[off + t];
     }
-    // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
-    // tokens per pass when each warp owns a single segment
-    const int spw = (p.nseg + kWarps2 - 1) / kWarps2;
     p.rg = row_groups(p.nseg);
-    const int tb = (spw == 1 && B > 1) ? 2 : 1;
     for (int64_t t0 = 0; t0 < B; t0 += tb) {
         p.t0 = (int)t0;
         p.ntok = (int)((B - t0) < tb ? (B - t0) : tb);
