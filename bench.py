@@ -1,8 +1,9 @@
 """Throughput of the low-bit decode GEMV path on GB300 (one JSON line on rank 0).
 
 A step is one decode pass (batch 1) over the large-shape workload: CQ-W4A8 GEMV
-(``a8_quantize`` -> rotation -> ``cq_gemv``) and Q4_0 GEMV (``q4_0_gemv``) on the four
-matrices [8192, 8192], [28672, 8192], [8192, 28672] and the lm_head [128256, 4096]
+(``a8_quantize`` -> ``cq_gemv``, which rotates the activations in its prologue) and Q4_0
+GEMV (``q4_0_gemv``) on the four matrices [8192, 8192], [28672, 8192], [8192, 28672] and
+the lm_head [128256, 4096]
 (1.15 GB of packed weights per step, far larger than L2, so no flush is needed).
 Weights are encoded once before timing (offline, as the format intends); the timed
 region holds only the decode work.  ``value`` is algorithmic GB/s: packed indices +
@@ -396,9 +397,10 @@ def gpu_arm(args, rank, world, local_rank):
             "e2e": {"value": round(world * total_b / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps * len(mats) * (3 * ("cq" in kinds) + ("q4_0" in kinds)),
-            "gpu_launches_note": "per decode step: a8_quantize, rotation and cq_gemv kernels per "
-                                 "CQ matrix, one q4_0_gemv kernel per Q4_0 matrix",
+            "gpu_launches": args.steps * len(mats) * (2 * ("cq" in kinds) + ("q4_0" in kinds)),
+            "gpu_launches_note": "per decode step: a8_quantize and cq_gemv (which rotates the "
+                                 "activations in its prologue at batch 1) per CQ matrix, one "
+                                 "q4_0_gemv kernel per Q4_0 matrix",
             "clocks": clocks,
         }
         if not args.no_prefill:
