@@ -13,6 +13,8 @@
 // nibbles, which is what lets the MMA rate approach the tensor-core peak.
 //
 // One CTA per SM (persistent), tile = 128 out-rows x 192 tokens, K in chunks of 64.
+// Shared memory: the codeword-pair table (64 KB, one copy per lane) at a 64 KB boundary of
+// the shared window, so a lookup address is one byte permute; four 28 KB stages around it.
 // Tensor memory (512 columns): 4 A stages of 32 columns (64 bf16 per row) and two
 // 192-column fp32 accumulators (the epilogue of a tile overlaps the next main loop).
 // Warp roles:
@@ -23,9 +25,12 @@
 //   warps 2-9   epilogue: tcgen05.ld (two warps per TMEM lane quarter, 96 tokens each,
 //               16-column pieces),
 //               bf16, store
-//   warps 10-17 dequant: packed tile -> codeword pairs from a per-lane shared table,
-//               scaled by the group norm, bf16, tcgen05.st into the A stage (two warps
-//               per lane quarter, 32 k each)
+//   warps 10-25 dequant, two groups of eight taking alternate stages (a stage's
+//               dequant latency - table loads, tensor-memory store and its wait - is
+//               longer than its share of the MMA time, so each group gets two stage
+//               times per stage): packed tile -> codeword pairs from a per-lane shared
+//               table, scaled by the group norm, bf16, tcgen05.st into the A stage
+//               (two warps per lane quarter, 32 k each)
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a device error
 // flag, stops issuing work, frees its tensor memory and returns.
 
@@ -44,17 +49,19 @@ constexpr int kBO = 128;                 // out-rows per tile (MMA M, TMEM lanes
 constexpr int kBT = 192;                 // tokens per tile (MMA N)
 constexpr int kBK = 64;                  // K per stage (128 bytes of bf16)
 constexpr int kStages = 4;
-constexpr int kThreadsGemm = 576;        // 18 warps
+constexpr int kThreadsGemm = 832;        // 26 warps: TMA, MMA, 8 epilogue, 16 dequant
 constexpr int kEpiWarp0 = 2;             // warps 2..9: two per TMEM lane quarter
 constexpr int kEpiWarps = 8;
 constexpr int kDequantWarp0 = kEpiWarp0 + kEpiWarps;
-constexpr int kDequantWarps = 8;         // warps 10..17: two per TMEM lane quarter
+constexpr int kDequantWarps = 8;         // per stage: two per TMEM lane quarter
+constexpr int kDequantGroups = 2;        // warps 10..17 take even stages, 18..25 odd ones
 constexpr int kXTileBytes = kBT * kBK * 2;            // 24 KB of bf16 activations
 constexpr int kPTileBytes = kBO * kBK / 2;            // 4 KB of packed nibbles
 constexpr int kStageBytes = kXTileBytes + kPTileBytes;
 constexpr int kTmemCols = 512;
 constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
 constexpr int kDCol0 = kStages * kACols;              // accumulators start at column 128
+constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + 4 stages + barriers
 constexpr int kMaxProblems = 120;
 constexpr int kMaxActs = 8;
 static_assert(kDCol0 + 2 * kBT <= kTmemCols, "tensor memory budget");
@@ -278,6 +285,20 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// 32-bit shared address of the pair-table entry in byte J of `wv` for this lane (table
+// at a 64 KB boundary, entry e of lane l at e << 8 | l << 3): one byte permute
+template <int J>
+__device__ __forceinline__ uint32_t pair_addr(uint32_t wv, uint32_t lb) {
+    uint32_t a;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(wv), "r"(lb), "n"(0x7604 | (J << 4)));
+    return a;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -289,12 +310,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 
 __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~(uintptr_t)1023);
-    // stage s: [X (bf16, swizzled, 192 rows) | P (packed, 32 B per out-row)]
-    uint8_t* stage_base = smem;
-    float2* lut2 = reinterpret_cast<float2*>(smem + kStages * kStageBytes);   // [256][32]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(lut2 + 256 * 32);
+    // The codeword-pair table sits at a 64 KB boundary of the shared window (the address
+    // of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the four
+    // 1024-byte aligned stages fill the space below it, then the space above it.
+    const uint32_t sbase = smem_u32(smem_raw), send = sbase + (uint32_t)kGemmSmem;
+    const uint32_t tbase = (sbase + 65535u) & ~65535u;
+    const uint32_t a0 = (sbase + 1023u) & ~1023u;
+    const int nA = tbase >= a0 + kStageBytes ? min(kStages, (int)((tbase - a0) / kStageBytes)) : 0;
+    const uint32_t b0 = tbase + 256u * 32u * 8u;
+    auto gen = [&](uint32_t a) { return smem_raw + (a - sbase); };
+    auto stage_ptr = [&](int s) {
+        return gen(s < nA ? a0 + (uint32_t)s * kStageBytes : b0 + (uint32_t)(s - nA) * kStageBytes);
+    };
+    float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [256][32]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gen(b0 + (uint32_t)(kStages - nA) * kStageBytes));
+    const bool layout_ok = b0 + (uint32_t)(kStages - nA) * kStageBytes + 256u <= send;
     uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
     uint64_t* full_b = bars + kStages;            // dequant: A stage written to TMEM
     uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
@@ -304,6 +334,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (!layout_ok) {   // the launch's shared memory cannot hold the plan (host sizing error)
+        if (tid == 0) atomicOr(p.err, 4u);
+        return;
+    }
 
     // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]), one copy per lane
     for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
@@ -352,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 const CUtensorMap* xmap = &p.tmap[pr.act];
                 for (int kc = 0; kc < pr.K / kBK; ++kc) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p)) { ok = false; break; }
-                    uint8_t* st = stage_base + s * kStageBytes;
+                    uint8_t* st = stage_ptr(s);
                     mbar_arrive_tx(&full_a[s], kXTileBytes + kPTileBytes);
                     tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
                     tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK / 2), tr.nt * kBO, &full_a[s]);
@@ -381,7 +415,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                     if (!mbar_wait(&full_a[s], ph, abort_flag, p) ||
                         !mbar_wait(&full_b[s], ph, abort_flag, p)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(stage_base + s * kStageBytes));
+                    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(stage_ptr(s)));
                     const uint32_t a0 = tmem_base + (uint32_t)(s * kACols);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -441,52 +475,39 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         }
     } else {
         // ------------------------------ dequant -----------------------------------
-        // warp -> TMEM lane quarter q (out-rows 32q..32q+31) and k half kh (32 of the 64 k
-        // of a stage); lane -> one row: 16 packed bytes -> 16 codeword pairs (one table
-        // lookup each) x norm -> bf16 pairs -> tcgen05.st of 16 columns
+        // warp -> TMEM lane quarter q (out-rows 32q..32q+31), k half kh (32 of the 64 k of
+        // a stage) and stage group grp; lane -> one row: 16 packed bytes -> 16 codeword
+        // pairs (one table lookup each) x norm -> bf16 pairs -> tcgen05.st of 16 columns
+        const int dw = warp - kDequantWarp0;
         const int q = warp & 3;
-        const int kh = (warp - kDequantWarp0) >> 2;
+        const int kh = (dw >> 2) & 1;
+        const int grp = dw >> 3;
         const int r = q * 32 + lane;
-        const char* lut_bytes = reinterpret_cast<const char*>(lut2);
-        const uint32_t lane8 = (uint32_t)lane << 3;
-        int s = 0;
-        uint32_t ph = 0;
+        const uint32_t lb = tbase | ((uint32_t)lane << 3);
         bool ok = true;
-        int tile = blockIdx.x;
-        float nrm = 0.0f;
-        if (tile < p.total_tiles) {
-            const TileRef tr = tile_ref(p, tile);
-            nrm = load_norm(p.prob[tr.prob], tr.nt * kBO + r, 0);
-        }
-        for (; ok && tile < p.total_tiles; tile += gridDim.x) {
+        int gi = 0;   // global stage index
+        for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
             const TileRef tr = tile_ref(p, tile);
             const GemmProblem& pr = p.prob[tr.prob];
             const int nk = pr.K / kBK;
-            for (int kc = 0; kc < nk; ++kc) {
-                // prefetch the norm of the next chunk (or of the next tile's first chunk)
-                float nrm_next = 0.0f;
-                if (kc + 1 < nk) {
-                    nrm_next = load_norm(pr, tr.nt * kBO + r, kc + 1);
-                } else if (tile + (int)gridDim.x < p.total_tiles) {
-                    const TileRef tn = tile_ref(p, tile + gridDim.x);
-                    nrm_next = load_norm(p.prob[tn.prob], tn.nt * kBO + r, 0);
-                }
+            for (int kc = 0; kc < nk; ++kc, ++gi) {
+                if (gi % kDequantGroups != grp) continue;   // the other group's stage
+                const int s = gi % kStages;
+                const uint32_t ph = (uint32_t)((gi / kStages) & 1);
+                const float nrm = load_norm(pr, tr.nt * kBO + r, kc);
                 if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
-                const uint4 w = *reinterpret_cast<const uint4*>(stage_base + s * kStageBytes +
-                                                                kXTileBytes + r * 32 + kh * 16);
+                const uint4 w = *reinterpret_cast<const uint4*>(stage_ptr(s) + kXTileBytes + r * 32 + kh * 16);
                 const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
                 const float2 n2 = make_float2(nrm, nrm);
                 uint32_t pk[16];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    // byte j -> offset (byte << 8) | (lane << 3) of the lane's own table copy
-                    const uint32_t off[4] = {((wv[k] << 8) & 0xFF00u) | lane8, (wv[k] & 0xFF00u) | lane8,
-                                             ((wv[k] >> 8) & 0xFF00u) | lane8,
-                                             ((wv[k] >> 16) & 0xFF00u) | lane8};
+                    const float2 c[4] = {lds_f2(pair_addr<0>(wv[k], lb)), lds_f2(pair_addr<1>(wv[k], lb)),
+                                         lds_f2(pair_addr<2>(wv[k], lb)), lds_f2(pair_addr<3>(wv[k], lb))};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float2 c = __fmul2_rn(*reinterpret_cast<const float2*>(lut_bytes + off[j]), n2);
-                        __nv_bfloat162 v = __floats2bfloat162_rn(c.x, c.y);
+                        const float2 cn = __fmul2_rn(c[j], n2);
+                        __nv_bfloat162 v = __floats2bfloat162_rn(cn.x, cn.y);
                         pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
                     }
                 }
@@ -495,8 +516,6 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full_b[s]);
-                if (++s == kStages) { s = 0; ph ^= 1u; }
-                nrm = nrm_next;
             }
         }
     }
@@ -543,7 +562,7 @@ cq_status host_setup(unsigned int** err) {
         g_err_ptr[dev] = static_cast<unsigned int*>(pe);
     }
     if (!g_attr_done[dev]) {
-        const size_t smem = (size_t)kStages * kStageBytes + 256 * 32 * 8 + 256 + 1024;  // + align slack
+        const size_t smem = (size_t)kGemmSmem;
         e = cudaFuncSetAttribute(cq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
         g_attr_done[dev] = true;
@@ -719,7 +738,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
         fill_levels(prm.lv, b, cbk);
         prm.err = err;
         prm.timeout_ns = 2000000000ull;   // 2 s per wait
-        const size_t smem = (size_t)kStages * kStageBytes + 256 * 32 * 8 + 256 + 1024;  // + align slack
+        const size_t smem = (size_t)kGemmSmem;
         const int grid = tiles < sm_count() ? tiles : sm_count();
         cq_gemm_kernel<<<grid, kThreadsGemm, smem, cs>>>(prm);
         st = check_launch();
