@@ -217,18 +217,36 @@ __device__ __forceinline__ int find_problem(const GemmParams& p, int tile) {
 }
 
 // ---------------------------------------------------------------------------------
-// B = bf16(Hu @ q * s_t / 128) per 128-group; one warp per (token, group).  The fp32
-// butterfly is exact (integers below 2^24); the product with s_t / 128 and the bf16
-// conversion are the only roundings.
+// B = bf16(Hu @ q * s_t / 128) per 128-group; one warp per (token, group), for up to
+// kMaxRotJobs distinct activations in one launch.  The fp32 butterfly is exact (integers
+// below 2^24); the product with s_t / 128 and the bf16 conversion are the only roundings.
 // ---------------------------------------------------------------------------------
+struct RotJob {
+    const int8_t* Xq;
+    const float* scale;
+    __nv_bfloat16* out;
+    int64_t first;             // first group of this job in the launch's group numbering
+    int64_t groups;            // M * K / 128
+    int64_t groups_per_token;  // K / 128
+};
+constexpr int kMaxRotJobs = 8;
+struct RotParams {
+    RotJob job[kMaxRotJobs];
+    int njobs;
+    int64_t groups;            // all jobs
+};
+
 __global__ void __launch_bounds__(256)
-rotate_act_bf16_kernel(const int8_t* __restrict__ Xq, const float* __restrict__ scale,
-                       int64_t groups, int64_t groups_per_token, __nv_bfloat16* __restrict__ out) {
+rotate_act_bf16_kernel(const __grid_constant__ RotParams rp) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * 256) >> 5;
-    for (int64_t gi = warp; gi < groups; gi += nwarps) {
-        const char4 c = *reinterpret_cast<const char4*>(Xq + gi * kGroup + 4 * lane);
+    for (int64_t gg = warp; gg < rp.groups; gg += nwarps) {
+        int j = 0;
+        while (j + 1 < rp.njobs && rp.job[j + 1].first <= gg) ++j;
+        const RotJob& jb = rp.job[j];
+        const int64_t gi = gg - jb.first;
+        const char4 c = *reinterpret_cast<const char4*>(jb.Xq + gi * kGroup + 4 * lane);
         float v0 = c.x, v1 = c.y, v2 = c.z, v3 = c.w;
         float a0 = v0 + v1, a1 = v0 - v1, a2 = v2 + v3, a3 = v2 - v3;
         v0 = a0 + a2; v2 = a0 - a2; v1 = a1 + a3; v3 = a1 - a3;
@@ -244,13 +262,13 @@ rotate_act_bf16_kernel(const int8_t* __restrict__ Xq, const float* __restrict__ 
             v2 = upper ? (p2 - v2) : (v2 + p2);
             v3 = upper ? (p3 - v3) : (v3 + p3);
         }
-        const float sc = __ldg(scale + gi / groups_per_token) * (1.0f / 128.0f);
+        const float sc = __ldg(jb.scale + gi / jb.groups_per_token) * (1.0f / 128.0f);
         __nv_bfloat162 lo = __floats2bfloat162_rn(v0 * sc, v1 * sc);
         __nv_bfloat162 hi = __floats2bfloat162_rn(v2 * sc, v3 * sc);
         uint2 pk;
         pk.x = *reinterpret_cast<uint32_t*>(&lo);
         pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(out + gi * kGroup + 4 * lane) = pk;
+        *reinterpret_cast<uint2*>(jb.out + gi * kGroup + 4 * lane) = pk;
     }
 }
 
@@ -339,16 +357,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         return;
     }
 
-    // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]), one copy per lane
+    // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]), one copy per lane, built
+    // from the 16 levels staged in shared memory (one unrolled select per level thread)
+    float* slv = reinterpret_cast<float*>(bars) + 40;   // 64 bytes inside the barrier block
+    if (tid < 16) {
+        float v = 0.0f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v = (u == tid) ? p.lv[u] : v;
+        slv[tid] = v;
+    }
+    __syncthreads();
     for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
         const int e = i >> 5;
-        float a = 0.0f, b = 0.0f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            a = (u == (e & 15)) ? p.lv[u] : a;
-            b = (u == (e >> 4)) ? p.lv[u] : b;
-        }
-        lut2[i] = make_float2(a, b);
+        lut2[i] = make_float2(slv[e & 15], slv[e >> 4]);
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -571,7 +592,40 @@ cq_status host_setup(unsigned int** err) {
     return CQ_OK;
 }
 
+// Encoded weight maps by (address, N, K): a map depends on nothing else, so a cached one
+// stays valid for any tensor later placed at the same address with the same shape.
+// Guarded by g_host_mu (held by the caller).
+struct MapEntry {
+    const void* base;
+    int64_t N, K;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 4096;   // power of two
+MapEntry g_map_cache[kMapCache];
+
+cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N, int64_t K);
+
 cq_status make_packed_map(CUtensorMap* map, const void* base, int64_t N, int64_t K) {
+    uint64_t h = reinterpret_cast<uint64_t>(base) * 0x9E3779B97F4A7C15ull ^ (uint64_t)N * 0xC2B2AE3D27D4EB4Full ^
+                 (uint64_t)K;
+    for (int probe = 0; probe < 8; ++probe) {
+        MapEntry& e = g_map_cache[(h + (uint64_t)probe) & (kMapCache - 1)];
+        if (e.base == base && e.N == N && e.K == K) {
+            *map = e.map;
+            return CQ_OK;
+        }
+        if (e.base == nullptr) {
+            const cq_status st = make_packed_map_uncached(&e.map, base, N, K);
+            if (st != CQ_OK) return st;
+            e.base = base; e.N = N; e.K = K;
+            *map = e.map;
+            return CQ_OK;
+        }
+    }
+    return make_packed_map_uncached(map, base, N, K);   // neighbourhood full: no caching
+}
+
+cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N, int64_t K) {
     cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
     cuuint32_t box[2] = {(cuuint32_t)(kBK / 2), (cuuint32_t)kBO};
@@ -659,7 +713,8 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
     if (st != CQ_OK) return st;
     cudaStream_t cs = as_stream(stream);
 
-    // distinct activations -> rotated bf16 copies in the workspace
+    // distinct activations -> rotated bf16 copies in the workspace, up to kMaxRotJobs
+    // activations per rotation launch
     if (count > 1024) return CQ_ERR_UNSUPPORTED;
     const int8_t* act_src[1024];
     const void* act_dst[1024];
@@ -668,6 +723,19 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
     int nact = 0;
     size_t off = 0;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    RotParams rp;
+    rp.njobs = 0;
+    rp.groups = 0;
+    auto flush_rot = [&]() -> cq_status {
+        if (rp.njobs == 0) return CQ_OK;
+        int64_t grid = (rp.groups + 7) / 8;
+        const int64_t cap = (int64_t)sm_count() * 16;
+        if (grid > cap) grid = cap;
+        rotate_act_bf16_kernel<<<(unsigned)grid, 256, 0, cs>>>(rp);
+        rp.njobs = 0;
+        rp.groups = 0;
+        return check_launch();
+    };
     for (int i = 0; i < count; ++i) {
         int a = -1;
         for (int j = 0; j < nact; ++j)
@@ -677,19 +745,24 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
             act_src[a] = probs[i].Xq;
             act_dst[a] = ws + off;
             act_K[a] = probs[i].K;
-            const int64_t groups = M * (probs[i].K / kGroup);
-            int64_t grid = (groups + 7) / 8;
-            const int64_t cap = (int64_t)sm_count() * 16;
-            if (grid > cap) grid = cap;
-            rotate_act_bf16_kernel<<<(unsigned)grid, 256, 0, cs>>>(
-                probs[i].Xq, probs[i].scale, groups, probs[i].K / kGroup,
-                reinterpret_cast<__nv_bfloat16*>(ws + off));
-            st = check_launch();
-            if (st != CQ_OK) return st;
+            if (rp.njobs == kMaxRotJobs) {
+                st = flush_rot();
+                if (st != CQ_OK) return st;
+            }
+            RotJob& jb = rp.job[rp.njobs++];
+            jb.Xq = probs[i].Xq;
+            jb.scale = probs[i].scale;
+            jb.out = reinterpret_cast<__nv_bfloat16*>(ws + off);
+            jb.first = rp.groups;
+            jb.groups_per_token = probs[i].K / kGroup;
+            jb.groups = M * jb.groups_per_token;
+            rp.groups += jb.groups;
             off += ((size_t)M * (size_t)probs[i].K * 2u + 255u) & ~(size_t)255u;
         }
         act_of[i] = a;
     }
+    st = flush_rot();
+    if (st != CQ_OK) return st;
 
     // launches of at most kMaxProblems problems and kMaxActs activations each, larger K
     // first so the long tiles start early
