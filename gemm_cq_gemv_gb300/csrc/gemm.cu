@@ -433,8 +433,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 const uint32_t d = tmem_base + (uint32_t)(kDCol0 + buf * kBT);
                 const int nk = pr.K / kBK;
                 for (int kc = 0; kc < nk; ++kc) {
-                    if (!mbar_wait(&full_a[s], ph, abort_flag, p) ||
-                        !mbar_wait(&full_b[s], ph, abort_flag, p)) { ok = false; break; }
+                    // the dequant warps arrive on full_b only after waiting on the TMA
+                    // barrier of the same stage, so it also orders the TMA writes
+                    if (!mbar_wait(&full_b[s], ph, abort_flag, p)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t bdesc0 = smem_desc_sw128(smem_u32(stage_ptr(s)));
                     const uint32_t a0 = tmem_base + (uint32_t)(s * kACols);
