@@ -46,32 +46,47 @@ namespace cq {
 namespace {
 
 constexpr int kBO = 128;                 // out-rows per tile (MMA M, TMEM lanes)
-constexpr int kBT = 192;                 // tokens per tile (MMA N)
-constexpr int kBK = 64;                  // K per stage (128 bytes of bf16)
-constexpr int kStages = 4;
+constexpr int kBK = 64;                  // K per stage (128 bytes of 16-bit operands)
 constexpr int kThreadsGemm = 832;        // 26 warps: TMA, MMA, 8 epilogue, 16 dequant
 constexpr int kEpiWarp0 = 2;             // warps 2..9: two per TMEM lane quarter
 constexpr int kEpiWarps = 8;
 constexpr int kDequantWarp0 = kEpiWarp0 + kEpiWarps;
 constexpr int kDequantWarps = 8;         // per stage: two per TMEM lane quarter
 constexpr int kDequantGroups = 2;        // warps 10..17 take even stages, 18..25 odd ones
-constexpr int kXTileBytes = kBT * kBK * 2;            // 24 KB of bf16 activations
 constexpr int kPTileBytes = kBO * kBK / 2;            // 4 KB of packed nibbles
-constexpr int kStageBytes = kXTileBytes + kPTileBytes;
 constexpr int kTmemCols = 512;
 constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
-constexpr int kDCol0 = kStages * kACols;              // accumulators start at column 128
-constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + 4 stages + barriers
+constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + stages + barriers
+constexpr int kBarBytes = 512;           // barrier block: barriers, TMEM slot, flags, levels
 constexpr int kMaxProblems = 120;
 constexpr int kMaxActs = 8;
-static_assert(kDCol0 + 2 * kBT <= kTmemCols, "tensor memory budget");
+
+// Tile configuration of one kernel instance.
+//   BT      tokens per tile (MMA N)
+//   F16     fp16 operands and fp32 output (the batched-decode form of the product);
+//           otherwise bf16 operands and bf16 output (prefill)
+//   STAGES  depth of the shared-memory ring (= tensor-memory A stages)
+template <int BT_, bool F16_, int STAGES_>
+struct GemmCfg {
+    static constexpr int BT = BT_;
+    static constexpr bool F16 = F16_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int XTILE = BT * kBK * 2;        // activation tile bytes
+    static constexpr int STAGE = XTILE + kPTileBytes;
+    static constexpr int DCOL0 = STAGES * kACols;     // accumulators after the A stages
+    static_assert(DCOL0 + 2 * BT <= kTmemCols, "tensor memory budget");
+    static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+    static_assert((3 * STAGES + 4) * 8 + 8 + 64 <= kBarBytes, "barrier block");
+};
+using PrefillCfg = GemmCfg<192, false, 4>;   // 24 KB activation tile, 28 KB stages
+using DecodeCfg = GemmCfg<32, true, 8>;      // 4 KB activation tile, 8 KB stages
 
 struct GemmProblem {
     CUtensorMap pmap;        // packed bytes as [N][K/2] uint8, box 32 x 128
     const uint8_t* packed;   // [N][K/128][64]
     const uint16_t* norms;   // [N][K/128]
     const float* scale;      // [M]
-    __nv_bfloat16* Y;        // [M][N]
+    void* Y;                 // [M][N] bf16 (prefill) or fp32 (decode)
     int N, K;
     int act;                 // index of the activation tensor map
     int tiles_n;
@@ -163,9 +178,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both bf16 or both fp16
+// (format code 1 / 0), both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int m, int n, bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
 }
 
@@ -217,14 +233,14 @@ __device__ __forceinline__ int find_problem(const GemmParams& p, int tile) {
 }
 
 // ---------------------------------------------------------------------------------
-// B = bf16(Hu @ q * s_t / 128) per 128-group; one warp per (token, group), for up to
+// B = bf16 or fp16 (Hu @ q * s_t / 128) per 128-group; one warp per (token, group), for up to
 // kMaxRotJobs distinct activations in one launch.  The fp32 butterfly is exact (integers
 // below 2^24); the product with s_t / 128 and the bf16 conversion are the only roundings.
 // ---------------------------------------------------------------------------------
 struct RotJob {
     const int8_t* Xq;
     const float* scale;
-    __nv_bfloat16* out;
+    void* out;                 // bf16 or fp16 [M][K]
     int64_t first;             // first group of this job in the launch's group numbering
     int64_t groups;            // M * K / 128
     int64_t groups_per_token;  // K / 128
@@ -236,8 +252,9 @@ struct RotParams {
     int64_t groups;            // all jobs
 };
 
+template <bool F16>
 __global__ void __launch_bounds__(256)
-rotate_act_bf16_kernel(const __grid_constant__ RotParams rp) {
+rotate_act_kernel16(const __grid_constant__ RotParams rp) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * 256) >> 5;
@@ -263,12 +280,19 @@ rotate_act_bf16_kernel(const __grid_constant__ RotParams rp) {
             v3 = upper ? (p3 - v3) : (v3 + p3);
         }
         const float sc = __ldg(jb.scale + gi / jb.groups_per_token) * (1.0f / 128.0f);
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v0 * sc, v1 * sc);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v2 * sc, v3 * sc);
         uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(jb.out + gi * kGroup + 4 * lane) = pk;
+        if constexpr (F16) {
+            __half2 lo = __floats2half2_rn(v0 * sc, v1 * sc);
+            __half2 hi = __floats2half2_rn(v2 * sc, v3 * sc);
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v0 * sc, v1 * sc);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v2 * sc, v3 * sc);
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        }
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(jb.out) + gi * kGroup + 4 * lane) = pk;
     }
 }
 
@@ -326,10 +350,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+template <class C>
 __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_constant__ GemmParams p) {
+    constexpr int kBT = C::BT;
+    constexpr int kStages = C::STAGES;
+    constexpr int kXTileBytes = C::XTILE;
+    constexpr int kStageBytes = C::STAGE;
+    constexpr int kDCol0 = C::DCOL0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // The codeword-pair table sits at a 64 KB boundary of the shared window (the address
-    // of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the four
+    // of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
     // 1024-byte aligned stages fill the space below it, then the space above it.
     const uint32_t sbase = smem_u32(smem_raw), send = sbase + (uint32_t)kGemmSmem;
     const uint32_t tbase = (sbase + 65535u) & ~65535u;
@@ -342,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     };
     float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [256][32]
     uint64_t* bars = reinterpret_cast<uint64_t*>(gen(b0 + (uint32_t)(kStages - nA) * kStageBytes));
-    const bool layout_ok = b0 + (uint32_t)(kStages - nA) * kStageBytes + 256u <= send;
+    const bool layout_ok = b0 + (uint32_t)(kStages - nA) * kStageBytes + (uint32_t)kBarBytes <= send;
     uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
     uint64_t* full_b = bars + kStages;            // dequant: A stage written to TMEM
     uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
@@ -359,7 +389,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
 
     // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]), one copy per lane, built
     // from the 16 levels staged in shared memory (one unrolled select per level thread)
-    float* slv = reinterpret_cast<float*>(bars) + 40;   // 64 bytes inside the barrier block
+    float* slv = reinterpret_cast<float*>(tmem_slot + 4);   // 64 bytes inside the barrier block
     if (tid < 16) {
         float v = 0.0f;
 #pragma unroll
@@ -419,7 +449,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(kBO, kBT);
+            constexpr uint32_t idesc = idesc_f16kind(kBO, kBT, C::F16);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -472,7 +502,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             const int o = tr.nt * kBO + q * 32 + lane;
             const int t0 = tr.mt * kBT + th * (kBT / 2);
             const bool ook = o < pr.N;
-            __nv_bfloat16* ycol = pr.Y + o;
+            __nv_bfloat16* ycol = static_cast<__nv_bfloat16*>(pr.Y) + o;
+            float* ycolf = static_cast<float*>(pr.Y) + o;
             // 16-column pieces, each load issued before the previous piece is stored
             constexpr int kPieces = (kBT / 2) / 16;
             uint32_t rr[2][16];
@@ -481,7 +512,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int t = tb + j;
-                    if (t < p.M) ycol[(int64_t)t * pr.N] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    if (t < p.M) {
+                        if constexpr (C::F16) ycolf[(int64_t)t * pr.N] = __uint_as_float(r[j]);
+                        else ycol[(int64_t)t * pr.N] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    }
                 }
             };
             tmem_ld16_async(col0, rr[0]);
@@ -529,8 +563,13 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float2 cn = __fmul2_rn(c[j], n2);
-                        __nv_bfloat162 v = __floats2bfloat162_rn(cn.x, cn.y);
-                        pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
+                        if constexpr (C::F16) {
+                            __half2 v = __floats2half2_rn(cn.x, cn.y);
+                            pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
+                        } else {
+                            __nv_bfloat162 v = __floats2bfloat162_rn(cn.x, cn.y);
+                            pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
+                        }
                     }
                 }
                 tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
@@ -559,7 +598,7 @@ static __device__ unsigned int g_gemm_err;
 std::mutex g_host_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned int* g_err_ptr[64] = {nullptr};
-bool g_attr_done[64] = {false};
+bool g_attr_done[64][2] = {};
 
 cq_status host_setup(unsigned int** err) {
     int dev = 0;
@@ -583,11 +622,17 @@ cq_status host_setup(unsigned int** err) {
         if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
         g_err_ptr[dev] = static_cast<unsigned int*>(pe);
     }
-    if (!g_attr_done[dev]) {
-        const size_t smem = (size_t)kGemmSmem;
-        e = cudaFuncSetAttribute(cq_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (!g_attr_done[dev][0]) {
+        e = cudaFuncSetAttribute(cq_gemm_kernel<PrefillCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemmSmem);
         if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
-        g_attr_done[dev] = true;
+        g_attr_done[dev][0] = true;
+    }
+    if (!g_attr_done[dev][1]) {
+        e = cudaFuncSetAttribute(cq_gemm_kernel<DecodeCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemmSmem);
+        if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+        g_attr_done[dev][1] = true;
     }
     *err = g_err_ptr[dev];
     return CQ_OK;
@@ -639,12 +684,13 @@ cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N
     return CQ_OK;
 }
 
-cq_status make_act_map(CUtensorMap* map, const void* base, int64_t M, int64_t K) {
+cq_status make_act_map(CUtensorMap* map, const void* base, int64_t M, int64_t K, int bt, bool f16) {
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBT};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)bt};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+    CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -687,34 +733,19 @@ extern "C" size_t cq_gemm_grouped_workspace_bytes(const cq_gemm_problem* probs, 
     return total;
 }
 
-extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, int64_t M, int g,
-                                     int b, const cq_codebook* cbk, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
-    if (!probs || count < 1 || !cbk || M < 1 || M > (1 << 30)) return CQ_ERR_INVALID_ARG;
-    if (g != kGroup || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
-    if (b != 4) return CQ_ERR_UNSUPPORTED;
-    for (int i = 0; i < count; ++i) {
-        const cq_gemm_problem& q = probs[i];
-        if (!q.packed || !q.norms || !q.Xq || !q.scale || !q.Y) return CQ_ERR_INVALID_ARG;
-        if (q.N < 1 || q.K < kGroup || q.K % kGroup != 0 || q.N % 16 != 0 || q.K > (1 << 24) ||
-            q.N > (1 << 24))
-            return CQ_ERR_INVALID_ARG;
-        if (!aligned16(q.packed) || !aligned16(q.norms) || !aligned16(q.Xq) ||
-            !aligned16(q.scale) || !aligned16(q.Y))
-            return CQ_ERR_ALIGNMENT;
-        for (int j = 0; j < i; ++j)
-            if (probs[j].Xq == q.Xq && probs[j].K != q.K) return CQ_ERR_INVALID_ARG;
-    }
-    const size_t need = cq_gemm_grouped_workspace_bytes(probs, count, M);
-    if (!workspace || workspace_bytes < need) return CQ_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CQ_ERR_ALIGNMENT;
-
+// The launch sequence shared by the prefill GEMM and the batched decode product: the
+// distinct activations are rotated into the workspace, then the problems go out in
+// launches of at most kMaxProblems problems and kMaxActs activations each.  The caller
+// has validated the problems and the workspace.  Each problem's Y is bf16 (prefill) or
+// fp32 (decode, C::F16).
+template <class C>
+cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
+                      const cq_codebook* cbk, void* workspace, cudaStream_t cs) {
     unsigned int* err = nullptr;
     cq_status st = host_setup(&err);
     if (st != CQ_OK) return st;
-    cudaStream_t cs = as_stream(stream);
 
-    // distinct activations -> rotated bf16 copies in the workspace, up to kMaxRotJobs
+    // distinct activations -> rotated 16-bit copies in the workspace, up to kMaxRotJobs
     // activations per rotation launch
     if (count > 1024) return CQ_ERR_UNSUPPORTED;
     const int8_t* act_src[1024];
@@ -732,7 +763,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
         int64_t grid = (rp.groups + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
         if (grid > cap) grid = cap;
-        rotate_act_bf16_kernel<<<(unsigned)grid, 256, 0, cs>>>(rp);
+        rotate_act_kernel16<C::F16><<<(unsigned)grid, 256, 0, cs>>>(rp);
         rp.njobs = 0;
         rp.groups = 0;
         return check_launch();
@@ -753,7 +784,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
             RotJob& jb = rp.job[rp.njobs++];
             jb.Xq = probs[i].Xq;
             jb.scale = probs[i].scale;
-            jb.out = reinterpret_cast<__nv_bfloat16*>(ws + off);
+            jb.out = ws + off;
             jb.first = rp.groups;
             jb.groups_per_token = probs[i].K / kGroup;
             jb.groups = M * jb.groups_per_token;
@@ -783,20 +814,20 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
         int map_of_act[1024];
         for (int a = 0; a < nact; ++a) map_of_act[a] = -1;
         int nmaps = 0, np = 0, tiles = 0;
-        const int tiles_m = (int)((M + kBT - 1) / kBT);
+        const int tiles_m = (int)((M + C::BT - 1) / C::BT);
         while (i0 < count && np < kMaxProblems) {
             const int pi = order[i0];
             const int a = act_of[pi];
             if (map_of_act[a] < 0) {
                 if (nmaps == kMaxActs) break;
-                st = make_act_map(&prm.tmap[nmaps], act_dst[a], M, act_K[a]);
+                st = make_act_map(&prm.tmap[nmaps], act_dst[a], M, act_K[a], C::BT, C::F16);
                 if (st != CQ_OK) return st;
                 map_of_act[a] = nmaps++;
             }
             const cq_gemm_problem& q = probs[pi];
             GemmProblem& gp = prm.prob[np++];
             gp.packed = q.packed; gp.norms = q.norms; gp.scale = q.scale;
-            gp.Y = reinterpret_cast<__nv_bfloat16*>(q.Y);
+            gp.Y = q.Y;
             gp.N = (int)q.N; gp.K = (int)q.K; gp.act = map_of_act[a];
             st = make_packed_map(&gp.pmap, q.packed, q.N, q.K);
             if (st != CQ_OK) return st;
@@ -814,11 +845,37 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
         prm.timeout_ns = 2000000000ull;   // 2 s per wait
         const size_t smem = (size_t)kGemmSmem;
         const int grid = tiles < sm_count() ? tiles : sm_count();
-        cq_gemm_kernel<<<grid, kThreadsGemm, smem, cs>>>(prm);
+        cq_gemm_kernel<C><<<grid, kThreadsGemm, smem, cs>>>(prm);
         st = check_launch();
         if (st != CQ_OK) return st;
     }
     return CQ_OK;
+}
+
+
+extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, int64_t M, int g,
+                                     int b, const cq_codebook* cbk, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    if (!probs || count < 1 || !cbk || M < 1 || M > (1 << 30)) return CQ_ERR_INVALID_ARG;
+    if (g != kGroup || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
+    if (b != 4) return CQ_ERR_UNSUPPORTED;
+    for (int i = 0; i < count; ++i) {
+        const cq_gemm_problem& q = probs[i];
+        if (!q.packed || !q.norms || !q.Xq || !q.scale || !q.Y) return CQ_ERR_INVALID_ARG;
+        if (q.N < 1 || q.K < kGroup || q.K % kGroup != 0 || q.N % 16 != 0 || q.K > (1 << 24) ||
+            q.N > (1 << 24))
+            return CQ_ERR_INVALID_ARG;
+        if (!aligned16(q.packed) || !aligned16(q.norms) || !aligned16(q.Xq) ||
+            !aligned16(q.scale) || !aligned16(q.Y))
+            return CQ_ERR_ALIGNMENT;
+        for (int j = 0; j < i; ++j)
+            if (probs[j].Xq == q.Xq && probs[j].K != q.K) return CQ_ERR_INVALID_ARG;
+    }
+    const size_t need = cq_gemm_grouped_workspace_bytes(probs, count, M);
+    if (!workspace || workspace_bytes < need) return CQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CQ_ERR_ALIGNMENT;
+
+    return run_grouped<PrefillCfg>(probs, count, M, b, cbk, workspace, as_stream(stream));
 }
 
 extern "C" cq_status cq_gemm(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
@@ -831,3 +888,20 @@ extern "C" cq_status cq_gemm(const uint8_t* packed, const uint16_t* norms, int64
     return cq_gemm_grouped(&q, 1, M, g, b, cbk, workspace, workspace_bytes, stream);
 }
 
+
+namespace cq {
+
+// The batched decode product of cq_gemv for 4-bit indices on the tensor cores: the same
+// pipeline with 32-token tiles, fp16 operands (so the result meets the fp32 GEMV's error
+// bound) and fp32 output.  `workspace` (16-byte aligned, at least B * K * 2 + 256 bytes)
+// receives the rotated fp16 activations.
+cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
+                      const cq_codebook* cbk, const int8_t* Xq, const float* scale, int64_t B,
+                      float* Y, void* workspace, cudaStream_t st) {
+    cq_gemm_problem q;
+    q.packed = packed; q.norms = norms; q.N = N; q.K = K; q.Xq = Xq; q.scale = scale;
+    q.Y = reinterpret_cast<uint16_t*>(Y);   // the pipeline stores fp32 for this configuration
+    return run_grouped<DecodeCfg>(&q, 1, B, 4, cbk, workspace, st);
+}
+
+}  // namespace cq

@@ -222,6 +222,8 @@ __device__ __forceinline__ Reduce carve_reduce(void* base, int tb) {
 // flight, so the load latency overlaps the decode instead of following it.
 // ---------------------------------------------------------------------------------
 constexpr int kUnitRows = 4;
+// smallest batch that cq_gemv sends to the tensor-core path (4-bit indices)
+constexpr int64_t kTensorMinBatch = 3;
 // row coordinates of the tensor copies are 32-bit (with a tile of slack past N)
 constexpr int64_t kMaxGemvRows = ((int64_t)1 << 31) - 1024;
 constexpr int kRing = 4;       // a power of two (slot = unit & 3, phase = unit >> 2)
@@ -1027,6 +1029,10 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     if (!aligned16(workspace)) return CQ_ERR_ALIGNMENT;
     if (K > 2 * kWarps2 * kSeg) return CQ_ERR_UNSUPPORTED;   // at most 2 segments per warp
     cudaStream_t st = as_stream(stream);
+    // batches of 4-bit rows go through the tensor cores: the weights are read and decoded
+    // once for all tokens (the workspace, B * K * 4 bytes, holds the fp16 activations)
+    if (b == 4 && B >= kTensorMinBatch && N % 16 == 0)
+        return gemv_tensor(packed, norms, N, K, cbk, Xq, scale, B, Y, workspace, st);
     // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
     // tokens per pass when each warp owns a single segment
     const int nseg = (int)((K + kSeg - 1) / kSeg);

@@ -109,13 +109,21 @@ cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* Xq, float* s
  *   Y[t][o] = s_t * sum_j (norm[o][j] / 128) * sum_i cb[idx[o][j][i]] * xr[t][128 j + i]
  * with xr = Hu @ Xq per group (the rotated int8 activations, exact integers), which
  * equals (W_hat @ (s * Xq)^T)^T in real arithmetic because Hu is symmetric.
- * The rotation is done once per call into `workspace` and shared by every row.
+ * Two execution paths, chosen from the arguments:
+ *   - B <= 2, or b < 4, or N not a multiple of 16: the CUDA-core GEMV, fp32 products
+ *     and accumulation; at B <= 2 the rotation happens inside the kernel, otherwise
+ *     once per call into `workspace`, shared by every row.
+ *   - b = 4, B >= 3, N a multiple of 16: the tensor-core pipeline of cq_gemm with 32-token
+ *     tiles.  The weights are decoded once for all tokens; the operands are fp16
+ *     (cb * norm, and xr * s_t / 128 in `workspace`), the accumulation fp32.  The
+ *     relative error stays within 1e-3 of the exact product; activations must satisfy
+ *     max |X[t][k]| <= 65504 (fp16 range).
  *   packed, norms  as written by cq_encode
  *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
  *   Y  [B][N] float32
  *   workspace      device scratch of at least cq_gemv_workspace_bytes(B, K) bytes
- * K is limited to 32768 and N to 2^31 - 1024 (CQ_ERR_UNSUPPORTED above).  Deterministic: the same inputs give
- * bit-identical outputs.
+ * K is limited to 32768 and N to 2^31 - 1024 (CQ_ERR_UNSUPPORTED above).  Deterministic:
+ * the same inputs give bit-identical outputs.
  * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
 size_t cq_gemv_workspace_bytes(int64_t B, int64_t K);
 cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,

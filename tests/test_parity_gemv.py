@@ -87,6 +87,15 @@ def test_cq_gemv_large_sampled(m, B):
     assert max_rel_err(Y, ref) < TOL
 
 
+@pytest.mark.parametrize("N,K,B", [(400, 1152, 3), (128, 8192, 8), (1040, 4096, 37), (16, 128, 5),
+                                   (2048, 2048, 32)])
+def test_cq_gemv_batched_tensor_path(N, K, B):
+    """4-bit batches of >= 3 tokens (rows a multiple of 16) run on the tensor cores with fp16
+    operands and fp32 accumulation: ragged row tiles, ragged token tiles, long K."""
+    Y, ref = _cq_case(N, K, 4, B, 5 * N + K, 13 * K + B, outliers=True)
+    assert max_rel_err(Y, ref) < TOL
+
+
 def test_cq_gemv_batch_consistency():
     """Each token of a batched call equals the same token alone (up to fp32 rounding)."""
     cb = fitted_cb28()
