@@ -69,6 +69,8 @@ SIGNATURES = {
     "cq_device_error": (_INT, [_P]),
     "q4_0_quantize": (_INT, [_P, _I64, _I64, _P, _P]),
     "q4_0_gemv": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P]),
+    "q4_0_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
+    "q4_0_gemm": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P]),
 }
 
 
@@ -294,5 +296,25 @@ def q4_0_gemv(blocks, N, K, X, Y=None, stream=None):
         Y = torch.empty((B, N), dtype=torch.float32, device=X.device)
     _check("q4_0_gemv", lib().q4_0_gemv(_ptr(blocks, torch.uint8, "blocks"), N, K,
                                         _ptr(X, torch.float32, "X"), B, _ptr(Y, torch.float32, "Y"),
+                                        _stream(stream)))
+    return Y
+
+
+def q4_0_gemm_workspace_bytes(M, K) -> int:
+    return int(lib().q4_0_gemm_workspace_bytes(M, K))
+
+
+def q4_0_gemm(blocks, N, K, X, Y=None, workspace=None, stream=None):
+    """Q4_0 GEMM on the tensor cores: Y [M, N] float32 for float32 activations X [M, K]
+    (ceil(K/32) a multiple of 8)."""
+    M = X.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    need = q4_0_gemm_workspace_bytes(M, K)
+    if workspace is None:
+        workspace = torch.empty((max(need, 256),), dtype=torch.uint8, device=X.device)
+    _check("q4_0_gemm", lib().q4_0_gemm(_ptr(blocks, torch.uint8, "blocks"), N, K,
+                                        _ptr(X, torch.float32, "X"), M, _ptr(Y, torch.float32, "Y"),
+                                        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
                                         _stream(stream)))
     return Y

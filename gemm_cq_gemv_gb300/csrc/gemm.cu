@@ -61,25 +61,41 @@ constexpr int kBarBytes = 512;           // barrier block: barriers, TMEM slot, 
 constexpr int kMaxProblems = 120;
 constexpr int kMaxActs = 8;
 
+// Q4_0 weights reach shared memory in slabs of 256 k (8 blocks, 144 bytes per row: the
+// smallest 16-byte multiple of the 18-byte block), on a ring of slabs; each slab feeds
+// four 64-k stages.
+constexpr int kQSlabK = 256;
+constexpr int kQSlabRowBytes = 144;
+constexpr int kQSlabBytes = kBO * kQSlabRowBytes;       // 18 KB
+
+enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
+
 // Tile configuration of one kernel instance.
 //   BT      tokens per tile (MMA N)
 //   F16     fp16 operands and fp32 output (the batched-decode form of the product);
 //           otherwise bf16 operands and bf16 output (prefill)
 //   STAGES  depth of the shared-memory ring (= tensor-memory A stages)
-template <int BT_, bool F16_, int STAGES_>
+//   FMT     weight format: CQ (packed indices + norms) or Q4_0 blocks
+//   SLABS   Q4_0: depth of the weight-slab ring
+template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
     static constexpr int STAGES = STAGES_;
+    static constexpr int FMT = FMT_;
+    static constexpr int SLABS = SLABS_;
     static constexpr int XTILE = BT * kBK * 2;        // activation tile bytes
-    static constexpr int STAGE = XTILE + kPTileBytes;
+    static constexpr int STAGE = XTILE + (FMT == kFmtCQ ? kPTileBytes : 0);
     static constexpr int DCOL0 = STAGES * kACols;     // accumulators after the A stages
     static_assert(DCOL0 + 2 * BT <= kTmemCols, "tensor memory budget");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-    static_assert((3 * STAGES + 4) * 8 + 8 + 64 <= kBarBytes, "barrier block");
+    static_assert((3 * STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
+    static_assert(FMT == kFmtCQ || (F16 && SLABS >= 2), "Q4_0 runs with fp16 operands on a slab ring");
 };
-using PrefillCfg = GemmCfg<192, false, 4>;   // 24 KB activation tile, 28 KB stages
-using DecodeCfg = GemmCfg<32, true, 8>;      // 4 KB activation tile, 8 KB stages
+using PrefillCfg = GemmCfg<192, false, 4>;               // 24 KB activation tile, 28 KB stages
+using DecodeCfg = GemmCfg<32, true, 8>;                  // 4 KB activation tile, 8 KB stages
+using Q40WideCfg = GemmCfg<192, true, 4, kFmtQ40, 4>;    // Q4_0, many tokens: 96 + 72 KB
+using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4>;   // Q4_0, up to 32 tokens: 32 + 72 KB
 
 struct GemmProblem {
     CUtensorMap pmap;        // packed bytes as [N][K/2] uint8, box 32 x 128
@@ -296,6 +312,40 @@ rotate_act_kernel16(const __grid_constant__ RotParams rp) {
     }
 }
 
+// Q4_0 activations: X [M][K] fp32 -> Xh [M][Kp] fp16, Kp = 32 ceil(K / 32), zero past K.
+// Inside each group of eight k the order is 0 4 1 5 2 6 3 7, the order in which the
+// dequant warps write a block's nibbles (a word's nibbles j and j + 4 share one fp16
+// pair); the product sums over k, so the same order on both operands leaves it unchanged.
+__global__ void __launch_bounds__(256)
+q4_act_kernel(const float* __restrict__ X, int64_t K, int64_t Kp, int64_t groups,
+              uint16_t* __restrict__ Xh) {
+    const int64_t gpt = Kp / 8;   // groups of eight per token
+    for (int64_t gg = (int64_t)blockIdx.x * 256 + threadIdx.x; gg < groups;
+         gg += (int64_t)gridDim.x * 256) {
+        const int64_t t = gg / gpt;
+        const int64_t k0 = (gg - t * gpt) * 8;
+        const float* xr = X + t * K;
+        float v[8];
+        if (k0 + 8 <= K && (K & 3) == 0) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(xr + k0));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(xr + k0 + 4));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = (k0 + i < K) ? __ldg(xr + k0 + i) : 0.0f;
+        }
+        uint4 o;
+        uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __half2 h = __floats2half2_rn(v[j], v[j + 4]);
+            ow[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(Xh + t * Kp + k0) = o;
+    }
+}
+
 // ---------------------------------------------------------------------------------
 // The persistent tcgen05 GEMM.
 // ---------------------------------------------------------------------------------
@@ -358,27 +408,42 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     constexpr int kStageBytes = C::STAGE;
     constexpr int kDCol0 = C::DCOL0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // The codeword-pair table sits at a 64 KB boundary of the shared window (the address
-    // of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
+    // CQ: the codeword-pair table sits at a 64 KB boundary of the shared window (the
+    // address of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
     // 1024-byte aligned stages fill the space below it, then the space above it.
+    // Q4_0: no table; the stages, then the two weight slabs.
     const uint32_t sbase = smem_u32(smem_raw), send = sbase + (uint32_t)kGemmSmem;
-    const uint32_t tbase = (sbase + 65535u) & ~65535u;
     const uint32_t a0 = (sbase + 1023u) & ~1023u;
-    const int nA = tbase >= a0 + kStageBytes ? min(kStages, (int)((tbase - a0) / kStageBytes)) : 0;
-    const uint32_t b0 = tbase + 256u * 32u * 8u;
+    uint32_t tbase, b0, slab0, bars_at;
+    int nA;
+    if constexpr (C::FMT == kFmtCQ) {
+        tbase = (sbase + 65535u) & ~65535u;
+        nA = tbase >= a0 + kStageBytes ? min(kStages, (int)((tbase - a0) / kStageBytes)) : 0;
+        b0 = tbase + 256u * 32u * 8u;
+        slab0 = 0;
+        bars_at = b0 + (uint32_t)(kStages - nA) * kStageBytes;
+    } else {
+        tbase = 0;
+        nA = kStages;
+        b0 = a0;
+        slab0 = a0 + (uint32_t)kStages * kStageBytes;
+        bars_at = slab0 + (uint32_t)(C::SLABS * kQSlabBytes);
+    }
     auto gen = [&](uint32_t a) { return smem_raw + (a - sbase); };
     auto stage_ptr = [&](int s) {
         return gen(s < nA ? a0 + (uint32_t)s * kStageBytes : b0 + (uint32_t)(s - nA) * kStageBytes);
     };
-    float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [256][32]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(gen(b0 + (uint32_t)(kStages - nA) * kStageBytes));
-    const bool layout_ok = b0 + (uint32_t)(kStages - nA) * kStageBytes + (uint32_t)kBarBytes <= send;
+    float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [256][32] (CQ)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gen(bars_at));
+    const bool layout_ok = bars_at + (uint32_t)kBarBytes <= send;
     uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
     uint64_t* full_b = bars + kStages;            // dequant: A stage written to TMEM
     uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
     uint64_t* acc_full = bars + 3 * kStages;      // [2] accumulator buffer ready
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator buffer drained
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    uint64_t* slab_full = acc_empty + 2;          // [SLABS] Q4_0: weight slab landed
+    uint64_t* slab_empty = slab_full + C::SLABS;  // [SLABS] Q4_0: slab read by its four stages
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(slab_empty + C::SLABS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -397,9 +462,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         slv[tid] = v;
     }
     __syncthreads();
-    for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
-        const int e = i >> 5;
-        lut2[i] = make_float2(slv[e & 15], slv[e >> 4]);
+    if constexpr (C::FMT == kFmtCQ) {
+        for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
+            const int e = i >> 5;
+            lut2[i] = make_float2(slv[e & 15], slv[e >> 4]);
+        }
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -410,6 +477,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kEpiWarps);
+        }
+        for (int b = 0; b < C::SLABS; ++b) {
+            mbar_init(&slab_full[b], 1);
+            mbar_init(&slab_empty[b], 4 * kDequantWarps);   // four stages, eight warps each
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -431,16 +502,36 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
+            int pg = 0;   // Q4_0: slabs issued
             for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
                 const TileRef tr = tile_ref(p, tile);
                 const GemmProblem& pr = p.prob[tr.prob];
                 const CUtensorMap* xmap = &p.tmap[pr.act];
                 for (int kc = 0; kc < pr.K / kBK; ++kc) {
+                    if constexpr (C::FMT == kFmtQ40) {
+                        if ((kc & 3) == 0) {   // the slab of this stage and the next three
+                            const int qs = pg % C::SLABS;
+                            const uint32_t sph = (uint32_t)((pg / C::SLABS) & 1);
+                            if (!mbar_wait(&slab_empty[qs], sph ^ 1u, abort_flag, p)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_tx(&slab_full[qs], kQSlabBytes);
+                            tma_load_2d(gen(slab0 + (uint32_t)(qs * kQSlabBytes)), &pr.pmap,
+                                        (kc >> 2) * kQSlabRowBytes, tr.nt * kBO, &slab_full[qs]);
+                            ++pg;
+                        }
+                    }
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p)) { ok = false; break; }
                     uint8_t* st = stage_ptr(s);
-                    mbar_arrive_tx(&full_a[s], kXTileBytes + kPTileBytes);
-                    tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
-                    tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK / 2), tr.nt * kBO, &full_a[s]);
+                    if constexpr (C::FMT == kFmtCQ) {
+                        mbar_arrive_tx(&full_a[s], kXTileBytes + kPTileBytes);
+                        tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
+                        tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK / 2), tr.nt * kBO, &full_a[s]);
+                    } else {
+                        mbar_arrive_tx(&full_a[s], kXTileBytes);
+                        tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
+                    }
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
@@ -550,6 +641,55 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 if (gi % kDequantGroups != grp) continue;   // the other group's stage
                 const int s = gi % kStages;
                 const uint32_t ph = (uint32_t)((gi / kStages) & 1);
+                if constexpr (C::FMT == kFmtQ40) {
+                    // the full_a wait frees the A stage (its previous MMA has completed)
+                    // and, through full_b, orders the activation tile for the MMA
+                    if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
+                    const int sg = gi >> 2;   // every K is a whole number of slabs
+                    const int qs = sg % C::SLABS;
+                    if (!mbar_wait(&slab_full[qs], (uint32_t)((sg / C::SLABS) & 1), abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    // block (kc & 3) * 2 + kh of this row's 144-byte slab row starts at
+                    // byte 36 (kc & 3) + 18 kh: five words from the 4-byte boundary at or
+                    // below it hold the fp16 scale and the 16 nibble bytes
+                    const uint32_t* w32 = reinterpret_cast<const uint32_t*>(
+                        gen(slab0 + (uint32_t)(qs * kQSlabBytes) + (uint32_t)(r * kQSlabRowBytes)));
+                    const int wb = 9 * (kc & 3) + 4 * kh;
+                    uint32_t w[5];
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) w[i] = w32[wb + i];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&slab_empty[qs]);
+                    uint32_t d2;   // the scale in both halves
+                    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d2) : "r"(w[0]), "r"(kh ? 0x3232u : 0x1010u));
+                    const __half2 hd = *reinterpret_cast<const __half2*>(&d2);
+                    const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6408u),
+                                                        __ushort_as_half((unsigned short)0x6408u));
+                    const uint32_t sh = kh ? 32u : 16u;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        // nibbles 0..7 of this word are the block's elements 8i..8i+7;
+                        // output word 4i + j holds elements (8i + j, 8i + j + 4), each as
+                        // 1024 + nib in fp16, minus 1032, times d
+                        const uint32_t qw = __funnelshift_rc(w[i], w[i + 1], sh);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t v = ((qw >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+                            __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v), bias);
+                            h = __hmul2(h, hd);
+                            pk[4 * i + j] = *reinterpret_cast<uint32_t*>(&h);
+                        }
+                    }
+                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    continue;
+                }
                 const float nrm = load_norm(pr, tr.nt * kBO + r, kc);
                 if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
                 const uint4 w = *reinterpret_cast<const uint4*>(stage_ptr(s) + kXTileBytes + r * 32 + kh * 16);
@@ -598,7 +738,17 @@ static __device__ unsigned int g_gemm_err;
 std::mutex g_host_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned int* g_err_ptr[64] = {nullptr};
-bool g_attr_done[64][2] = {};
+bool g_attr_done[64][4] = {};
+
+template <class C>
+cq_status set_smem_attr(int dev, int slot) {
+    if (g_attr_done[dev][slot]) return CQ_OK;
+    const cudaError_t e = cudaFuncSetAttribute(cq_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kGemmSmem);
+    if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+    g_attr_done[dev][slot] = true;
+    return CQ_OK;
+}
 
 cq_status host_setup(unsigned int** err) {
     int dev = 0;
@@ -622,18 +772,11 @@ cq_status host_setup(unsigned int** err) {
         if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
         g_err_ptr[dev] = static_cast<unsigned int*>(pe);
     }
-    if (!g_attr_done[dev][0]) {
-        e = cudaFuncSetAttribute(cq_gemm_kernel<PrefillCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kGemmSmem);
-        if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
-        g_attr_done[dev][0] = true;
-    }
-    if (!g_attr_done[dev][1]) {
-        e = cudaFuncSetAttribute(cq_gemm_kernel<DecodeCfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kGemmSmem);
-        if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
-        g_attr_done[dev][1] = true;
-    }
+    cq_status st = set_smem_attr<PrefillCfg>(dev, 0);
+    if (st == CQ_OK) st = set_smem_attr<DecodeCfg>(dev, 1);
+    if (st == CQ_OK) st = set_smem_attr<Q40WideCfg>(dev, 2);
+    if (st == CQ_OK) st = set_smem_attr<Q40NarrowCfg>(dev, 3);
+    if (st != CQ_OK) return st;
     *err = g_err_ptr[dev];
     return CQ_OK;
 }
@@ -675,6 +818,22 @@ cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N
     cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
     cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
     cuuint32_t box[2] = {(cuuint32_t)(kBK / 2), (cuuint32_t)kBO};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { set_last_cuda_error((int)r); return CQ_ERR_CUDA; }
+    return CQ_OK;
+}
+
+// Q4_0 block rows [N][nblk * 18] bytes (nblk a multiple of 8), box = one 144-byte slab
+// row (8 blocks) x 128 rows
+cq_status make_q40_map(CUtensorMap* map, const void* base, int64_t N, int64_t nblk) {
+    const cuuint64_t rowbytes = (cuuint64_t)nblk * 18u;
+    cuuint64_t dims[2] = {rowbytes, (cuuint64_t)N};
+    cuuint64_t strides[1] = {rowbytes};
+    cuuint32_t box[2] = {(cuuint32_t)kQSlabRowBytes, (cuuint32_t)kBO};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -905,3 +1064,81 @@ cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, i
 }
 
 }  // namespace cq
+
+
+// ---------------------------------------------------------------------------------
+// Q4_0 on the tensor cores: the activations are converted once to fp16 (workspace),
+// then the persistent pipeline decodes each weight block once per tile of tokens.
+// ---------------------------------------------------------------------------------
+namespace cq {
+namespace {
+
+int64_t q40_padded_k(int64_t K) { return (K + 31) / 32 * 32; }
+
+template <class C>
+cq_status run_q40(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t M, float* Y,
+                  void* workspace, cudaStream_t cs) {
+    unsigned int* err = nullptr;
+    cq_status st = host_setup(&err);
+    if (st != CQ_OK) return st;
+    const int64_t Kp = q40_padded_k(K);
+    uint16_t* xh = static_cast<uint16_t*>(workspace);
+    {
+        const int64_t groups = M * (Kp / 8);
+        int64_t grid = (groups + 255) / 256;
+        const int64_t cap = (int64_t)sm_count() * 8;
+        if (grid > cap) grid = cap;
+        q4_act_kernel<<<(unsigned)grid, 256, 0, cs>>>(X, K, Kp, groups, xh);
+        st = check_launch();
+        if (st != CQ_OK) return st;
+    }
+    static GemmParams prm;   // large; built on the host, passed by value to the launch
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    memset(&prm, 0, sizeof(prm));
+    st = make_act_map(&prm.tmap[0], xh, M, Kp, C::BT, true);
+    if (st != CQ_OK) return st;
+    GemmProblem& gp = prm.prob[0];
+    gp.packed = blocks;
+    gp.Y = Y;
+    gp.N = (int)N;
+    gp.K = (int)Kp;
+    gp.act = 0;
+    st = make_q40_map(&gp.pmap, blocks, N, Kp / 32);
+    if (st != CQ_OK) return st;
+    const int tiles_m = (int)((M + C::BT - 1) / C::BT);
+    gp.tiles_n = (int)((N + kBO - 1) / kBO);
+    gp.tile_begin = 0;
+    prm.nprob = 1;
+    prm.M = (int)M;
+    prm.tiles_m = tiles_m;
+    prm.total_tiles = gp.tiles_n * tiles_m;
+    prm.err = err;
+    prm.timeout_ns = 2000000000ull;   // 2 s per wait
+    const int grid = prm.total_tiles < sm_count() ? prm.total_tiles : sm_count();
+    cq_gemm_kernel<C><<<grid, kThreadsGemm, (size_t)kGemmSmem, cs>>>(prm);
+    return check_launch();
+}
+
+}  // namespace
+}  // namespace cq
+
+extern "C" size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t K) {
+    if (M < 1 || K < 1) return 0;
+    return ((size_t)M * (size_t)cq::q40_padded_k(K) * 2u + 255u) & ~(size_t)255u;
+}
+
+extern "C" cq_status q4_0_gemm(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t M,
+                               float* Y, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!blocks || !X || !Y || N < 1 || K < 1 || M < 1) return CQ_ERR_INVALID_ARG;
+    if (M > (1 << 30) || N > (1 << 24) || K > (1 << 24) || M * N > ((int64_t)1 << 40))
+        return CQ_ERR_UNSUPPORTED;
+    // whole 256-k slabs: rows of a multiple of 8 blocks (also the 16-byte row stride the
+    // tensor copies need)
+    if ((cq::q40_padded_k(K) / 32) % 8 != 0) return CQ_ERR_UNSUPPORTED;
+    if (!aligned16(blocks) || !aligned16(X) || !aligned16(Y)) return CQ_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < q4_0_gemm_workspace_bytes(M, K)) return CQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CQ_ERR_ALIGNMENT;
+    cudaStream_t cs = as_stream(stream);
+    if (M <= 32) return run_q40<Q40NarrowCfg>(blocks, N, K, X, M, Y, workspace, cs);
+    return run_q40<Q40WideCfg>(blocks, N, K, X, M, Y, workspace, cs);
+}

@@ -209,6 +209,27 @@ cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks, v
 cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t B,
                     float* Y, void* stream);
 
+/* ---- Q4_0 GEMM on the tensor cores (KMCU page, §2, §3 for the block format; the same
+ * product as q4_0_gemv for M tokens at once: prefill, or a decode batch).  Computes
+ *   Y[t][o] = sum_k fp16((nib[o][k] - 8) * d[o][k/32]) * fp16(X[t][k]),
+ * with the products summed in float32 (tcgen05 MMA, fp32 accumulation in tensor memory).
+ * `X` is converted once per call into `workspace` as fp16 [M][32 ceil(K/32)], zero past K;
+ * each weight block is then read and decoded once per tile of up to 192 tokens (32 when
+ * M <= 32).  The relative error stays within 1e-3 of the exact product; X must satisfy
+ * max |X[t][k]| <= 65504 and the scales max |d| <= 8188 (fp16 range).
+ *   blocks [N][ceil(K/32) * 18] uint8 (as written by q4_0_quantize), X [M][K] float32,
+ *   Y [M][N] float32; all 16-byte aligned.
+ *   workspace: >= q4_0_gemm_workspace_bytes(M, K) bytes, 256-byte aligned.
+ * ceil(K/32) must be a multiple of 8 (whole 256-column slabs; CQ_ERR_UNSUPPORTED
+ * otherwise: use q4_0_gemv); N and K are limited to 2^24, M to 2^30.
+ * A device-side wait that does not complete within 2 s sets a device error flag and
+ * the kernel returns early; cq_device_error() reports it as CQ_ERR_DEVICE_TIMEOUT.
+ * Deterministic: the same inputs give bit-identical outputs.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
+size_t q4_0_gemm_workspace_bytes(int64_t M, int64_t K);
+cq_status q4_0_gemm(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t M,
+                    float* Y, void* workspace, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

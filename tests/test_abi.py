@@ -119,3 +119,19 @@ def test_gemm_validation(lib):
     assert lib.cq_gemm_grouped(probs, 3, 512, 128, 4, _cb(), A, 1000, None) == WS
     probs[1].K = 1024   # same Xq with a different K is rejected
     assert lib.cq_gemm_grouped(probs, 3, 512, 128, 4, _cb(), A, big, None) == INV
+
+
+def test_q4_0_gemm_validation(lib):
+    INV, ALN, UNS, WS = 1, 2, 3, 6
+    f = lib.q4_0_gemm
+    big = 1 << 30
+    assert f(A, 64, 256, A, 0, A, A, big, None) == INV      # M = 0
+    assert f(None, 64, 256, A, 4, A, A, big, None) == INV   # NULL
+    assert f(A, 64, 312, A, 4, A, A, big, None) == UNS      # 10 blocks: not whole slabs
+    assert f(A, 64, 257, A, 4, A, A, big, None) == UNS      # 9 blocks
+    assert f(A, 64, 256, M, 4, A, A, big, None) == ALN
+    assert f(A, 64, 256, A, 4, A, A + 16, big, None) == ALN  # workspace 256-byte alignment
+    assert f(A, 64, 256, A, 4, A, A, 100, None) == WS
+    # K = 250 pads to 256 columns: 8 blocks
+    assert cq.q4_0_gemm_workspace_bytes(3, 250) == (3 * 256 * 2 + 255) // 256 * 256
+    assert cq.q4_0_gemm_workspace_bytes(0, 256) == 0
