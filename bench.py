@@ -9,6 +9,11 @@ Weights are encoded once before timing (offline, as the format intends); the tim
 region holds only the decode work.  ``value`` is algorithmic GB/s: packed indices +
 norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step time.
 
+The line also reports, beside the headline, the grouped prefill GEMM of the 20-layer
+model (``prefill``, TFLOP/s) and decode batches of 8 and 32 tokens on the tensor cores
+(``batched``: ``cq_gemv`` at 4 bits and ``q4_0_gemm``, GB/s of weights, each call timed
+alone after an L2 flush).
+
 ``--impl reference`` times the CPU oracle as it stands on a bounded sample of the same
 workload.  ``--gpus N`` (under torchrun) runs N independent replicas, one per GPU:
 the path needs no exchange, so there is no collective beyond the timing barrier.
@@ -266,6 +271,64 @@ def prefill_report(dev, cb, torch, cq, synth, steps, warmup, peaks, kind):
     return out
 
 
+def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 32), kinds=("cq", "q4_0")):
+    """Decode batches on the tensor cores: cq_gemv (4-bit, B >= 3 takes the tcgen05 path) and
+    q4_0_gemm, per large matrix, each call timed alone with CUDA events after an L2 flush
+    (the [8192, 8192] weights would otherwise stay in the 129 MB L2)."""
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    out = {"workload": "large-shape decode batches, weights read once per call for all tokens",
+           "dtype": "fp16 MMA operands, fp32 accumulate, fp32 out",
+           "timing": "per call, CUDA events, L2 flushed before each call"}
+
+    def one(fn):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        cq.cq_device_error()
+        return statistics.median(ts)
+
+    for B in batches:
+        res = {k: {"us": {}, "bytes": 0, "ms": 0.0} for k in kinds}
+        for i, d in enumerate(mats):
+            m = d["m"]
+            g = torch.Generator(device=dev)
+            g.manual_seed(synth.activation_seed(4, B) + i)
+            X = torch.randn((B, m.K), device=dev, generator=g)
+            Y = torch.empty((B, m.N), dtype=torch.float32, device=dev)
+            if "cq" in kinds:
+                Xq, sc = cq.a8_quantize(X)
+                ws = torch.empty((cq.cq_gemv_workspace_bytes(B, m.K),), dtype=torch.uint8, device=dev)
+                ms = one(lambda: cq.cq_gemv(d["packed"], d["norms"], m.N, m.K, 4, cb, Xq, sc, Y=Y,
+                                            workspace=ws))
+                r = res["cq"]
+                r["us"][m.name] = round(ms * 1e3, 1)
+                r["ms"] += ms
+                r["bytes"] += d["packed"].numel() + 2 * d["norms"].numel() + B * m.K + 4 * B * (1 + m.N)
+            if "q4_0" in kinds:
+                ws = torch.empty((max(cq.q4_0_gemm_workspace_bytes(B, m.K), 256),), dtype=torch.uint8,
+                                 device=dev)
+                ms = one(lambda: cq.q4_0_gemm(d["blocks"], m.N, m.K, X, Y=Y, workspace=ws))
+                r = res["q4_0"]
+                r["us"][m.name] = round(ms * 1e3, 1)
+                r["ms"] += ms
+                r["bytes"] += d["blocks"].numel() + 4 * B * m.K + 4 * B * m.N
+        out[f"B{B}"] = {("cq_gemv" if k == "cq" else "q4_0_gemm"):
+                        {"us": v["us"], "GBps": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
+                        for k, v in res.items()}
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
     import gemm_cq_gemv_gb300 as cq
@@ -287,6 +350,12 @@ def gpu_arm(args, rank, world, local_rank):
         return
     mats = build_workload(dev, cb, torch, cq, synth, only=args.case)
     kinds = tuple(args.kernels)
+    if args.batched_only:
+        rep_ = batched_report(mats, cb, torch, cq, synth, dev, args.steps, args.warmup,
+                              batches=(args.batch,), kinds=kinds)
+        if rank == 0:
+            print(json.dumps(rep_), flush=True)
+        return
     cq_b, q4_b, weights = step_bytes(mats)
     cq_b = cq_b if "cq" in kinds else 0
     q4_b = q4_b if "q4_0" in kinds else 0
@@ -406,6 +475,8 @@ def gpu_arm(args, rank, world, local_rank):
         if not args.no_prefill:
             line["prefill"] = prefill_report(dev, cb, torch, cq, synth, max(3, args.steps // 5),
                                              args.warmup, peaks, kind)
+        if not args.no_batched:
+            line["batched"] = batched_report(mats, cb, torch, cq, synth, dev, 10, 3, kinds=kinds)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
         print(json.dumps(line), flush=True)
@@ -510,6 +581,10 @@ def main(argv=None):
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the grouped prefill GEMM (profiling runs)")
     ap.add_argument("--prefill-m", type=int, default=2048)
+    ap.add_argument("--no-batched", action="store_true", help="skip the decode-batch report")
+    ap.add_argument("--batched-only", action="store_true",
+                    help="time only the tensor-core decode batch of --batch tokens (profiling runs)")
+    ap.add_argument("--batch", type=int, default=32)
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
