@@ -106,6 +106,10 @@ struct GemmProblem {
     int act;                 // index of the activation tensor map
     int tiles_n;
     int tile_begin;          // first global tile index of this problem
+    int tiles_per_split;     // tiles_n * tiles_m
+    int ksplit;              // 1, or 2: each output tile is two half-K tiles whose fp32
+                             // partials are added into Y (zeroed by the host)
+    int kchunk;              // stages of one split
 };
 
 struct GemmParams {
@@ -336,16 +340,28 @@ q4_act_kernel(const float* __restrict__ X, int64_t K, int64_t Kp, int64_t groups
 // The persistent tcgen05 GEMM.
 // ---------------------------------------------------------------------------------
 struct TileRef {
-    int prob, mt, nt;
+    int prob, mt, nt, ks;
 };
 
 __device__ __forceinline__ TileRef tile_ref(const GemmParams& p, int tile) {
     TileRef t;
     t.prob = find_problem(p, tile);
-    const int local = tile - p.prob[t.prob].tile_begin;
+    const GemmProblem& pr = p.prob[t.prob];
+    int local = tile - pr.tile_begin;
+    t.ks = 0;
+    if (local >= pr.tiles_per_split) {   // the second half-K tile of a split problem
+        t.ks = 1;
+        local -= pr.tiles_per_split;
+    }
     t.mt = local % p.tiles_m;
     t.nt = local / p.tiles_m;
     return t;
+}
+
+// the stages [kb, ke) of split ks of a problem
+__device__ __forceinline__ void k_range(const GemmProblem& pr, int ks, int& kb, int& ke) {
+    kb = ks * pr.kchunk;
+    ke = min(pr.K / kBK, kb + pr.kchunk);
 }
 
 // norm (as fp32) of row `o` for K-chunk `kc`, 0 for rows past N
@@ -493,7 +509,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 const TileRef tr = tile_ref(p, tile);
                 const GemmProblem& pr = p.prob[tr.prob];
                 const CUtensorMap* xmap = &p.tmap[pr.act];
-                for (int kc = 0; kc < pr.K / kBK; ++kc) {
+                int kb, ke;
+                k_range(pr, tr.ks, kb, ke);
+                for (int kc = kb; kc < ke; ++kc) {
                     if constexpr (C::FMT == kFmtQ40) {
                         if ((kc & 3) == 0) {   // the slab of this stage and the next three
                             const int qs = pg % C::SLABS;
@@ -532,14 +550,16 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
-                const GemmProblem& pr = p.prob[find_problem(p, tile)];
+                const TileRef tr = tile_ref(p, tile);
+                const GemmProblem& pr = p.prob[tr.prob];
                 const int buf = it & 1;
                 const uint32_t aph = (uint32_t)((it >> 1) & 1);
                 if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, p)) break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(kDCol0 + buf * kBT);
-                const int nk = pr.K / kBK;
-                for (int kc = 0; kc < nk; ++kc) {
+                int kb, ke;
+                k_range(pr, tr.ks, kb, ke);
+                for (int kc = kb; kc < ke; ++kc) {
                     // the dequant warps arrive on full_b only after waiting on the TMA
                     // barrier of the same stage, so it also orders the TMA writes
                     if (!mbar_wait(&full_b[s], ph, abort_flag, p)) { ok = false; break; }
@@ -551,7 +571,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                         // A: 8 TMEM columns (16 bf16) per K step; B: +32 bytes along K
                         // inside the swizzle atom = +2 in the 16-byte-unit address field
                         umma_bf16_tmem_a(d, a0 + (uint32_t)(8 * kk), bdesc0 + 2u * kk, idesc,
-                                         (kc > 0 || kk > 0) ? 1u : 0u);
+                                         (kc > kb || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);
                     if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -590,8 +610,12 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 for (int j = 0; j < 16; ++j) {
                     const int t = tb + j;
                     if (t < p.M) {
-                        if constexpr (C::F16) ycolf[(int64_t)t * pr.N] = __uint_as_float(r[j]);
-                        else ycol[(int64_t)t * pr.N] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                        if constexpr (C::F16) {
+                            if (pr.ksplit > 1) atomicAdd(ycolf + (int64_t)t * pr.N, __uint_as_float(r[j]));
+                            else ycolf[(int64_t)t * pr.N] = __uint_as_float(r[j]);
+                        } else {
+                            ycol[(int64_t)t * pr.N] = __float2bfloat16_rn(__uint_as_float(r[j]));
+                        }
                     }
                 }
             };
@@ -622,8 +646,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
             const TileRef tr = tile_ref(p, tile);
             const GemmProblem& pr = p.prob[tr.prob];
-            const int nk = pr.K / kBK;
-            for (int kc = 0; kc < nk; ++kc, ++gi) {
+            int kb, ke;
+            k_range(pr, tr.ks, kb, ke);
+            for (int kc = kb; kc < ke; ++kc, ++gi) {
                 if (gi % kDequantGroups != grp) continue;   // the other group's stage
                 const int s = gi % kStages;
                 const uint32_t ph = (uint32_t)((gi / kStages) & 1);
@@ -843,6 +868,27 @@ cq_status make_act_map(CUtensorMap* map, const void* base, int64_t M, int64_t K,
     return CQ_OK;
 }
 
+// K split of one problem.  The 32-token configurations reach one weight tile per ~120
+// cycles of MMA issue per SM, so every SM should hold tiles: when the output tiles alone
+// number under 1.5 per SM, each is cut into two half-K tiles (a multiple of `align`
+// stages) whose fp32 partials the epilogue adds into Y.  Two addends on a zeroed Y give
+// the same sum in either order, so results stay bit-reproducible.
+template <class C>
+void choose_split(GemmProblem& gp, int tiles_m, int align) {
+    const int nk = gp.K / kBK;
+    gp.tiles_per_split = gp.tiles_n * tiles_m;
+    gp.ksplit = 1;
+    gp.kchunk = nk;
+    if (C::F16 && C::BT == 32 && 2 * gp.tiles_per_split <= 3 * sm_count() && nk >= 2 * align) {
+        int chunk = (nk + 1) / 2;
+        chunk = (chunk + align - 1) / align * align;
+        if (chunk < nk) {
+            gp.ksplit = 2;
+            gp.kchunk = chunk;
+        }
+    }
+}
+
 void fill_levels(float (&lv)[16], int b, const cq_codebook* cbk) {
     for (int t = 0; t < 16; ++t) lv[t] = 0.0f;
     const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
@@ -978,7 +1024,12 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
             if (st != CQ_OK) return st;
             gp.tiles_n = (int)((q.N + kBO - 1) / kBO);
             gp.tile_begin = tiles;
-            tiles += gp.tiles_n * tiles_m;
+            choose_split<C>(gp, tiles_m, 1);
+            if (gp.ksplit > 1) {
+                const cudaError_t e = cudaMemsetAsync(q.Y, 0, (size_t)M * (size_t)q.N * sizeof(float), cs);
+                if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+            }
+            tiles += gp.tiles_per_split * gp.ksplit;
             ++i0;
         }
         prm.nprob = np;
@@ -1094,10 +1145,15 @@ cq_status run_q40(const uint8_t* blocks, int64_t N, int64_t K, const float* X, i
     const int tiles_m = (int)((M + C::BT - 1) / C::BT);
     gp.tiles_n = (int)((N + kBO - 1) / kBO);
     gp.tile_begin = 0;
+    choose_split<C>(gp, tiles_m, 4);   // Q4_0 splits on whole 256-column slabs
+    if (gp.ksplit > 1) {
+        const cudaError_t e = cudaMemsetAsync(Y, 0, (size_t)M * (size_t)N * sizeof(float), cs);
+        if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
+    }
     prm.nprob = 1;
     prm.M = (int)M;
     prm.tiles_m = tiles_m;
-    prm.total_tiles = gp.tiles_n * tiles_m;
+    prm.total_tiles = gp.tiles_per_split * gp.ksplit;
     prm.err = err;
     prm.timeout_ns = 2000000000ull;   // 2 s per wait
     const int grid = prm.total_tiles < sm_count() ? prm.total_tiles : sm_count();

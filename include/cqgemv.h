@@ -117,7 +117,9 @@ cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* Xq, float* s
  *     tiles.  The weights are decoded once for all tokens; the operands are fp16
  *     (cb * norm, and xr * s_t / 128 in `workspace`), the accumulation fp32.  The
  *     relative error stays within 1e-3 of the exact product; activations must satisfy
- *     max |X[t][k]| <= 65504 (fp16 range).
+ *     max |X[t][k]| <= 65504 (fp16 range).  When the row tiles are too few to occupy the
+ *     GPU, K is split in two: Y is zeroed on `stream` and both halves add their fp32
+ *     partials into it (two addends on zero: the same sum in either order).
  *   packed, norms  as written by cq_encode
  *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
  *   Y  [B][N] float32
@@ -215,7 +217,8 @@ cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X,
  * with the products summed in float32 (tcgen05 MMA, fp32 accumulation in tensor memory).
  * `X` is converted once per call into `workspace` as fp16 [M][32 ceil(K/32)], zero past K;
  * each weight block is then read and decoded once per tile of up to 192 tokens (32 when
- * M <= 32).  The relative error stays within 1e-3 of the exact product; X must satisfy
+ * M <= 32; with few row tiles such calls split K in two and add both fp32 partials into Y,
+ * zeroed first on `stream`).  The relative error stays within 1e-3 of the exact product; X must satisfy
  * max |X[t][k]| <= 65504 and the scales max |d| <= 8188 (fp16 range).
  *   blocks [N][ceil(K/32) * 18] uint8 (as written by q4_0_quantize), X [M][K] float32,
  *   Y [M][N] float32; all 16-byte aligned.

@@ -96,6 +96,18 @@ def test_cq_gemv_batched_tensor_path(N, K, B):
     assert max_rel_err(Y, ref) < TOL
 
 
+def test_cq_gemv_batched_tensor_path_deterministic():
+    """The tensor-core batch with a two-way K split (few row tiles) reruns bit-identically."""
+    cb = fitted_cb28()
+    W = synth.weights(512, 4096, seed=41)
+    X = synth.activations(8, 4096, seed=42)
+    packed, norms = cq.cq_encode(to_dev(W), 4, cb)
+    q, s = cq.a8_quantize(to_dev(X))
+    a = to_host(cq.cq_gemv(packed, norms, 512, 4096, 4, cb, q, s))
+    b = to_host(cq.cq_gemv(packed, norms, 512, 4096, 4, cb, q, s))
+    assert np.array_equal(a, b)
+
+
 def test_cq_gemv_batch_consistency():
     """Each token of a batched call equals the same token alone (up to fp32 rounding)."""
     cb = fitted_cb28()

@@ -74,8 +74,10 @@ def test_q4_0_gemm_matches_gemv_per_token():
     assert max_rel_err(Yg, Yv) < TOL
 
 
-def test_q4_0_gemm_deterministic():
-    N, K, M = 384, 1024, 40
+@pytest.mark.parametrize("N,K,M", [(384, 1024, 40), (256, 2048, 8)])
+def test_q4_0_gemm_deterministic(N, K, M):
+    """Bit-identical reruns, including the two-way K split of small-token calls (two
+    partials added onto a zeroed output in either order give the same sum)."""
     W = synth.weights(N, K, seed=31)
     X = to_dev(synth.activations(M, K, seed=32))
     blocks = cq.q4_0_quantize(to_dev(W))
