@@ -27,6 +27,34 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start while the
+// previous kernel of the stream is still finishing; it calls pdl_wait() before its first
+// global-memory access (which then sees everything the previous kernel wrote) and
+// pdl_trigger() once all its blocks are resident, so the next launch can begin early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+template <typename... Params, typename... Args>
+cq_status launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+    if (e != cudaSuccess) {
+        set_last_cuda_error((int)e);
+        return CQ_ERR_CUDA;
+    }
+    return check_launch();
+}
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

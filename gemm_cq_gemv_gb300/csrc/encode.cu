@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(kA8Threads)
 a8_quantize_kernel(const float* __restrict__ X, int64_t K, int8_t* __restrict__ Xq,
                    float* __restrict__ scale) {
     __shared__ float red[kA8Threads / 32];
+    pdl_trigger();
+    pdl_wait();
     const int64_t t = blockIdx.x;
     const float* x = X + t * K;
     int8_t* xq = Xq + t * K;
@@ -296,8 +298,8 @@ extern "C" cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* X
                                  float* scale, void* stream) {
     if (!X || !Xq || !scale || B < 1 || K < 1 || B > 2147483647LL) return CQ_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(Xq) || !aligned16(scale)) return CQ_ERR_ALIGNMENT;
-    a8_quantize_kernel<<<(unsigned)B, kA8Threads, 0, as_stream(stream)>>>(X, K, Xq, scale);
-    return check_launch();
+    return launch_pdl(a8_quantize_kernel, dim3((unsigned)B), dim3(kA8Threads), 0, as_stream(stream), X, K, Xq,
+                      scale);
 }
 
 extern "C" cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks,

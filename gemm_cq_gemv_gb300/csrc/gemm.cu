@@ -261,6 +261,8 @@ struct RotParams {
 template <bool F16>
 __global__ void __launch_bounds__(256)
 rotate_act_kernel16(const __grid_constant__ RotParams rp) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * 256) >> 5;
@@ -309,6 +311,8 @@ rotate_act_kernel16(const __grid_constant__ RotParams rp) {
 __global__ void __launch_bounds__(256)
 q4_act_kernel(const float* __restrict__ X, int64_t K, int64_t Kp, int64_t groups,
               uint16_t* __restrict__ Xh) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t gpt = Kp / 8;   // groups of eight per token
     for (int64_t gg = (int64_t)blockIdx.x * 256 + threadIdx.x; gg < groups;
          gg += (int64_t)gridDim.x * 256) {
@@ -449,6 +453,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
     if (!layout_ok) {   // the launch's shared memory cannot hold the plan (host sizing error)
         if (tid == 0) atomicOr(p.err, 4u);
         return;
@@ -497,6 +502,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the table, the barriers and the tensor memory are set up while the previous kernel
+    // of the stream finishes; global memory is touched only after it has
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
@@ -954,10 +962,10 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
         int64_t grid = (rp.groups + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
         if (grid > cap) grid = cap;
-        rotate_act_kernel16<C::F16><<<(unsigned)grid, 256, 0, cs>>>(rp);
+        const cq_status r = launch_pdl(rotate_act_kernel16<C::F16>, dim3((unsigned)grid), dim3(256), 0, cs, rp);
         rp.njobs = 0;
         rp.groups = 0;
-        return check_launch();
+        return r;
     };
     for (int i = 0; i < count; ++i) {
         int a = -1;
@@ -1041,8 +1049,7 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
         prm.timeout_ns = 2000000000ull;   // 2 s per wait
         const size_t smem = (size_t)kGemmSmem;
         const int grid = tiles < sm_count() ? tiles : sm_count();
-        cq_gemm_kernel<C><<<grid, kThreadsGemm, smem, cs>>>(prm);
-        st = check_launch();
+        st = launch_pdl(cq_gemm_kernel<C>, dim3(grid), dim3(kThreadsGemm), smem, cs, prm);
         if (st != CQ_OK) return st;
     }
     return CQ_OK;
@@ -1125,8 +1132,7 @@ cq_status run_q40(const uint8_t* blocks, int64_t N, int64_t K, const float* X, i
         int64_t grid = (groups + 255) / 256;
         const int64_t cap = (int64_t)sm_count() * 8;
         if (grid > cap) grid = cap;
-        q4_act_kernel<<<(unsigned)grid, 256, 0, cs>>>(X, K, Kp, groups, xh);
-        st = check_launch();
+        st = launch_pdl(q4_act_kernel, dim3((unsigned)grid), dim3(256), 0, cs, X, K, Kp, groups, xh);
         if (st != CQ_OK) return st;
     }
     static GemmParams prm;   // large; built on the host, passed by value to the launch
@@ -1157,8 +1163,7 @@ cq_status run_q40(const uint8_t* blocks, int64_t N, int64_t K, const float* X, i
     prm.err = err;
     prm.timeout_ns = 2000000000ull;   // 2 s per wait
     const int grid = prm.total_tiles < sm_count() ? prm.total_tiles : sm_count();
-    cq_gemm_kernel<C><<<grid, kThreadsGemm, (size_t)kGemmSmem, cs>>>(prm);
-    return check_launch();
+    return launch_pdl(cq_gemm_kernel<C>, dim3(grid), dim3(kThreadsGemm), (size_t)kGemmSmem, cs, prm);
 }
 
 }  // namespace

@@ -31,6 +31,8 @@ constexpr int kSeg = 1024;      // positions per segment (32 lanes x 32)
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads)
 rotate_act_kernel(const int8_t* __restrict__ Xq, int64_t groups, float* __restrict__ xr) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
     constexpr int E = 1 << (2 * BITS);
     extern __shared__ __align__(128) unsigned char smem_c[];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    pdl_trigger();
     const uint32_t sbase = smem_u32(smem_c), send = sbase + p.smem_bytes;
     uint32_t tbase;
     SmemCarve cv;
@@ -461,13 +464,14 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
             nx_base += (int64_t)gridDim.x * tile_rows;
         }
     };
-    // the first units are in flight while the table and the activations are set up
-    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
-
+    // the table is built while the previous kernel of the stream finishes; then the
+    // first units go in flight while the activations are set up
     for (int i = tid; i < E * 32; i += kWarps2 * 32) {
         const int e = i >> 5;
         lut2[i] = make_float2(slv[e & (L - 1)], slv[e >> BITS]);
     }
+    pdl_wait();
+    for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
     float2 xx[SPW][TB][16];
 #pragma unroll
     for (int i = 0; i < SPW; ++i) {
@@ -715,6 +719,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
     uint64_t* rbar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kRing * kSlotB);  // [16][kRing]
     const Reduce rd = carve_reduce(rbar + kWarps2 * kRing, TB);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    pdl_trigger();
     if (tid == 0) prefetch_tensormap(&p.bmap);
     if (lane < kRing) mbar_init(&rbar[w * kRing + lane], 1);   // each warp its own ring barriers
     if (tid < kSlots) {
@@ -752,6 +757,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
         }
     };
     // the first units are in flight while the activations are loaded
+    pdl_wait();
     for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
     float2 xx[SPW][TB][16];
     float cblk[SPW][TB];
@@ -807,7 +813,9 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_rows_kernel(const Q
     uint8_t* stage = smem_q;                                              // [16][8][608]
     const Reduce rd = carve_reduce(smem_q + kWarps2 * kRows * kStage, TB);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    pdl_trigger();
     if (tid == 0) init_reduce(rd);
+    pdl_wait();
     const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
     const int slot = w % nsl, rgi = w / nsl;
     const bool busy = rgi < p.rg;
@@ -972,8 +980,7 @@ cq_status run_cq_gemv(CqGemvParams p, cudaStream_t st) {
     int grid = 0;
     const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
     if (s != CQ_OK) return s;
-    kern<<<grid, kWarps2 * 32, smem, st>>>(p);
-    return check_launch();
+    return launch_pdl(kern, dim3(grid), dim3(kWarps2 * 32), smem, st, p);
 }
 
 template <int TB, int SPW, bool RING>
@@ -986,8 +993,7 @@ cq_status run_q4_0_gemv(Q40GemvParams p, cudaStream_t st) {
     int grid = 0;
     const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
     if (s != CQ_OK) return s;
-    kern<<<grid, kWarps2 * 32, smem, st>>>(p);
-    return check_launch();
+    return launch_pdl(kern, dim3(grid), dim3(kWarps2 * 32), smem, st, p);
 }
 
 template <int BITS>
@@ -1047,8 +1053,8 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         int64_t grid = (groups + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
         if (grid > cap) grid = cap;
-        rotate_act_kernel<<<(unsigned)grid, kThreads, 0, st>>>(Xq, groups, xr);
-        const cq_status s = check_launch();
+        const cq_status s = launch_pdl(rotate_act_kernel, dim3((unsigned)grid), dim3(kThreads), 0, st, Xq,
+                                       groups, xr);
         if (s != CQ_OK) return s;
     }
     CqGemvParams p;
