@@ -6,7 +6,8 @@ GEMV (``q4_0_gemv``) on the four matrices [8192, 8192], [28672, 8192], [8192, 28
 the lm_head [128256, 4096]
 (1.15 GB of packed weights per step, far larger than L2, so no flush is needed).
 Weights are encoded once before timing (offline, as the format intends); the timed
-region holds only the decode work (one event pair around the K steps; the per-kernel
+region holds only the decode work (K replays of the step captured as a CUDA graph, one
+event pair around them; the per-kernel
 times behind ``roofline`` come from a second pass of the same steps with events around
 each launch).  ``value`` is algorithmic GB/s: packed indices +
 norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step time.
@@ -235,18 +236,27 @@ def build_prefill(dev, cb, torch, cq, synth, M):
 
 
 def time_prefill(pf, cb, cq, torch, steps, warmup):
-    """Device time of the grouped prefill GEMM (rotation + tcgen05 GEMM), CUDA events."""
+    """Device time of the grouped prefill GEMM (rotation + tcgen05 GEMM): the call captured
+    as a CUDA graph, `steps` replays between CUDA events."""
     f = lambda: cq.cq_gemm_grouped(pf["probs"], pf["M"], 4, cb, workspace=pf["ws"])
     for _ in range(warmup):
         f()
     torch.cuda.synchronize()
     cq.cq_device_error()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        f()
+    torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        f()
-    e1.record()
+    with torch.cuda.stream(cap):
+        graph.replay()   # one untimed replay
+        e0.record(cap)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(cap)
     torch.cuda.synchronize()
     cq.cq_device_error()
     return e0.elapsed_time(e1) / steps
@@ -367,6 +377,14 @@ def gpu_arm(args, rank, world, local_rank):
     for _ in range(args.warmup):
         run_step(mats, cb, cq, kinds=kinds)
     torch.cuda.synchronize()
+    # one decode step captured as a CUDA graph (same launches, same buffers); the timed
+    # region replays it K times
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        run_step(mats, cb, cq, kinds=kinds)
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
@@ -377,11 +395,13 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(args.steps):
-        run_step(mats, cb, cq, kinds=kinds)
-    t1.record()
+    with torch.cuda.stream(cap):
+        t0.record(cap)
+        for _ in range(args.steps):
+            graph.replay()
+        t1.record(cap)
     torch.cuda.synchronize()
+    cq.cq_device_error()
     if dist:
         dist.barrier()
     ms = reduce_max(t0.elapsed_time(t1) / args.steps, dist, dev)
