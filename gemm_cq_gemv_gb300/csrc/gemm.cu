@@ -59,6 +59,7 @@ constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A s
 constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + stages + barriers
 constexpr int kBarBytes = 512;           // barrier block: barriers, TMEM slot, flags, levels
 constexpr int kMaxProblems = 120;
+constexpr int kMaxCtaTiles = 256;        // tiles per CTA whose lookup is precomputed in shared memory
 constexpr int kMaxActs = 8;
 
 // Q4_0 weights reach shared memory in slabs of 256 k (8 blocks, 144 bytes per row: the
@@ -76,13 +77,16 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //   STAGES  depth of the shared-memory ring (= tensor-memory A stages)
 //   FMT     weight format: CQ (packed indices + norms) or Q4_0 blocks
 //   SLABS   Q4_0: depth of the weight-slab ring
-template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0>
+//   TLIST   look the CTA's tiles up once, into shared memory (grouped launches of many
+//           problems, where each lookup is a binary search over the parameter block)
+template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
     static constexpr int STAGES = STAGES_;
     static constexpr int FMT = FMT_;
     static constexpr int SLABS = SLABS_;
+    static constexpr bool TLIST = TLIST_;
     static constexpr int XTILE = BT * kBK * 2;        // activation tile bytes
     static constexpr int STAGE = XTILE + (FMT == kFmtCQ ? kPTileBytes : 0);
     static constexpr int DCOL0 = STAGES * kACols;     // accumulators after the A stages
@@ -91,7 +95,7 @@ struct GemmCfg {
     static_assert((3 * STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
     static_assert(FMT == kFmtCQ || (F16 && SLABS >= 2), "Q4_0 runs with fp16 operands on a slab ring");
 };
-using PrefillCfg = GemmCfg<192, false, 4>;               // 24 KB activation tile, 28 KB stages
+using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true>;   // 24 KB activation tile, 28 KB stages
 using DecodeCfg = GemmCfg<32, true, 8>;                  // 4 KB activation tile, 8 KB stages
 using Q40WideCfg = GemmCfg<192, true, 4, kFmtQ40, 4>;    // Q4_0, many tokens: 96 + 72 KB
 using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4>;   // Q4_0, up to 32 tokens: 32 + 72 KB
@@ -441,7 +445,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     };
     float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [256][32] (CQ)
     uint64_t* bars = reinterpret_cast<uint64_t*>(gen(bars_at));
-    const bool layout_ok = bars_at + (uint32_t)kBarBytes <= send;
+    // this CTA's tile list (problem, row tile, token tile, K half), after the barriers
+    const uint32_t tiles_at = bars_at + (uint32_t)kBarBytes;
+    const bool layout_ok = tiles_at + (C::TLIST ? (uint32_t)(kMaxCtaTiles * sizeof(TileRef)) : 0u) <= send;
     uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
     uint64_t* full_b = bars + kStages;            // dequant: A stage written to TMEM
     uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
@@ -498,6 +504,19 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // Each role walks the tiles blockIdx.x, + gridDim.x, ...; their problem lookups (a
+    // binary search over the parameter block) are done here once, by all threads, so a
+    // tile boundary costs one shared-memory load instead of a chain of dependent loads.
+    TileRef* tlist = reinterpret_cast<TileRef*>(gen(tiles_at));
+    if constexpr (C::TLIST) {
+        const int ncta = (int)blockIdx.x < p.total_tiles ? (p.total_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const int nl = ncta < kMaxCtaTiles ? ncta : kMaxCtaTiles;
+        for (int i = tid; i < nl; i += kThreadsGemm) tlist[i] = tile_ref(p, (int)blockIdx.x + i * (int)gridDim.x);
+    }
+    auto tile_at = [&](int i, int tile) {
+        if constexpr (C::TLIST) return i < kMaxCtaTiles ? tlist[i] : tile_ref(p, tile);
+        else return tile_ref(p, tile);
+    };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -513,8 +532,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             uint32_t ph = 0;
             bool ok = true;
             int pg = 0;   // Q4_0: slabs issued
-            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-                const TileRef tr = tile_ref(p, tile);
+            int ti = 0;
+            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++ti) {
+                const TileRef tr = tile_at(ti, tile);
                 const GemmProblem& pr = p.prob[tr.prob];
                 const CUtensorMap* xmap = &p.tmap[pr.act];
                 int kb, ke;
@@ -558,7 +578,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
-                const TileRef tr = tile_ref(p, tile);
+                const TileRef tr = tile_at(it, tile);
                 const GemmProblem& pr = p.prob[tr.prob];
                 const int buf = it & 1;
                 const uint32_t aph = (uint32_t)((it >> 1) & 1);
@@ -597,7 +617,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         const int th = (warp - kEpiWarp0) >> 2;
         int it = 0;
         for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
-            const TileRef tr = tile_ref(p, tile);
+            const TileRef tr = tile_at(it, tile);
             const GemmProblem& pr = p.prob[tr.prob];
             const int buf = it & 1;
             if (!mbar_wait(&acc_full[buf], (uint32_t)((it >> 1) & 1), abort_flag, p)) break;
@@ -651,8 +671,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         const uint32_t lb = tbase | ((uint32_t)lane << 3);
         bool ok = true;
         int gi = 0;   // global stage index
-        for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-            const TileRef tr = tile_ref(p, tile);
+        int ti = 0;
+        for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++ti) {
+            const TileRef tr = tile_at(ti, tile);
             const GemmProblem& pr = p.prob[tr.prob];
             int kb, ke;
             k_range(pr, tr.ks, kb, ke);
