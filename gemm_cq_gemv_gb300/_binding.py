@@ -67,6 +67,7 @@ SIGNATURES = {
     "cq_gemm_grouped": (_INT, [ctypes.POINTER(cq_gemm_problem), _INT, _I64, _INT, _INT,
                                ctypes.POINTER(cq_codebook), _P, _SZ, _P]),
     "cq_device_error": (_INT, [_P]),
+    "cq_probe_bounded_wait": (_INT, [ctypes.c_uint64, _P]),
     "q4_0_quantize": (_INT, [_P, _I64, _I64, _P, _P]),
     "q4_0_gemv": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "q4_0_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
@@ -258,6 +259,11 @@ def cq_gemm_grouped(problems, M, b, cb, workspace=None, g=128, stream=None, devi
 def cq_device_error(stream=None):
     """Raise CQError(CQ_ERR_DEVICE_TIMEOUT) if a bounded device wait gave up (clears it)."""
     _check("cq_device_error", lib().cq_device_error(_stream(stream)))
+
+
+def cq_probe_bounded_wait(timeout_ns=20_000_000, stream=None):
+    """Enqueue the failure-detection probe (bounded waits that nothing completes)."""
+    _check("cq_probe_bounded_wait", lib().cq_probe_bounded_wait(int(timeout_ns), _stream(stream)))
 
 
 NOALLOC_MAX_ELEMS = 1 << 20   # CQ_GEMV_NOALLOC_MAX_ELEMS

@@ -64,3 +64,11 @@ extern "C" cq_status cq_device_error(void* stream) {
     }
     return raised ? CQ_ERR_DEVICE_TIMEOUT : CQ_OK;
 }
+
+extern "C" cq_status cq_probe_bounded_wait(uint64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000u || timeout_ns > 10000000000ull) return CQ_ERR_INVALID_ARG;
+    cudaStream_t cs = cq::as_stream(stream);
+    const cq_status s = cq::probe_gemm_wait(timeout_ns, cs);
+    if (s != CQ_OK) return s;
+    return cq::probe_gemv_wait(timeout_ns, cs);
+}

@@ -64,6 +64,12 @@ int sm_count();
 unsigned int* gemm_error_word(int dev);
 unsigned int* gemv_error_word(int dev);
 
+// Failure-detection probes (one per unit): a one-thread kernel whose bounded wait on a
+// barrier phase that nothing completes gives up after `timeout_ns` and raises the unit's
+// error word.
+cq_status probe_gemm_wait(unsigned long long timeout_ns, cudaStream_t st);
+cq_status probe_gemv_wait(unsigned long long timeout_ns, cudaStream_t st);
+
 // float64 -> IEEE binary16 bits, one round-to-nearest-even step (ties to even),
 // written from the binary16 definition: 1 sign bit, 5 exponent bits (bias 15),
 // 10 fraction bits, subnormals with unit 2^-24, overflow to infinity.

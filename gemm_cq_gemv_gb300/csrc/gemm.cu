@@ -164,21 +164,25 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
 }
 
 // Bounded wait: false when the deadline passed or another thread already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                          const GemmParams& p) {
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                                unsigned int* err, unsigned long long timeout_ns) {
     if (mbar_try(b, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try(b, parity)) return true;
         if ((i & 255u) == 0u) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > p.timeout_ns) {
+            if (global_ns() - t0 > timeout_ns) {
                 *abort_flag = 1;
-                atomicOr(p.err, 1u);
+                atomicOr(err, 1u);
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          const GemmParams& p) {
+    return mbar_wait_until(b, parity, abort_flag, p.err, p.timeout_ns);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -925,6 +929,29 @@ void fill_levels(float (&lv)[16], int b, const cq_codebook* cbk) {
 }
 
 }  // namespace
+
+// Failure-detection probe for the pipeline's wait: one thread waits on a barrier phase that
+// nothing completes; after p.timeout_ns the wait raises the abort flag and the error word
+// and returns (the path every role of cq_gemm_kernel takes when a wait runs out).
+__global__ void bounded_wait_probe_gemm_kernel(unsigned int* err, unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)mbar_wait_until(&bar, 0u, &abort_flag, err, timeout_ns);
+}
+
+cq_status probe_gemm_wait(unsigned long long timeout_ns, cudaStream_t st) {
+    unsigned int* err = nullptr;
+    const cq_status se = host_setup(&err);
+    if (se != CQ_OK) return se;
+    bounded_wait_probe_gemm_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+    return check_launch();
+}
 
 unsigned int* gemm_error_word(int dev) {
     if (dev < 0 || dev >= 64) return nullptr;

@@ -128,14 +128,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Bounded wait (2 s): on expiry raise the device error flag and give up (the result of
-// the call is then undefined and cq_device_error() reports the timeout).
-__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err) {
+// Bounded wait (2 s by default): on expiry raise the device error flag and give up (the
+// result of the call is then undefined and cq_device_error() reports the timeout).
+__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err,
+                                          unsigned long long timeout_ns = 2000000000ull) {
     if (mbar_try(b, parity)) return;
     const unsigned long long t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try(b, parity)) return;
-        if ((i & 255u) == 0u && global_ns() - t0 > 2000000000ull) {
+        if ((i & 255u) == 0u && global_ns() - t0 > timeout_ns) {
             atomicOr(err, 2u);
             return;
         }
@@ -917,6 +918,18 @@ cq_status device_error_word(unsigned int** out) {
     return CQ_OK;
 }
 
+// Failure-detection probe: one thread waits, with this unit's bounded wait, on a barrier
+// phase that nothing completes.  The wait gives up after `timeout_ns`, raises the error
+// word and the kernel returns; nothing faults or hangs.
+__global__ void bounded_wait_probe_kernel(unsigned int* err, unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_wait(&bar, 0u, err, timeout_ns);
+    }
+}
+
 // cuTensorMapEncodeTiled from the driver (cached; no link against libcuda)
 std::mutex g_enc_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
@@ -948,14 +961,18 @@ cq_status encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
     return CQ_OK;
 }
 
+// `attr`: one flag per device (the shared-memory attribute is set per device context)
 template <typename Kern>
-cq_status launch_once(Kern kern, size_t smem, int64_t ntiles, cudaStream_t st, bool* attr,
+cq_status launch_once(Kern kern, size_t smem, int64_t ntiles, cudaStream_t st, bool (&attr)[64],
                       int* grid_out) {
-    if (!*attr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch();
+    if (dev < 0 || dev >= 64) return CQ_ERR_UNSUPPORTED;
+    if (!attr[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) !=
             cudaSuccess)
             return check_launch();
-        *attr = true;
+        attr[dev] = true;
     }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps2 * 32, smem) != cudaSuccess)
@@ -972,26 +989,26 @@ inline int row_groups(int nseg) { return nseg >= kWarps2 ? 1 : kWarps2 / nseg; }
 
 template <int BITS, int TB, int SPW>
 cq_status run_cq_gemv(CqGemvParams p, cudaStream_t st) {
-    static bool attr = false;
+    static bool attr[64] = {};
     auto kern = cq_gemv_kernel<BITS, TB, SPW>;
     const size_t smem = cq_smem_bytes<BITS>(TB);
     p.smem_bytes = (uint32_t)smem;
     const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int grid = 0;
-    const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
+    const cq_status s = launch_once(kern, smem, ntiles, st, attr, &grid);
     if (s != CQ_OK) return s;
     return launch_pdl(kern, dim3(grid), dim3(kWarps2 * 32), smem, st, p);
 }
 
 template <int TB, int SPW, bool RING>
 cq_status run_q4_0_gemv(Q40GemvParams p, cudaStream_t st) {
-    static bool attr = false;
+    static bool attr[64] = {};
     auto kern = RING ? q4_0_gemv_ring_kernel<TB, SPW> : q4_0_gemv_rows_kernel<TB, SPW>;
     const size_t smem = RING ? (size_t)kWarps2 * kRing * kUnitRows * kQSeg + kWarps2 * kRing * 8 + reduce_bytes(TB)
                              : (size_t)kWarps2 * kRows * kStage + reduce_bytes(TB);
     const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int grid = 0;
-    const cq_status s = launch_once(kern, smem, ntiles, st, &attr, &grid);
+    const cq_status s = launch_once(kern, smem, ntiles, st, attr, &grid);
     if (s != CQ_OK) return s;
     return launch_pdl(kern, dim3(grid), dim3(kWarps2 * 32), smem, st, p);
 }
@@ -1004,6 +1021,14 @@ cq_status dispatch_cq(CqGemvParams p, int tb, int spw, cudaStream_t st) {
 }
 
 }  // namespace
+
+cq_status probe_gemv_wait(unsigned long long timeout_ns, cudaStream_t st) {
+    unsigned int* err = nullptr;
+    const cq_status se = device_error_word(&err);
+    if (se != CQ_OK) return se;
+    bounded_wait_probe_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+    return check_launch();
+}
 
 unsigned int* gemv_error_word(int dev) {
     if (dev < 0 || dev >= 64) return nullptr;

@@ -171,6 +171,15 @@ cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, int64_t M, in
                           const cq_codebook* cbk, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Failure-detection probe: enqueues on `stream` one single-thread kernel per compute unit
+ * (GEMM pipeline, GEMV) whose bounded wait - the same device function the product kernels
+ * use - waits on a barrier phase that nothing completes.  Each wait gives up after about
+ * `timeout_ns` (1 us .. 10 s; the deadline is checked every 256 polls, each of which may
+ * sleep up to 1 ms), raises its unit's device error word and returns: no fault, no hang.
+ * A following cq_device_error() then reports CQ_ERR_DEVICE_TIMEOUT, and the context stays
+ * usable.  Errors: INVALID_ARG (timeout out of range), CUDA. */
+cq_status cq_probe_bounded_wait(uint64_t timeout_ns, void* stream);
+
 /* Reports (and clears) the device error flags raised by a bounded wait that timed out
  * (2 s) in a GEMM or GEMV launch on the current device: CQ_ERR_DEVICE_TIMEOUT if any
  * was raised, else CQ_OK.  Synchronises `stream`. */
