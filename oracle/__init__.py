@@ -18,8 +18,9 @@ Sources (cited by title and section; the pages are Chinese-language web articles
           rotation, nearest Lloyd-Max codeword, FP16 L2 norm, reconstruction
           ``w_group = (codebook_bits[idx] * norm) H``, 400k samples / 200 iterations,
           ``cb2[4] | cb3[8] | cb4[16]``, LSB-first nibble packing, low nibble = even
-          column, ``WEIGHT_BITS 4 / ACT_BITS 8``) and §三 (weights pre-transposed to
-          ``[out, in]``).
+          column, ``WEIGHT_BITS 4 / ACT_BITS 8``), §三 (weights pre-transposed to
+          ``[out, in]``) and §四 (int8 KV cache, per-head A8 query quantization and KV
+          fake-quant, one 4-byte scale per ``KV_GROUP = 32`` values).
 * [MMAP]  "免解析加载的秘诀：mmap 直读张量与 Needle 的秒级冷启动",
           section "mmap 之下张量按偏移直读" (groups of 128, the same reconstruction,
           the analytic 1-bit codebook ``{-sqrt(2/pi), +sqrt(2/pi)}``).
@@ -48,7 +49,7 @@ from .cq import (
     cq_encode,
     cq_reconstruct,
 )
-from .a8 import a8_quantize, a8_dequantize
+from .a8 import a8_quantize, a8_dequantize, a8_quantize_groups, a8_fake_quant_groups
 from .q4_0 import q4_0_quantize, q4_0_dequantize, q4_0_row_bytes, Q4_0_BLOCK, Q4_0_BLOCK_BYTES
 from .products import cq_gemv_ref, cq_gemm_ref, q4_0_gemv_ref
 
@@ -57,7 +58,7 @@ __all__ = [
     "lloyd_max_gaussian_fit", "gaussian_quantile_init", "ONE_BIT_LEVEL",
     "GROUP", "codebook_levels", "codebook_concat", "pack_indices", "unpack_indices",
     "cq_encode", "cq_reconstruct",
-    "a8_quantize", "a8_dequantize",
+    "a8_quantize", "a8_dequantize", "a8_quantize_groups", "a8_fake_quant_groups",
     "q4_0_quantize", "q4_0_dequantize", "q4_0_row_bytes", "Q4_0_BLOCK", "Q4_0_BLOCK_BYTES",
     "cq_gemv_ref", "cq_gemm_ref", "q4_0_gemv_ref",
 ]

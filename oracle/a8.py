@@ -25,3 +25,30 @@ def a8_quantize(X: np.ndarray):
 def a8_dequantize(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """``x_hat = s_t * q`` in float64."""
     return np.asarray(q, np.float64) * np.asarray(s, np.float64)[:, None]
+
+
+# ---------------------------------------------------------------------------------------
+# Grouped A8 for the attention side ([CACT] §四, KV cache budget: the key / value cache is
+# int8 (``kv_bits = 8``), the query gets per-head symmetric A8 quantization, keys and
+# values a per-head A8 fake-quant, and the per-layer budget stores one 4-byte scale per
+# ``KV_GROUP = 32`` cached values).  Reading: the same per-token symmetric rule as
+# ``a8_quantize``, applied to every group of G consecutive features of a row (a head, or
+# a KV_GROUP of 32 values); the fake-quant returns ``q * s`` (float32 product).
+# ---------------------------------------------------------------------------------------
+def a8_quantize_groups(X: np.ndarray, G: int):
+    """``X`` float32 ``[T, D]``, ``G | D`` -> (``q`` int8 ``[T, D]``, ``s`` float32 ``[T, D/G]``)."""
+    X = np.asarray(X, dtype=np.float32)
+    T, D = X.shape
+    if G < 1 or D % G:
+        raise ValueError("G must divide D")
+    q, s = a8_quantize(X.reshape(T * (D // G), G))
+    return q.reshape(T, D), s.reshape(T, D // G)
+
+
+def a8_fake_quant_groups(X: np.ndarray, G: int) -> np.ndarray:
+    """Quantize then dequantize every G-group: ``float32(q * s)``, float32 ``[T, D]``."""
+    X = np.asarray(X, dtype=np.float32)
+    T, D = X.shape
+    q, s = a8_quantize_groups(X, G)
+    s_full = np.repeat(s, G, axis=1)
+    return (q.astype(np.float32) * s_full).astype(np.float32)

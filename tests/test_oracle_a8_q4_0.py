@@ -1,4 +1,5 @@
-"""Pins for int8 activations ("ACT_BITS 8", Needle .cact page §一) and Q4_0
+"""Pins for int8 activations ("ACT_BITS 8", Needle .cact page §一; grouped for the query and
+the KV cache, §四) and Q4_0
 (Minueza -> KMCU v1 page §2 "Q4_0 量化", §3 "行对齐到 32")."""
 
 import json
@@ -8,6 +9,7 @@ import numpy as np
 import pytest
 
 from gemm_cq_gemv_gb300.synth import MINUEZA_LAYER, activations, weights
+import oracle
 from oracle import (Q4_0_BLOCK, Q4_0_BLOCK_BYTES, a8_quantize, q4_0_dequantize,
                     q4_0_quantize, q4_0_row_bytes)
 
@@ -87,3 +89,53 @@ def test_q4_0_padding_and_shapes():
     amax = np.abs(blocks.reshape(3, 10, 32)).max(axis=2)
     d = (amax / 8).repeat(32, axis=1)[:, :312]
     assert np.all(np.abs(back - W) <= d * (1 + 8 * 2.0 ** -11) + 1e-9)
+
+
+# ---- grouped A8 (attention side: per-head query quantization, KV fake-quant) -----------
+
+def test_a8_groups_worked_example():
+    """One group whose max is 127 (scale exactly 1): the codes are the rounded values,
+    half to even (-63.5 -> -64, 0.25 -> 0), and the fake-quant returns them; a zero group
+    gets scale 1 and zeros."""
+    X = np.array([[127.0, -63.5, 0.25, 1.0, 0.0, 0.0, 0.0, 0.0]], np.float32)
+    q, s = oracle.a8_quantize_groups(X, 4)
+    assert q.tolist() == [[127, -64, 0, 1, 0, 0, 0, 0]]
+    assert s.tolist() == [[1.0, 1.0]]
+    assert oracle.a8_fake_quant_groups(X, 4).tolist() == [[127.0, -64.0, 0.0, 1.0, 0.0, 0.0, 0.0, 0.0]]
+
+
+def test_a8_groups_reduce_to_per_token_when_one_group():
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((5, 96)).astype(np.float32)
+    q, s = oracle.a8_quantize_groups(X, 96)
+    q1, s1 = oracle.a8_quantize(X)
+    assert np.array_equal(q, q1) and np.array_equal(s[:, 0], s1)
+
+
+def test_a8_groups_are_independent_and_scale_exactly():
+    """Scaling one group by a power of two scales its scale by it and leaves every code
+    (and every other group) unchanged: a misplaced group index would break this."""
+    rng = np.random.default_rng(4)
+    X = rng.standard_normal((3, 128)).astype(np.float32)
+    q, s = oracle.a8_quantize_groups(X, 32)
+    Y = X.copy()
+    Y[1, 64:96] *= np.float32(8.0)
+    q2, s2 = oracle.a8_quantize_groups(Y, 32)
+    assert np.array_equal(q, q2)
+    expect = s.copy()
+    expect[1, 2] *= np.float32(8.0)
+    assert np.array_equal(s2, expect)
+
+
+def test_a8_fake_quant_error_bound_and_extremes():
+    """|fq(x) - x| <= s/2 (plus float32 rounding of the product), and each group's largest
+    magnitude maps to +-127."""
+    rng = np.random.default_rng(5)
+    X = (rng.standard_normal((16, 256)) * rng.uniform(0.01, 100.0, (16, 1))).astype(np.float32)
+    q, s = oracle.a8_quantize_groups(X, 32)
+    fq = oracle.a8_fake_quant_groups(X, 32)
+    s_full = np.repeat(s, 32, axis=1).astype(np.float64)
+    err = np.abs(fq.astype(np.float64) - X.astype(np.float64))
+    assert np.all(err <= 0.5 * s_full * (1 + 1e-6) + np.abs(X) * 2.0**-23)
+    qg = np.abs(q.astype(np.int32)).reshape(16, 8, 32)
+    assert np.all(qg.max(axis=2) == 127)
