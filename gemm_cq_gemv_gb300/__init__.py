@@ -13,11 +13,12 @@ from ._binding import (CQError, LIB_PATH, NOALLOC_MAX_ELEMS, SIGNATURES, a8_quan
                        cq_gemm, cq_gemm_grouped, cq_gemm_grouped_workspace_bytes,
                        cq_gemm_problem, cq_gemm_workspace_bytes, cq_device_error,
                        make_gemm_problems, q4_0_gemm, q4_0_gemm_workspace_bytes,
-                       cq_probe_bounded_wait)
+                       cq_probe_bounded_wait, a8_quantize_groups, a8_fake_quant_groups)
 
 __all__ = ["CQError", "LIB_PATH", "NOALLOC_MAX_ELEMS", "SIGNATURES", "a8_quantize", "cq_abi_version", "cq_codebook",
            "cq_codebook_fit", "cq_encode", "cq_gemv", "cq_gemv_noalloc", "cq_gemv_workspace_bytes",
            "cq_status_string", "lib", "make_codebook", "q4_0_gemv", "q4_0_quantize",
            "cq_gemm", "cq_gemm_grouped", "cq_gemm_grouped_workspace_bytes", "cq_gemm_problem",
            "cq_gemm_workspace_bytes", "cq_device_error", "make_gemm_problems", "q4_0_gemm",
-           "q4_0_gemm_workspace_bytes", "cq_probe_bounded_wait"]
+           "q4_0_gemm_workspace_bytes", "cq_probe_bounded_wait", "a8_quantize_groups",
+           "a8_fake_quant_groups"]

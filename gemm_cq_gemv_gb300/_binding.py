@@ -55,6 +55,8 @@ SIGNATURES = {
     "cq_codebook_fit": (_INT, [_P, _I64, _INT, _INT, _P, _P]),
     "cq_encode": (_INT, [_P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _P]),
     "a8_quantize": (_INT, [_P, _I64, _I64, _P, _P, _P]),
+    "a8_quantize_groups": (_INT, [_P, _I64, _I64, _INT, _P, _P, _P]),
+    "a8_fake_quant_groups": (_INT, [_P, _I64, _I64, _INT, _P, _P]),
     "cq_gemv_workspace_bytes": (_SZ, [_I64, _I64]),
     "cq_gemv": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _I64,
                        _P, _P, _SZ, _P]),
@@ -179,6 +181,30 @@ def a8_quantize(X, Xq=None, scale=None, stream=None):
     _check("a8_quantize", lib().a8_quantize(xp, B, K, _ptr(Xq, torch.int8, "Xq"),
                                             _ptr(scale, torch.float32, "scale"), _stream(stream)))
     return Xq, scale
+
+
+def a8_quantize_groups(X, G, codes=None, scales=None, stream=None):
+    """Grouped A8: X [T, D] float32 -> (codes int8 [T, D], scales float32 [T, D/G])."""
+    T, D = X.shape
+    if codes is None:
+        codes = torch.empty((T, D), dtype=torch.int8, device=X.device)
+    if scales is None:
+        scales = torch.empty((T, D // G), dtype=torch.float32, device=X.device)
+    _check("a8_quantize_groups", lib().a8_quantize_groups(_ptr(X, torch.float32, "X", 2), T, D, G,
+                                                          _ptr(codes, torch.int8, "codes"),
+                                                          _ptr(scales, torch.float32, "scales"),
+                                                          _stream(stream)))
+    return codes, scales
+
+
+def a8_fake_quant_groups(X, G, Y=None, stream=None):
+    """Grouped A8 fake-quant: Y [T, D] float32 = q * s per group of G features."""
+    T, D = X.shape
+    if Y is None:
+        Y = torch.empty((T, D), dtype=torch.float32, device=X.device)
+    _check("a8_fake_quant_groups", lib().a8_fake_quant_groups(_ptr(X, torch.float32, "X", 2), T, D, G,
+                                                              _ptr(Y, torch.float32, "Y"), _stream(stream)))
+    return Y
 
 
 def cq_gemv_workspace_bytes(B, K) -> int:

@@ -217,6 +217,50 @@ a8_quantize_kernel(const float* __restrict__ X, int64_t K, int8_t* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------------
+// Grouped A8 for the attention side (Needle .cact page, §四: int8 KV cache, per-head A8
+// quantization of the query, per-head A8 fake-quant of keys and values, one 4-byte scale
+// per 32 cached values).  Every group of G consecutive features of a row gets the
+// per-token rule of a8_quantize: s = float32(max |x|) / 127 (1 for an all-zero group),
+// q = clip(rint(x / s), -127, 127); the fake-quant writes float32(q * s).  One warp per
+// group, G / 32 values per lane.
+// ---------------------------------------------------------------------------------
+template <bool FAKE>
+__global__ void __launch_bounds__(256)
+a8_groups_kernel(const float* __restrict__ X, int64_t groups, int G, int8_t* __restrict__ codes,
+                 float* __restrict__ scales, float* __restrict__ Y) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * 256 + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * 256) >> 5;
+    const int per = G >> 5;   // values per lane (G is a multiple of 32, at most 256)
+    for (int64_t g = warp; g < groups; g += nwarps) {
+        const float* x = X + g * G;
+        float v[8];
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = (i < per) ? x[i * 32 + lane] : 0.0f;
+            am = fmaxf(am, fabsf(v[i]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, m));
+        const float s = (am > 0.0f) ? __fdiv_rn(am, 127.0f) : 1.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (i < per) {
+                const int8_t q = a8_code(v[i], s);
+                if constexpr (FAKE) Y[g * G + i * 32 + lane] = __fmul_rn((float)q, s);
+                else codes[g * G + i * 32 + lane] = q;
+            }
+        }
+        if constexpr (!FAKE) {
+            if (lane == 0) scales[g] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
 // A7: Q4_0 quantize.  One thread per 32-weight block of a zero-padded row.
 // ---------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
@@ -312,4 +356,40 @@ extern "C" cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t
     if (grid > 2147483647LL) return CQ_ERR_UNSUPPORTED;
     q4_0_quantize_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(W, N, K, nblk, blocks);
     return check_launch();
+}
+
+namespace {
+cq_status a8_groups_args(const float* X, int64_t T, int64_t D, int G) {
+    if (!X || T < 1 || D < 1 || G < 32 || G > 256 || G % 32 != 0 || D % G != 0) return CQ_ERR_INVALID_ARG;
+    if (T > ((int64_t)1 << 40) / D) return CQ_ERR_UNSUPPORTED;
+    return CQ_OK;
+}
+unsigned a8_groups_grid(int64_t groups) {
+    int64_t grid = (groups + 7) / 8;
+    const int64_t cap = (int64_t)sm_count() * 16;
+    if (grid > cap) grid = cap;
+    return (unsigned)(grid < 1 ? 1 : grid);
+}
+}  // namespace
+
+extern "C" cq_status a8_quantize_groups(const float* X, int64_t T, int64_t D, int G, int8_t* codes,
+                                        float* scales, void* stream) {
+    cq_status st = a8_groups_args(X, T, D, G);
+    if (st != CQ_OK) return st;
+    if (!codes || !scales) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(codes) || !aligned16(scales)) return CQ_ERR_ALIGNMENT;
+    const int64_t groups = T * (D / G);
+    return launch_pdl(a8_groups_kernel<false>, dim3(a8_groups_grid(groups)), dim3(256), 0, as_stream(stream), X,
+                      groups, G, codes, scales, (float*)nullptr);
+}
+
+extern "C" cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, float* Y,
+                                          void* stream) {
+    cq_status st = a8_groups_args(X, T, D, G);
+    if (st != CQ_OK) return st;
+    if (!Y) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Y)) return CQ_ERR_ALIGNMENT;
+    const int64_t groups = T * (D / G);
+    return launch_pdl(a8_groups_kernel<true>, dim3(a8_groups_grid(groups)), dim3(256), 0, as_stream(stream), X,
+                      groups, G, (int8_t*)nullptr, (float*)nullptr, Y);
 }

@@ -104,6 +104,21 @@ cq_status cq_encode(const float* W, int64_t N, int64_t K, int g, int b,
 cq_status a8_quantize(const float* X, int64_t B, int64_t K, int8_t* Xq, float* scale,
                       void* stream);
 
+/* ---- Grouped A8 for the attention side (Needle .cact page, §四: int8 KV cache, per-head A8
+ * quantization of the query, per-head A8 fake-quant of keys and values, one 4-byte scale
+ * per KV_GROUP = 32 cached values).  Every group of G consecutive features of a row of
+ * X [T][D] float32 gets a8_quantize's per-token rule:
+ *   s = float32(max |x|) / 127 (IEEE float32 division; 1 for an all-zero group),
+ *   q = clip(rint(x / s), -127, 127).
+ * a8_quantize_groups writes the codes [T][D] int8 and the scales [T][D/G] float32 (the
+ * cache layout); a8_fake_quant_groups writes Y [T][D] = float32(q * s).  G is a multiple of
+ * 32 up to 256 dividing D (a head of 32..256 features, or a KV group of 32).  Bit-exact with
+ * the oracle.  Pointers 16-byte aligned.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (T * D above 2^40), CUDA. */
+cq_status a8_quantize_groups(const float* X, int64_t T, int64_t D, int G, int8_t* codes,
+                             float* scales, void* stream);
+cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, float* Y, void* stream);
+
 /* ---- A4 + A5: decode GEMV (Needle .cact page, §三: each output row streams along
  * the reduction axis; §一: reconstruction formula).  Computes, in float32,
  *   Y[t][o] = s_t * sum_j (norm[o][j] / 128) * sum_i cb[idx[o][j][i]] * xr[t][128 j + i]

@@ -135,3 +135,14 @@ def test_q4_0_gemm_validation(lib):
     # K = 250 pads to 256 columns: 8 blocks
     assert cq.q4_0_gemm_workspace_bytes(3, 250) == (3 * 256 * 2 + 255) // 256 * 256
     assert cq.q4_0_gemm_workspace_bytes(0, 256) == 0
+
+
+def test_a8_groups_validation(lib):
+    INV, ALN = 1, 2
+    assert lib.a8_quantize_groups(A, 4, 100, 32, A, A, None) == INV        # G does not divide D
+    assert lib.a8_quantize_groups(A, 4, 96, 48, A, A, None) == INV         # G not a multiple of 32
+    assert lib.a8_quantize_groups(A, 4, 512, 512, A, A, None) == INV       # G above 256
+    assert lib.a8_quantize_groups(A, 0, 96, 32, A, A, None) == INV
+    assert lib.a8_quantize_groups(M, 4, 96, 32, A, A, None) == ALN
+    assert lib.a8_fake_quant_groups(A, 4, 96, 32, None, None) == INV
+    assert lib.a8_fake_quant_groups(A, 4, 96, 32, M, None) == ALN

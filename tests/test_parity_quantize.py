@@ -102,3 +102,19 @@ def test_codebook_fit_matches_oracle():
         ref = oracle.lloyd_max_gaussian_fit(s, L, 200)
         got = to_host(cq.cq_codebook_fit(ds, L, 200))
         assert np.allclose(got, ref, rtol=1e-6, atol=1e-7), (L, got, ref)
+
+
+@pytest.mark.parametrize("T,D,G", [(1, 32, 32), (7, 96, 32), (33, 512, 128), (5, 1024, 256),
+                                   (300, 128, 32), (2, 4096, 64)])
+def test_a8_groups_bit_exact(T, D, G):
+    """Grouped A8 (per-head query / KV cache, .cact page §四): codes, scales and the
+    fake-quant are bit-identical to the oracle, including zero groups and outliers."""
+    X = synth.activations(T, D, seed=T * 7 + D)
+    X[0, :G] = 0.0                                   # an all-zero group
+    X[-1, -1] = 1e4                                  # an outlier in the last group
+    codes, scales = cq.a8_quantize_groups(to_dev(X), G)
+    fq = cq.a8_fake_quant_groups(to_dev(X), G)
+    q_ref, s_ref = oracle.a8_quantize_groups(X, G)
+    assert np.array_equal(to_host(codes), q_ref)
+    assert np.array_equal(to_host(scales).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(to_host(fq).view(np.uint32), oracle.a8_fake_quant_groups(X, G).view(np.uint32))
