@@ -94,3 +94,36 @@ def test_gemm_grouped_20_layer_model(M):
             single = cq.cq_gemm(items[i][0], items[i][1], m.N, m.K, 4, cb, items[i][4],
                                 items[i][5])
             assert torch.equal(single, keep[i])
+
+
+def test_gemm_grouped_many_problems_and_activations():
+    """More problems than one launch holds (130 > 120) and more distinct activations than
+    one rotation launch or one GEMM launch takes (10 > 8): the call splits into several
+    launches and every matrix still matches its own single-matrix call bit for bit and
+    the oracle within the tolerance."""
+    cb = fitted_cb28()
+    dev = torch.device("cuda:0")
+    M = 70
+    Ks = [128, 256, 384, 512, 640, 768, 896, 1024, 1152, 1280]
+    X = {K: synth.activations(M, K, seed=900 + K) for K in Ks}
+    act = {K: cq.a8_quantize(to_dev(x)) for K, x in X.items()}
+    items, Ws, shapes = [], [], []
+    for i in range(130):
+        K = Ks[i % len(Ks)]
+        N = 16 * (1 + (i * 7) % 9)
+        W = synth.weights(N, K, seed=5000 + i)
+        Ws.append(W)
+        shapes.append((N, K))
+        packed, norms = cq.cq_encode(to_dev(W), 4, cb)
+        q, s = act[K]
+        items.append((packed, norms, N, K, q, s, torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+    cq.cq_gemm_grouped(cq.make_gemm_problems(items), M, 4, cb, device=dev)
+    cq.cq_device_error()
+    qs = {K: oracle.a8_quantize(x) for K, x in X.items()}
+    for i, (N, K) in enumerate(shapes):
+        single = cq.cq_gemm(items[i][0], items[i][1], N, K, 4, cb, items[i][4], items[i][5])
+        assert torch.equal(single, items[i][6]), i
+        if i % 13 == 0:
+            p_ref, n_ref = oracle.cq_encode(Ws[i], 4, cb)
+            ref = oracle.cq_gemm_ref(p_ref, n_ref, 4, cb, *qs[K])
+            assert max_rel_err(_bf16_to_np(items[i][6]), ref) < TOL, i
