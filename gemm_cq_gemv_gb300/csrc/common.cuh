@@ -105,9 +105,9 @@ __device__ __forceinline__ uint16_t f64_to_f16_bits_rne(double x) {
     return (uint16_t)(sign | (uint32_t)q);               // q == 1024 is the smallest normal
 }
 
-// Batched cq_gemv (4-bit indices) through the tensor-core pipeline of gemm.cu: fp16
+// Batched cq_gemv (1- to 4-bit indices) through the tensor-core pipeline of gemm.cu: fp16
 // operands, fp32 output; workspace >= B * K * 2 + 256 bytes, 16-byte aligned.
-cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
+cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K, int b,
                       const cq_codebook* cbk, const int8_t* Xq, const float* scale, int64_t B,
                       float* Y, void* workspace, cudaStream_t st);
 

@@ -53,7 +53,6 @@ constexpr int kEpiWarps = 8;
 constexpr int kDequantWarp0 = kEpiWarp0 + kEpiWarps;
 constexpr int kDequantWarps = 8;         // per stage: two per TMEM lane quarter
 constexpr int kDequantGroups = 2;        // warps 10..17 take even stages, 18..25 odd ones
-constexpr int kPTileBytes = kBO * kBK / 2;            // 4 KB of packed nibbles
 constexpr int kTmemCols = 512;
 constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
 constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + stages + barriers
@@ -64,9 +63,9 @@ constexpr int kMaxActs = 8;
 
 // Q4_0 weights reach shared memory in slabs of 256 k (8 blocks, 144 bytes per row: the
 // smallest 16-byte multiple of the 18-byte block), on a ring of slabs; each slab feeds
-// four 64-k stages.
+// four 64-k stages.  1- and 3-bit CQ rows (8 and 24 bytes per 64-k stage, no legal
+// tensor-copy box) take the same ring with slabs of two stages (16 and 48 bytes per row).
 constexpr int kQSlabRowBytes = 144;
-constexpr int kQSlabBytes = kBO * kQSlabRowBytes;       // 18 KB
 
 enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 
@@ -76,10 +75,13 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //           otherwise bf16 operands and bf16 output (prefill)
 //   STAGES  depth of the shared-memory ring (= tensor-memory A stages)
 //   FMT     weight format: CQ (packed indices + norms) or Q4_0 blocks
-//   SLABS   Q4_0: depth of the weight-slab ring
+//   SLABS   Q4_0 and 1-/3-bit CQ: depth of the weight-slab ring
 //   TLIST   look the CTA's tiles up once, into shared memory (grouped launches of many
 //           problems, where each lookup is a binary search over the parameter block)
-template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false>
+//   BITS    CQ index width: 4 or 2 (the packed tile rides in the stage, 32 or 16 bytes
+//           per row), 1 or 3 (slabs of two stages)
+template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false,
+          int BITS_ = 4>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
@@ -87,16 +89,28 @@ struct GemmCfg {
     static constexpr int FMT = FMT_;
     static constexpr int SLABS = SLABS_;
     static constexpr bool TLIST = TLIST_;
+    static constexpr int BITS = BITS_;
+    static constexpr bool CQSLAB = FMT == kFmtCQ && (BITS == 1 || BITS == 3);
+    static constexpr int PTILE = FMT == kFmtCQ && !CQSLAB ? kBO * kBK * BITS / 8 : 0;   // packed bytes per stage
+    static constexpr int SPS = FMT == kFmtQ40 ? 4 : 2;                            // stages per slab
+    static constexpr int SLABROW = FMT == kFmtQ40 ? kQSlabRowBytes : SPS * kBK * BITS / 8;
+    static constexpr int SLABBYTES = kBO * SLABROW;
     static constexpr int XTILE = BT * kBK * 2;        // activation tile bytes
-    static constexpr int STAGE = XTILE + (FMT == kFmtCQ ? kPTileBytes : 0);
+    static constexpr int STAGE = XTILE + PTILE;
     static constexpr int DCOL0 = STAGES * kACols;     // accumulators after the A stages
     static_assert(DCOL0 + 2 * BT <= kTmemCols, "tensor memory budget");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert((3 * STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
     static_assert(FMT == kFmtCQ || (F16 && SLABS >= 2), "Q4_0 runs with fp16 operands on a slab ring");
+    static_assert(BITS == 4 || (FMT == kFmtCQ && F16), "1- to 3-bit CQ rows: decode batches only");
+    static_assert(!CQSLAB || SLABS >= 2, "1- and 3-bit CQ rows run on a slab ring");
+    static_assert(FMT == kFmtQ40 || CQSLAB || SLABS == 0, "4- and 2-bit CQ tiles ride in the stages");
 };
 using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true>;   // 24 KB activation tile, 28 KB stages
 using DecodeCfg = GemmCfg<32, true, 8>;                  // 4 KB activation tile, 8 KB stages
+using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2>;   // 2-bit rows: 6 KB stages
+using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1>;   // 1-bit rows: 4 KB stages + 2 KB slabs
+using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3>;   // 3-bit rows: 4 KB stages + 6 KB slabs
 using Q40WideCfg = GemmCfg<192, true, 4, kFmtQ40, 4>;    // Q4_0, many tokens: 96 + 72 KB
 using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4>;   // Q4_0, up to 32 tokens: 32 + 72 KB
 
@@ -424,8 +438,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // CQ: the codeword-pair table sits at a 64 KB boundary of the shared window (the
     // address of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
-    // 1024-byte aligned stages fill the space below it, then the space above it.
-    // Q4_0: no table; the stages, then the two weight slabs.
+    // 1024-byte aligned stages fill the space below it, then the space above it, followed
+    // by the weight slabs of 1- and 3-bit rows.
+    // Q4_0: no table; the stages, then the weight slabs.
     const uint32_t sbase = smem_u32(smem_raw), send = sbase + (uint32_t)kGemmSmem;
     const uint32_t a0 = (sbase + 1023u) & ~1023u;
     uint32_t tbase, b0, slab0, bars_at;
@@ -433,21 +448,21 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     if constexpr (C::FMT == kFmtCQ) {
         tbase = (sbase + 65535u) & ~65535u;
         nA = tbase >= a0 + kStageBytes ? min(kStages, (int)((tbase - a0) / kStageBytes)) : 0;
-        b0 = tbase + 256u * 32u * 8u;
-        slab0 = 0;
-        bars_at = b0 + (uint32_t)(kStages - nA) * kStageBytes;
+        b0 = tbase + (1u << (2 * C::BITS)) * 32u * 8u;   // pair-table entries x lanes x 8 B
+        slab0 = b0 + (uint32_t)(kStages - nA) * kStageBytes;
+        bars_at = slab0 + (uint32_t)(C::SLABS * C::SLABBYTES);
     } else {
         tbase = 0;
         nA = kStages;
         b0 = a0;
         slab0 = a0 + (uint32_t)kStages * kStageBytes;
-        bars_at = slab0 + (uint32_t)(C::SLABS * kQSlabBytes);
+        bars_at = slab0 + (uint32_t)(C::SLABS * C::SLABBYTES);
     }
     auto gen = [&](uint32_t a) { return smem_raw + (a - sbase); };
     auto stage_ptr = [&](int s) {
         return gen(s < nA ? a0 + (uint32_t)s * kStageBytes : b0 + (uint32_t)(s - nA) * kStageBytes);
     };
-    float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [256][32] (CQ)
+    float2* lut2 = reinterpret_cast<float2*>(gen(tbase));   // [2^(2 BITS)][32] (CQ)
     uint64_t* bars = reinterpret_cast<uint64_t*>(gen(bars_at));
     // this CTA's tile list (problem, row tile, token tile, K half), after the barriers
     const uint32_t tiles_at = bars_at + (uint32_t)kBarBytes;
@@ -457,8 +472,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
     uint64_t* acc_full = bars + 3 * kStages;      // [2] accumulator buffer ready
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator buffer drained
-    uint64_t* slab_full = acc_empty + 2;          // [SLABS] Q4_0: weight slab landed
-    uint64_t* slab_empty = slab_full + C::SLABS;  // [SLABS] Q4_0: slab read by its four stages
+    uint64_t* slab_full = acc_empty + 2;          // [SLABS] weight slab landed
+    uint64_t* slab_empty = slab_full + C::SLABS;  // [SLABS] slab read by the dequant of its stages
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(slab_empty + C::SLABS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -469,8 +484,9 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         return;
     }
 
-    // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]), one copy per lane, built
-    // from the 16 levels staged in shared memory (one unrolled select per level thread)
+    // codeword-pair table: entry e = (cb[e & 15], cb[e >> 4]) for 4-bit indices,
+    // (cb[e & 3], cb[e >> 2]) for 2-bit ones, one copy per lane, built from the levels
+    // staged in shared memory (one unrolled select per level thread)
     float* slv = reinterpret_cast<float*>(tmem_slot + 4);   // 64 bytes inside the barrier block
     if (tid < 16) {
         float v = 0.0f;
@@ -480,9 +496,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     }
     __syncthreads();
     if constexpr (C::FMT == kFmtCQ) {
-        for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
+        constexpr int kHalf = C::BITS;                   // bits of one index of the pair
+        constexpr int kEntries = 1 << (2 * C::BITS);
+        for (int i = tid; i < kEntries * 32; i += kThreadsGemm) {
             const int e = i >> 5;
-            lut2[i] = make_float2(slv[e & 15], slv[e >> 4]);
+            lut2[i] = make_float2(slv[e & ((1 << kHalf) - 1)], slv[e >> kHalf]);
         }
     }
     if (tid == 0) {
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         }
         for (int b = 0; b < C::SLABS; ++b) {
             mbar_init(&slab_full[b], 1);
-            mbar_init(&slab_empty[b], 4 * kDequantWarps);   // four stages, eight warps each
+            mbar_init(&slab_empty[b], C::SPS * kDequantWarps);   // eight warps per stage
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -535,7 +553,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            int pg = 0;   // Q4_0: slabs issued
+            int pg = 0;   // slabs issued
             int ti = 0;
             for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++ti) {
                 const TileRef tr = tile_at(ti, tile);
@@ -544,26 +562,28 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 int kb, ke;
                 k_range(pr, tr.ks, kb, ke);
                 for (int kc = kb; kc < ke; ++kc) {
-                    if constexpr (C::FMT == kFmtQ40) {
-                        if ((kc & 3) == 0) {   // the slab of this stage and the next three
+                    if constexpr (C::SLABS > 0) {
+                        // the slab of this stage and the next SPS - 1 (tile K ranges are
+                        // whole slabs)
+                        if (kc % C::SPS == 0) {
                             const int qs = pg % C::SLABS;
                             const uint32_t sph = (uint32_t)((pg / C::SLABS) & 1);
                             if (!mbar_wait(&slab_empty[qs], sph ^ 1u, abort_flag, p)) {
                                 ok = false;
                                 break;
                             }
-                            mbar_arrive_tx(&slab_full[qs], kQSlabBytes);
-                            tma_load_2d(gen(slab0 + (uint32_t)(qs * kQSlabBytes)), &pr.pmap,
-                                        (kc >> 2) * kQSlabRowBytes, tr.nt * kBO, &slab_full[qs]);
+                            mbar_arrive_tx(&slab_full[qs], C::SLABBYTES);
+                            tma_load_2d(gen(slab0 + (uint32_t)(qs * C::SLABBYTES)), &pr.pmap,
+                                        (kc / C::SPS) * C::SLABROW, tr.nt * kBO, &slab_full[qs]);
                             ++pg;
                         }
                     }
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p)) { ok = false; break; }
                     uint8_t* st = stage_ptr(s);
-                    if constexpr (C::FMT == kFmtCQ) {
-                        mbar_arrive_tx(&full_a[s], kXTileBytes + kPTileBytes);
+                    if constexpr (C::PTILE > 0) {
+                        mbar_arrive_tx(&full_a[s], kXTileBytes + C::PTILE);
                         tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
-                        tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK / 2), tr.nt * kBO, &full_a[s]);
+                        tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK * C::BITS / 8), tr.nt * kBO, &full_a[s]);
                     } else {
                         mbar_arrive_tx(&full_a[s], kXTileBytes);
                         tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
@@ -689,7 +709,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                     // the full_a wait frees the A stage (its previous MMA has completed)
                     // and, through full_b, orders the activation tile for the MMA
                     if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
-                    const int sg = gi >> 2;   // every K is a whole number of slabs
+                    const int sg = gi / C::SPS;   // every K is a whole number of slabs
                     const int qs = sg % C::SLABS;
                     if (!mbar_wait(&slab_full[qs], (uint32_t)((sg / C::SLABS) & 1), abort_flag, p)) {
                         ok = false;
@@ -699,7 +719,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                     // byte 36 (kc & 3) + 18 kh: five words from the 4-byte boundary at or
                     // below it hold the fp16 scale and the 16 nibble bytes
                     const uint32_t* w32 = reinterpret_cast<const uint32_t*>(
-                        gen(slab0 + (uint32_t)(qs * kQSlabBytes) + (uint32_t)(r * kQSlabRowBytes)));
+                        gen(slab0 + (uint32_t)(qs * C::SLABBYTES) + (uint32_t)(r * C::SLABROW)));
                     const int wb = 9 * (kc & 3) + 4 * kh;
                     uint32_t w[5];
 #pragma unroll
@@ -736,8 +756,56 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 }
                 const float nrm = load_norm(pr, tr.nt * kBO + r, kc);
                 if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
-                const uint4 w = *reinterpret_cast<const uint4*>(stage_ptr(s) + kXTileBytes + r * 32 + kh * 16);
-                const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                if constexpr (C::CQSLAB) {
+                    const int sg = gi / C::SPS;   // every K is a whole number of slabs
+                    const int qs = sg % C::SLABS;
+                    if (!mbar_wait(&slab_full[qs], (uint32_t)((sg / C::SLABS) & 1), abort_flag, p)) {
+                        ok = false;
+                        break;
+                    }
+                    // half kh of stage kc & 1 starts at index 64 (kc & 1) + 32 kh of the
+                    // slab row: BITS whole words (the rows are LSB-first bit strings)
+                    const uint32_t* w32 = reinterpret_cast<const uint32_t*>(
+                        gen(slab0 + (uint32_t)(qs * C::SLABBYTES) + (uint32_t)(r * C::SLABROW)));
+                    const int wb = ((kc & 1) * 2 + kh) * C::BITS;
+                    uint32_t w[C::BITS + 1];
+#pragma unroll
+                    for (int i = 0; i < C::BITS; ++i) w[i] = w32[wb + i];
+                    w[C::BITS] = 0u;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&slab_empty[qs]);
+                    const float2 n2 = make_float2(nrm, nrm);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int pi = 0; pi < 16; ++pi) {
+                        // pair pi = indices 2 pi, 2 pi + 1: 2 BITS bits from bit 2 BITS pi
+                        constexpr int kPB = 2 * C::BITS;
+                        const int bo = kPB * pi;
+                        const uint32_t v = __funnelshift_r(w[bo >> 5], w[(bo >> 5) + 1], bo & 31);
+                        const uint32_t e = v & ((1u << kPB) - 1u);
+                        const float2 cn = __fmul2_rn(lds_f2(lb + (e << 8)), n2);
+                        __half2 h = __floats2half2_rn(cn.x, cn.y);
+                        pk[pi] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    continue;
+                }
+                // this lane's 32 indices of the stage half kh, as 16 pair bytes: 4-bit rows
+                // hold one pair per byte; a 2-bit byte holds two pairs, split by nibble
+                // (the low nibble is the byte's first pair)
+                uint32_t wv[4];
+                if constexpr (C::BITS == 4) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(stage_ptr(s) + kXTileBytes + r * 32 + kh * 16);
+                    wv[0] = w.x; wv[1] = w.y; wv[2] = w.z; wv[3] = w.w;
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2*>(stage_ptr(s) + kXTileBytes + r * 16 + kh * 8);
+                    wv[0] = w.x & 0x0F0F0F0Fu; wv[1] = (w.x >> 4) & 0x0F0F0F0Fu;
+                    wv[2] = w.y & 0x0F0F0F0Fu; wv[3] = (w.y >> 4) & 0x0F0F0F0Fu;
+                }
                 const float2 n2 = make_float2(nrm, nrm);
                 uint32_t pk[16];
 #pragma unroll
@@ -746,13 +814,16 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                                          lds_f2(pair_addr<2>(wv[k], lb)), lds_f2(pair_addr<3>(wv[k], lb))};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
+                        // pair index within the half: byte j of word k (4-bit), or byte j
+                        // of packed word k / 2, low or high nibble (2-bit)
+                        const int pi = C::BITS == 4 ? 4 * k + j : 8 * (k >> 1) + 2 * j + (k & 1);
                         const float2 cn = __fmul2_rn(c[j], n2);
                         if constexpr (C::F16) {
                             __half2 v = __floats2half2_rn(cn.x, cn.y);
-                            pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
+                            pk[pi] = *reinterpret_cast<uint32_t*>(&v);
                         } else {
                             __nv_bfloat162 v = __floats2bfloat162_rn(cn.x, cn.y);
-                            pk[4 * k + j] = *reinterpret_cast<uint32_t*>(&v);
+                            pk[pi] = *reinterpret_cast<uint32_t*>(&v);
                         }
                     }
                 }
@@ -782,7 +853,7 @@ static __device__ unsigned int g_gemm_err;
 std::mutex g_host_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned int* g_err_ptr[64] = {nullptr};
-bool g_attr_done[64][4] = {};
+bool g_attr_done[64][7] = {};
 
 template <class C>
 cq_status set_smem_attr(int dev, int slot) {
@@ -820,6 +891,9 @@ cq_status host_setup(unsigned int** err) {
     if (st == CQ_OK) st = set_smem_attr<DecodeCfg>(dev, 1);
     if (st == CQ_OK) st = set_smem_attr<Q40WideCfg>(dev, 2);
     if (st == CQ_OK) st = set_smem_attr<Q40NarrowCfg>(dev, 3);
+    if (st == CQ_OK) st = set_smem_attr<Decode2Cfg>(dev, 4);
+    if (st == CQ_OK) st = set_smem_attr<Decode1Cfg>(dev, 5);
+    if (st == CQ_OK) st = set_smem_attr<Decode3Cfg>(dev, 6);
     if (st != CQ_OK) return st;
     *err = g_err_ptr[dev];
     return CQ_OK;
@@ -831,37 +905,42 @@ cq_status host_setup(unsigned int** err) {
 struct MapEntry {
     const void* base;
     int64_t N, K;
+    int bits;
     CUtensorMap map;
 };
 constexpr int kMapCache = 4096;   // power of two
 MapEntry g_map_cache[kMapCache];
 
-cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N, int64_t K);
+cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N, int64_t K, int bits);
 
-cq_status make_packed_map(CUtensorMap* map, const void* base, int64_t N, int64_t K) {
+cq_status make_packed_map(CUtensorMap* map, const void* base, int64_t N, int64_t K, int bits) {
     uint64_t h = reinterpret_cast<uint64_t>(base) * 0x9E3779B97F4A7C15ull ^ (uint64_t)N * 0xC2B2AE3D27D4EB4Full ^
-                 (uint64_t)K;
+                 ((uint64_t)K << 3 | (uint64_t)bits);
     for (int probe = 0; probe < 8; ++probe) {
         MapEntry& e = g_map_cache[(h + (uint64_t)probe) & (kMapCache - 1)];
-        if (e.base == base && e.N == N && e.K == K) {
+        if (e.base == base && e.N == N && e.K == K && e.bits == bits) {
             *map = e.map;
             return CQ_OK;
         }
         if (e.base == nullptr) {
-            const cq_status st = make_packed_map_uncached(&e.map, base, N, K);
+            const cq_status st = make_packed_map_uncached(&e.map, base, N, K, bits);
             if (st != CQ_OK) return st;
-            e.base = base; e.N = N; e.K = K;
+            e.base = base; e.N = N; e.K = K; e.bits = bits;
             *map = e.map;
             return CQ_OK;
         }
     }
-    return make_packed_map_uncached(map, base, N, K);   // neighbourhood full: no caching
+    return make_packed_map_uncached(map, base, N, K, bits);   // neighbourhood full: no caching
 }
 
-cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N, int64_t K) {
-    cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)N};
-    cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-    cuuint32_t box[2] = {(cuuint32_t)(kBK / 2), (cuuint32_t)kBO};
+// packed index rows [N][K * bits / 8] bytes; box = one stage's kBK indices x 128 rows
+// (32 bytes for 4-bit rows, 16 for 2-bit ones), or a slab of two stages for 1- and 3-bit
+// rows (16 and 48 bytes)
+cq_status make_packed_map_uncached(CUtensorMap* map, const void* base, int64_t N, int64_t K, int bits) {
+    const int box_k = (bits == 1 || bits == 3) ? 2 * kBK : kBK;
+    cuuint64_t dims[2] = {(cuuint64_t)(K * bits / 8), (cuuint64_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(K * bits / 8)};
+    cuuint32_t box[2] = {(cuuint32_t)(box_k * bits / 8), (cuuint32_t)kBO};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -924,6 +1003,11 @@ void choose_split(GemmProblem& gp, int tiles_m, int align) {
 
 void fill_levels(float (&lv)[16], int b, const cq_codebook* cbk) {
     for (int t = 0; t < 16; ++t) lv[t] = 0.0f;
+    if (b == 1) {   // the fixed 1-bit codebook, +-sqrt(2 / pi)
+        const float c = 0.797884560802865355879892119868763737f;
+        lv[0] = -c; lv[1] = c;
+        return;
+    }
     const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
     for (int t = 0; t < (1 << b); ++t) lv[t] = cbk->cb[off + t];
 }
@@ -1076,11 +1160,11 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
             gp.packed = q.packed; gp.norms = q.norms; gp.scale = q.scale;
             gp.Y = q.Y;
             gp.N = (int)q.N; gp.K = (int)q.K; gp.act = map_of_act[a];
-            st = make_packed_map(&gp.pmap, q.packed, q.N, q.K);
+            st = make_packed_map(&gp.pmap, q.packed, q.N, q.K, C::BITS);
             if (st != CQ_OK) return st;
             gp.tiles_n = (int)((q.N + kBO - 1) / kBO);
             gp.tile_begin = tiles;
-            choose_split<C>(gp, tiles_m, 1);
+            choose_split<C>(gp, tiles_m, C::SLABS > 0 ? C::SPS : 1);   // whole slabs
             if (gp.ksplit > 1) {
                 const cudaError_t e = cudaMemsetAsync(q.Y, 0, (size_t)M * (size_t)q.N * sizeof(float), cs);
                 if (e != cudaSuccess) { set_last_cuda_error((int)e); return CQ_ERR_CUDA; }
@@ -1142,17 +1226,23 @@ extern "C" cq_status cq_gemm(const uint8_t* packed, const uint16_t* norms, int64
 
 namespace cq {
 
-// The batched decode product of cq_gemv for 4-bit indices on the tensor cores: the same
-// pipeline with 32-token tiles, fp16 operands (so the result meets the fp32 GEMV's error
-// bound) and fp32 output.  `workspace` (16-byte aligned, at least B * K * 2 + 256 bytes)
-// receives the rotated fp16 activations.
-cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
+// The batched decode product of cq_gemv (1- to 4-bit indices) on the tensor cores: the
+// same pipeline with 32-token tiles, fp16 operands (so the result meets the fp32 GEMV's
+// error bound) and fp32 output.  `workspace` (16-byte aligned, at least B * K * 2 + 256
+// bytes) receives the rotated fp16 activations.
+cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K, int b,
                       const cq_codebook* cbk, const int8_t* Xq, const float* scale, int64_t B,
                       float* Y, void* workspace, cudaStream_t st) {
     cq_gemm_problem q;
     q.packed = packed; q.norms = norms; q.N = N; q.K = K; q.Xq = Xq; q.scale = scale;
     q.Y = reinterpret_cast<uint16_t*>(Y);   // the pipeline stores fp32 for this configuration
-    return run_grouped<DecodeCfg>(&q, 1, B, 4, cbk, workspace, st);
+    switch (b) {
+        case 1: return run_grouped<Decode1Cfg>(&q, 1, B, 1, cbk, workspace, st);
+        case 2: return run_grouped<Decode2Cfg>(&q, 1, B, 2, cbk, workspace, st);
+        case 3: return run_grouped<Decode3Cfg>(&q, 1, B, 3, cbk, workspace, st);
+        case 4: return run_grouped<DecodeCfg>(&q, 1, B, 4, cbk, workspace, st);
+        default: return CQ_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace cq

@@ -1060,10 +1060,10 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     if (!aligned16(workspace)) return CQ_ERR_ALIGNMENT;
     if (K > 2 * kWarps2 * kSeg) return CQ_ERR_UNSUPPORTED;   // at most 2 segments per warp
     cudaStream_t st = as_stream(stream);
-    // batches of 4-bit rows go through the tensor cores: the weights are read and decoded
-    // once for all tokens (the workspace, B * K * 4 bytes, holds the fp16 activations)
-    if (b == 4 && B >= kTensorMinBatch && N % 16 == 0)
-        return gemv_tensor(packed, norms, N, K, cbk, Xq, scale, B, Y, workspace, st);
+    // batches go through the tensor cores: the weights are read and decoded once for all
+    // tokens (the workspace, B * K * 4 bytes, holds the fp16 activations)
+    if (B >= kTensorMinBatch && N % 16 == 0)
+        return gemv_tensor(packed, norms, N, K, b, cbk, Xq, scale, B, Y, workspace, st);
     // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
     // tokens per pass when each warp owns a single segment
     const int nseg = (int)((K + kSeg - 1) / kSeg);

@@ -125,11 +125,12 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  * with xr = Hu @ Xq per group (the rotated int8 activations, exact integers), which
  * equals (W_hat @ (s * Xq)^T)^T in real arithmetic because Hu is symmetric.
  * Two execution paths, chosen from the arguments:
- *   - B <= 2, or b < 4, or N not a multiple of 16: the CUDA-core GEMV, fp32 products
- *     and accumulation; at B <= 2 the rotation happens inside the kernel, otherwise
- *     once per call into `workspace`, shared by every row.
- *   - b = 4, B >= 3, N a multiple of 16: the tensor-core pipeline of cq_gemm with 32-token
- *     tiles.  The weights are decoded once for all tokens; the operands are fp16
+ *   - B <= 2, or N not a multiple of 16: the CUDA-core GEMV, fp32 products and
+ *     accumulation; at B <= 2 the rotation happens inside the kernel, otherwise once per
+ *     call into `workspace`, shared by every row.
+ *   - B >= 3, N a multiple of 16 (any b): the tensor-core pipeline of cq_gemm with
+ *     32-token tiles (4- and 2-bit rows reach shared memory per 64-index stage, 1- and
+ *     3-bit rows per 128-index slab).  The weights are decoded once for all tokens; the operands are fp16
  *     (cb * norm, and xr * s_t / 128 in `workspace`), the accumulation fp32.  The
  *     relative error stays within 1e-3 of the exact product; activations must satisfy
  *     max |X[t][k]| <= 65504 (fp16 range).  When the row tiles are too few to occupy the

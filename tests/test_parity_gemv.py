@@ -87,25 +87,28 @@ def test_cq_gemv_large_sampled(m, B):
     assert max_rel_err(Y, ref) < TOL
 
 
+@pytest.mark.parametrize("b", [4, 3, 2, 1])
 @pytest.mark.parametrize("N,K,B", [(400, 1152, 3), (128, 8192, 8), (1040, 4096, 37), (16, 128, 5),
                                    (2048, 2048, 32)])
-def test_cq_gemv_batched_tensor_path(N, K, B):
-    """4-bit batches of >= 3 tokens (rows a multiple of 16) run on the tensor cores with fp16
-    operands and fp32 accumulation: ragged row tiles, ragged token tiles, long K."""
-    Y, ref = _cq_case(N, K, 4, B, 5 * N + K, 13 * K + B, outliers=True)
+def test_cq_gemv_batched_tensor_path(N, K, B, b):
+    """Batches of >= 3 tokens (rows a multiple of 16) run on the tensor cores with fp16
+    operands and fp32 accumulation, every index width: ragged row tiles, ragged token
+    tiles, long K, K split in two (128 x 8192)."""
+    Y, ref = _cq_case(N, K, b, B, 5 * N + K + b, 13 * K + B, outliers=True)
     assert max_rel_err(Y, ref) < TOL
 
 
-def test_cq_gemv_batched_tensor_path_deterministic():
+@pytest.mark.parametrize("b", [4, 3, 2, 1])
+def test_cq_gemv_batched_tensor_path_deterministic(b):
     """The tensor-core batch with a two-way K split (few row tiles) reruns bit-identically."""
     cb = fitted_cb28()
     W = synth.weights(512, 4096, seed=41)
     X = synth.activations(8, 4096, seed=42)
-    packed, norms = cq.cq_encode(to_dev(W), 4, cb)
+    packed, norms = cq.cq_encode(to_dev(W), b, cb)
     q, s = cq.a8_quantize(to_dev(X))
-    a = to_host(cq.cq_gemv(packed, norms, 512, 4096, 4, cb, q, s))
-    b = to_host(cq.cq_gemv(packed, norms, 512, 4096, 4, cb, q, s))
-    assert np.array_equal(a, b)
+    y0 = to_host(cq.cq_gemv(packed, norms, 512, 4096, b, cb, q, s))
+    y1 = to_host(cq.cq_gemv(packed, norms, 512, 4096, b, cb, q, s))
+    assert np.array_equal(y0, y1)
 
 
 def test_cq_gemv_batch_consistency():
