@@ -201,8 +201,8 @@ cq_status cq_probe_bounded_wait(uint64_t timeout_ns, void* stream);
  * was raised, else CQ_OK.  Synchronises `stream`. */
 cq_status cq_device_error(void* stream);
 
-/* ---- cq_gemv without a workspace (the paper has no counterpart to this entry point:
- * it is a library convenience).  Same computation, arguments and errors as cq_gemv, minus the
+/* ---- cq_gemv without a workspace (no counterpart in the format's description: a library
+ * convenience).  Same computation, arguments and errors as cq_gemv, minus the
  * workspace, for callers that may not allocate device memory - typically code running
  * inside a host framework that owns every device allocation (an inference-server
  * plugin, an engine with a fixed memory budget) and forbids cudaMalloc while it runs.
