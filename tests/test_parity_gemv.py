@@ -87,6 +87,19 @@ def test_cq_gemv_large_sampled(m, B):
     assert max_rel_err(Y, ref) < TOL
 
 
+@pytest.mark.parametrize("b", [1, 2, 3])
+@pytest.mark.parametrize("B", [1, 32])
+def test_cq_gemv_large_widths_sampled(b, B):
+    """1- to 3-bit rows on [8192, 28672]: the longest K of the large shapes (448 stages,
+    K split in two on the tensor path at B = 32; two K segments per warp at B = 1)."""
+    m = synth.LARGE[2]
+    rows = np.sort(np.random.default_rng(b + B).choice(m.N, 128, replace=False))
+    rows[0], rows[-1] = 0, m.N - 1
+    Y, ref = _cq_case(m.N, m.K, b, B, synth.weight_seed(4, 2), synth.activation_seed(4, B),
+                      outliers=True, rows=rows)
+    assert max_rel_err(Y, ref) < TOL
+
+
 @pytest.mark.parametrize("b", [4, 3, 2, 1])
 @pytest.mark.parametrize("N,K,B", [(400, 1152, 3), (128, 8192, 8), (1040, 4096, 37), (16, 128, 5),
                                    (2048, 2048, 32)])
