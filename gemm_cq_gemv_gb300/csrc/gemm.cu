@@ -1072,6 +1072,11 @@ extern "C" size_t cq_gemm_grouped_workspace_bytes(const cq_gemm_problem* probs, 
 template <class C>
 cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
                       const cq_codebook* cbk, void* workspace, cudaStream_t cs) {
+    // tile numbers are 32-bit: a problem may hold up to 2^23 output tiles (twice that
+    // when split), so a launch of kMaxProblems problems stays below 2^31
+    const int64_t tiles_m64 = (M + C::BT - 1) / C::BT;
+    for (int i = 0; i < count; ++i)
+        if (tiles_m64 * ((probs[i].N + kBO - 1) / kBO) > ((int64_t)1 << 23)) return CQ_ERR_UNSUPPORTED;
     unsigned int* err = nullptr;
     cq_status st = host_setup(&err);
     if (st != CQ_OK) return st;

@@ -1062,7 +1062,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     if (!packed || !norms || !cbk || !Xq || !scale || !Y || N < 1 || K < 1 || B < 1)
         return CQ_ERR_INVALID_ARG;
     if (g != kGroup || K % kGroup != 0 || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
-    if (K > (1 << 24) || N > kMaxGemvRows) return CQ_ERR_UNSUPPORTED;
+    if (K > (1 << 24) || N > kMaxGemvRows || B > (1 << 30)) return CQ_ERR_UNSUPPORTED;
     if (!aligned16(packed) || !aligned16(norms) || !aligned16(Xq) || !aligned16(scale) ||
         !aligned16(Y))
         return CQ_ERR_ALIGNMENT;
@@ -1142,7 +1142,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
 extern "C" cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X,
                                int64_t B, float* Y, void* stream) {
     if (!blocks || !X || !Y || N < 1 || K < 1 || B < 1) return CQ_ERR_INVALID_ARG;
-    if (K > 2 * kWarps2 * kSeg || N > kMaxGemvRows) return CQ_ERR_UNSUPPORTED;
+    if (K > 2 * kWarps2 * kSeg || N > kMaxGemvRows || B > (1 << 30)) return CQ_ERR_UNSUPPORTED;
     if (!aligned16(blocks) || !aligned16(X) || !aligned16(Y)) return CQ_ERR_ALIGNMENT;
     Q40GemvParams p;
     p.blocks = blocks; p.X = X; p.Y = Y; p.N = N; p.K = (int)K;

@@ -140,7 +140,8 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
  *   Y  [B][N] float32
  *   workspace      device scratch of at least cq_gemv_workspace_bytes(B, K) bytes
- * K is limited to 32768 and N to 2^31 - 1024 (CQ_ERR_UNSUPPORTED above).  Deterministic:
+ * K is limited to 32768, N to 2^31 - 1024 and B to 2^30; on the tensor-core path also
+ * ceil(B / 32) * ceil(N / 128) to 2^23 (CQ_ERR_UNSUPPORTED above).  Deterministic:
  * the same inputs give bit-identical outputs.
  * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
 size_t cq_gemv_workspace_bytes(int64_t B, int64_t K);
@@ -154,7 +155,9 @@ cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64
  *   Y[t][o] = bf16( s_t / 128 * sum_k bf16(xr[t][k]) * bf16(cb[idx[o][k]] * norm[o][k/128]) )
  * with xr = Hu @ Xq per group (rotated once per call into `workspace`, bf16), tcgen05
  * MMA with fp32 accumulation in tensor memory.  Only b = 4 is implemented
- * (CQ_ERR_UNSUPPORTED otherwise).  N must be a multiple of 16.
+ * (CQ_ERR_UNSUPPORTED otherwise).  N must be a multiple of 16 (INVALID_ARG); N and K
+ * are limited to 2^24 (INVALID_ARG above), M to 2^30 (INVALID_ARG), and
+ * ceil(M / 192) * ceil(N / 128) output tiles to 2^23 (UNSUPPORTED above).
  *   Xq [M][K] int8, scale [M] float32 (a8_quantize), Y [M][N] bf16 (uint16 bits)
  *   workspace: >= cq_gemm_workspace_bytes(M, K) bytes, 256-byte aligned
  * A device-side wait that does not complete within 2 s sets a device error flag and
@@ -179,8 +182,9 @@ typedef struct cq_gemm_problem {
 } cq_gemm_problem;
 
 /* ---- A6 grouped: every problem of `probs` (host array of `count`) with the same M in
- * one persistent launch per 128 problems (e.g. the 120 matrices of a 20-layer model,
- * layer-major).  Same arithmetic, limits and errors as cq_gemm; the workspace holds one
+ * one persistent launch per 120 problems and 8 distinct activations (e.g. the 120
+ * matrices of a 20-layer model, layer-major; up to 1024 problems per call, UNSUPPORTED
+ * above).  Same arithmetic, limits and errors as cq_gemm; the workspace holds one
  * rotated copy per distinct Xq: cq_gemm_grouped_workspace_bytes(probs, count, M). */
 size_t cq_gemm_grouped_workspace_bytes(const cq_gemm_problem* probs, int count, int64_t M);
 cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, int64_t M, int g, int b,
@@ -231,7 +235,8 @@ cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks, v
  * row-aligned blocks).  Y[t][o] = sum_blocks fp32(d) * sum_k (nib - 8) * X[t][k],
  * float32 accumulation; padding columns are skipped.
  *   blocks [N][ceil(K/32) * 18] uint8, X [B][K] float32, Y [B][N] float32 (all 16-byte
- *   aligned); K is limited to 32768 and N to 2^31 - 1024 (CQ_ERR_UNSUPPORTED above).
+ *   aligned); K is limited to 32768, N to 2^31 - 1024 and B to 2^30 (CQ_ERR_UNSUPPORTED
+ *   above).
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA. */
 cq_status q4_0_gemv(const uint8_t* blocks, int64_t N, int64_t K, const float* X, int64_t B,
                     float* Y, void* stream);

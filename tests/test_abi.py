@@ -91,6 +91,11 @@ def test_gemv_validation(lib):
     assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 1, M, A, 1 << 20, None) == ALN
     assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 2, A, A, 16, None) == WS
     assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 2, A, None, 1 << 20, None) == WS
+    UNS = 3
+    assert f(A, A, 8, 128, 128, 4, _cb(), A, A, (1 << 30) + 1, A, A, 1 << 40, None) == UNS   # B
+    # tensor-core path: ceil(B / 32) * ceil(N / 128) = 2^15 * 2^17 output tiles > 2^23
+    assert f(A, A, 1 << 24, 128, 128, 2, _cb(), A, A, 1 << 20, A, A, 1 << 40, None) == UNS
+    assert lib.q4_0_gemv(A, 1, 32, A, (1 << 30) + 1, A, None) == UNS
 
 
 def test_codebook_fit_validation(lib):
@@ -109,6 +114,8 @@ def test_gemm_validation(lib):
     assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 0, A, A, big, None) == INV     # M = 0
     assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 256, M, A, big, None) == ALN
     assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 256, A, A, 100, None) == WS
+    # 2^24 rows x 2^30 tokens: far more than 2^23 output tiles
+    assert f(A, A, 1 << 24, 128, 128, 4, _cb(), A, A, 1 << 30, A, A, 1 << 40, None) == UNS
     assert cq.cq_gemm_workspace_bytes(300, 512) == (300 * 512 * 2 + 255) // 256 * 256
     # grouped: problems sharing an activation count it once
     probs = (cq.cq_gemm_problem * 3)()
