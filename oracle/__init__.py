@@ -23,7 +23,8 @@ Sources (cited by title and section; the pages are Chinese-language web articles
           fake-quant, one 4-byte scale per ``KV_GROUP = 32`` values).
 * [MMAP]  "免解析加载的秘诀：mmap 直读张量与 Needle 的秒级冷启动",
           section "mmap 之下张量按偏移直读" (groups of 128, the same reconstruction,
-          the analytic 1-bit codebook ``{-sqrt(2/pi), +sqrt(2/pi)}``).
+          the analytic 1-bit codebook ``{-sqrt(2/pi), +sqrt(2/pi)}`` and the ternary
+          ``{-c, 0, c}`` of bits = 5, both hard-coded in the engine).
 * [KMCU]  Minueza-32M -> KMCU v1 conversion page (pnsm.cn, MCU series),
           §1 (model shapes), §2 "Q4_0 量化" (32-weight blocks, fp16 ``d = max_abs/8``,
           ``q = clip(rint(w/d), -8, 7)``, nibble = q + 8, low nibble = even index,
@@ -39,9 +40,12 @@ No function in this package is "parity unpinned".
 """
 
 from .hadamard import sylvester_hadamard, fwht_butterfly
-from .lloyd_max import lloyd_max_gaussian_fit, gaussian_quantile_init, ONE_BIT_LEVEL
+from .lloyd_max import (lloyd_max_gaussian_fit, gaussian_quantile_init, ONE_BIT_LEVEL,
+                        TERNARY_LEVEL, ternary_gaussian_level)
 from .cq import (
     GROUP,
+    TERNARY,
+    field_bits,
     codebook_levels,
     codebook_concat,
     pack_indices,
@@ -56,7 +60,8 @@ from .products import cq_gemv_ref, cq_gemm_ref, q4_0_gemv_ref
 __all__ = [
     "sylvester_hadamard", "fwht_butterfly",
     "lloyd_max_gaussian_fit", "gaussian_quantile_init", "ONE_BIT_LEVEL",
-    "GROUP", "codebook_levels", "codebook_concat", "pack_indices", "unpack_indices",
+    "TERNARY_LEVEL", "ternary_gaussian_level",
+    "GROUP", "TERNARY", "field_bits", "codebook_levels", "codebook_concat", "pack_indices", "unpack_indices",
     "cq_encode", "cq_reconstruct",
     "a8_quantize", "a8_dequantize", "a8_quantize_groups", "a8_fake_quant_groups",
     "q4_0_quantize", "q4_0_dequantize", "q4_0_row_bytes", "Q4_0_BLOCK", "Q4_0_BLOCK_BYTES",

@@ -8,7 +8,8 @@ What the pages fix:
     and the group's L2 norm (FP16) are kept;
   * reconstruction ``w_group = (codebook_bits[idx] * norm) @ H``, H the normalised WHT;
   * codebooks ``cb2[4] | cb3[8] | cb4[16]`` concatenated, indexed by bit width; the
-    1-bit codebook is ``{-sqrt(2/pi), +sqrt(2/pi)}``, hard-coded, no table;
+    1-bit codebook is ``{-sqrt(2/pi), +sqrt(2/pi)}`` and the ternary one (bits = 5)
+    ``{-c, 0, +c}``, both hard-coded, no table ([MMAP]);
   * indices are packed LSB-first, the low nibble holding the even column.
 
 Readings taken (the pages are silent or inconsistent):
@@ -28,15 +29,25 @@ Readings taken (the pages are silent or inconsistent):
   * packing for b < 4 (the pages only describe nibbles): a dense LSB-first bit stream
     per group, index i in bits [b*i, b*i + b) of the group's little-endian bytes, so a
     group is 16*b bytes; for b = 4 this is exactly "low nibble = even column";
-  * norms are a separate ``[N, K/g]`` float16 array.
+  * norms are a separate ``[N, K/g]`` float16 array;
+  * ternary (bits = 5): ``c`` is the three-level Lloyd-Max Gaussian level (see
+    ``lloyd_max.ternary_gaussian_level``), the levels ``[-c, 0, +c]`` take indices
+    0, 1, 2, and an index is stored in a 2-bit field of the same LSB-first stream (the
+    smallest field that holds three values), so a group is 32 bytes.
 """
 
 import numpy as np
 
 from .hadamard import fwht_butterfly, sylvester_hadamard
-from .lloyd_max import ONE_BIT_LEVEL
+from .lloyd_max import ONE_BIT_LEVEL, TERNARY_LEVEL
 
 GROUP = 128  # [CACT] §一: "每个 group 默认 128 维"; [MMAP]: "按 128 的 group 切块"
+TERNARY = 5  # [MMAP]: the bits value of the ternary codebook
+
+
+def field_bits(b: int) -> int:
+    """Bits of one packed index of code ``b``: ``b``, or 2 for the ternary code."""
+    return 2 if b == TERNARY else b
 
 _CB_OFFSETS = {2: (0, 4), 3: (4, 12), 4: (12, 28)}
 
@@ -53,13 +64,17 @@ def codebook_concat(cb2, cb3, cb4) -> np.ndarray:
 def codebook_levels(cb28: np.ndarray, b: int) -> np.ndarray:
     """Levels for bit width ``b`` as float32, ascending.
 
-    b = 1 ignores the table and uses the analytic +-sqrt(2/pi) ([MMAP]).
+    b = 1 ignores the table and uses the analytic +-sqrt(2/pi); b = 5 (ternary) the
+    fixed ``[-c, 0, +c]`` ([MMAP]).
     """
     if b == 1:
         c = np.float32(ONE_BIT_LEVEL)
         return np.array([-c, c], dtype=np.float32)
+    if b == TERNARY:
+        c = np.float32(TERNARY_LEVEL)
+        return np.array([-c, 0.0, c], dtype=np.float32)
     if b not in _CB_OFFSETS:
-        raise ValueError("CQ bit width must be 1..4")
+        raise ValueError("CQ bit width must be 1..4, or 5 (ternary)")
     lo, hi = _CB_OFFSETS[b]
     return np.asarray(cb28, dtype=np.float32)[lo:hi].copy()
 
@@ -120,8 +135,9 @@ def _encode_groups(wg: np.ndarray, levels: np.ndarray):
 def cq_encode(W: np.ndarray, b: int, cb28: np.ndarray, g: int = GROUP):
     """CQ-encode ``W`` (``[N, K]`` float32, ``[out, in]``) at ``b`` bits.
 
-    Returns ``(packed, norms)``: ``packed`` uint8 ``[N, K/g, 16*b]`` and ``norms``
-    uint16 ``[N, K/g]`` holding the IEEE float16 bits of each group's L2 norm.
+    Returns ``(packed, norms)``: ``packed`` uint8 ``[N, K/g, 16*f]`` (``f`` =
+    ``field_bits(b)``) and ``norms`` uint16 ``[N, K/g]`` holding the IEEE float16 bits of
+    each group's L2 norm.
     """
     W = np.asarray(W, dtype=np.float32)
     if g != GROUP:
@@ -137,7 +153,8 @@ def cq_encode(W: np.ndarray, b: int, cb28: np.ndarray, g: int = GROUP):
     for c0 in range(0, N * G, 8192):          # chunks only bound host memory
         idx[c0:c0 + 8192], n[c0:c0 + 8192] = _encode_groups(flat[c0:c0 + 8192], levels)
     norms16 = n.astype(np.float16).view(np.uint16).reshape(N, G)
-    packed = pack_indices(idx, b).reshape(N, G, 16 * b)
+    f = field_bits(b)
+    packed = pack_indices(idx, f).reshape(N, G, 16 * f)
     return packed, norms16
 
 
@@ -151,7 +168,7 @@ def cq_reconstruct(packed: np.ndarray, norms16: np.ndarray, b: int, cb28: np.nda
     packed = np.asarray(packed, dtype=np.uint8)
     N, G, _ = packed.shape
     levels = codebook_levels(cb28, b).astype(np.float64)
-    idx = unpack_indices(packed, b, g)                         # [N, G, g]
+    idx = unpack_indices(packed, field_bits(b), g)             # [N, G, g]
     norm = np.asarray(norms16, dtype=np.uint16).view(np.float16).astype(np.float64)
     H = sylvester_hadamard(g) / np.sqrt(float(g))
     unit = levels[idx] / np.sqrt(float(g))                    # codewords on the unit sphere

@@ -2,7 +2,8 @@
 
 The page states the codebooks ``cb2[4] | cb3[8] | cb4[16]`` are fitted offline by the
 Lloyd-Max algorithm on 400,000 Gaussian samples for 200 iterations, and [MMAP] gives
-the 1-bit codebook in closed form, ``{-sqrt(2/pi), +sqrt(2/pi)}``.
+the 1-bit codebook in closed form, ``{-sqrt(2/pi), +sqrt(2/pi)}``, and the ternary one
+(bits = 5) as ``{-c, 0, +c}``, both hard-coded in the engine with no table.
 
 Readings taken where the pages are silent:
 
@@ -22,6 +23,27 @@ import numpy as np
 
 # [MMAP]: the 1-bit codebook is +-sqrt(2/pi), the mean of |N(0,1)|.
 ONE_BIT_LEVEL = math.sqrt(2.0 / math.pi)
+
+
+def ternary_gaussian_level(iters: int = 200) -> float:
+    """``c`` of the ternary codebook ``{-c, 0, +c}`` ([MMAP], bits = 5).
+
+    The page does not give ``c``.  Reading: the three-level Lloyd-Max quantizer of
+    N(0, 1), the same optimality rule as the fitted codebooks, solved on the exact
+    density instead of samples (like the 1-bit value).  Its middle level is 0 by
+    symmetry, its thresholds are the midpoints +-c/2, and the outer level is the mean of
+    N(0, 1) above its threshold:  ``c = phi(c/2) / (1 - Phi(c/2))``.  The iteration from
+    c = 1 contracts (float64) to 1.2240063619...
+    """
+    c = 1.0
+    for _ in range(iters):
+        t = c / 2.0
+        tail = 0.5 * math.erfc(t / math.sqrt(2.0))              # 1 - Phi(t)
+        c = math.exp(-0.5 * t * t) / math.sqrt(2.0 * math.pi) / tail
+    return c
+
+
+TERNARY_LEVEL = ternary_gaussian_level()
 
 
 def gaussian_quantile_init(L: int) -> np.ndarray:

@@ -9,11 +9,12 @@ import numpy as np
 import pytest
 
 from gemm_cq_gemv_gb300.synth import weights
-from oracle import (GROUP, codebook_levels, cq_encode, cq_reconstruct, fwht_butterfly,
-                    pack_indices, sylvester_hadamard, unpack_indices)
+from oracle import (GROUP, TERNARY, TERNARY_LEVEL, codebook_levels, cq_encode, cq_reconstruct,
+                    field_bits, fwht_butterfly, pack_indices, sylvester_hadamard, unpack_indices)
 from util import fitted_cb28, textbook_cb28
 
-TEXTBOOK_MSE = {1: 0.3634, 2: 0.1175, 3: 0.03454, 4: 0.009497}
+# Max 1960, Table I (4 figures); 5 = the ternary code, the table's three-level row
+TEXTBOOK_MSE = {1: 0.3634, 2: 0.1175, 3: 0.03454, 4: 0.009497, 5: 0.1902}
 
 
 def test_pack_examples(golden_dir):
@@ -23,8 +24,9 @@ def test_pack_examples(golden_dir):
         b = c["b"]
         idx = np.zeros(128, dtype=np.int64)
         idx[: len(c["idx_prefix"])] = c["idx_prefix"]
-        packed = pack_indices(idx, b)
-        assert packed.shape == (16 * b,)
+        f = field_bits(b)
+        packed = pack_indices(idx, f)
+        assert packed.shape == (16 * f,)
         want = bytes.fromhex(c["bytes_prefix_hex"])
         assert bytes(packed[: len(want)]) == want
         assert not packed[len(want):].any()
@@ -37,6 +39,19 @@ def test_pack_round_trip(b):
     p = pack_indices(idx, b)
     assert p.shape == (7, 3, 16 * b)
     assert np.array_equal(unpack_indices(p, b), idx)
+
+
+def test_ternary_packs_in_two_bit_fields():
+    rng = np.random.default_rng(11)
+    idx = rng.integers(0, 3, size=(5, 2, 128))
+    W = rng.standard_normal((5, 256)).astype(np.float32)
+    packed, _ = cq_encode(W, TERNARY, textbook_cb28())
+    assert packed.shape == (5, 2, 32)
+    p = pack_indices(idx, field_bits(TERNARY))
+    assert p.shape == (5, 2, 32)
+    assert np.array_equal(unpack_indices(p, 2), idx)
+    # every stored field of an encoding is 0, 1 or 2
+    assert unpack_indices(packed, 2).max() <= 2
 
 
 def test_four_bit_layout_is_low_nibble_even_column():
@@ -54,6 +69,10 @@ def test_codebook_levels_indexing():
     assert np.array_equal(codebook_levels(cb, 4), cb[12:28])
     one = codebook_levels(cb, 1)
     assert one[1] == np.float32(math.sqrt(2 / math.pi)) and one[0] == -one[1]
+    ter = codebook_levels(cb, TERNARY)
+    assert ter.tolist() == [-np.float32(TERNARY_LEVEL), 0.0, np.float32(TERNARY_LEVEL)]
+    with pytest.raises(ValueError):
+        codebook_levels(cb, 6)
 
 
 @pytest.mark.parametrize("cbname", ["textbook", "fitted"])
@@ -68,7 +87,7 @@ def test_encode_known_answers(golden_dir, cbname):
         else:
             W[0, 1] = 3.0
         packed, norms = cq_encode(W, c["b"], cb)
-        idx = unpack_indices(packed, c["b"])[0, 0]
+        idx = unpack_indices(packed, field_bits(c["b"]))[0, 0]
         if "all_idx" in c:
             assert np.all(idx == c["all_idx"]), (c, idx[:8])
         else:
@@ -76,13 +95,13 @@ def test_encode_known_answers(golden_dir, cbname):
         assert format(int(norms[0, 0]), "04x") == c["norm_f16_hex"]
 
 
-@pytest.mark.parametrize("b", [1, 2, 3, 4])
+@pytest.mark.parametrize("b", [1, 2, 3, 4, 5])
 def test_encode_brute_force_nearest(b):
     """Every chosen codeword is a nearest one, recomputed with the dense matrix."""
     cb = fitted_cb28()
     W = weights(8, 4 * 128, seed=77, outliers=True)
     packed, norms = cq_encode(W, b, cb)
-    idx = unpack_indices(packed, b)                           # [8, 4, 128]
+    idx = unpack_indices(packed, field_bits(b))               # [8, 4, 128]
     lv = codebook_levels(cb, b).astype(np.float64)
     Hu = sylvester_hadamard(128)
     for o in range(8):
@@ -107,9 +126,14 @@ def test_zero_group_and_one_bit_tie():
     assert np.all(idx[1, 1, 0::2] == 1)  # +sqrt(2) -> +c
     assert np.all(idx[1, 1, 1::2] == 0)  # exact tie at 0 -> lowest index
     assert np.all(idx[1, 0] == 0)
+    # ternary: the zero coordinates take the zero level (index 1), sqrt(2) takes +c
+    packed, norms = cq_encode(W, TERNARY, cb)
+    idx = unpack_indices(packed, 2)
+    assert not idx[0].any() and not idx[1, 0].any()
+    assert np.all(idx[1, 1, 0::2] == 2) and np.all(idx[1, 1, 1::2] == 1)
 
 
-@pytest.mark.parametrize("b", [1, 2, 3, 4])
+@pytest.mark.parametrize("b", [1, 2, 3, 4, 5])
 def test_reconstruction_error_matches_lloyd_max_mse(b):
     """||w - w_hat||^2 / ||w||^2 = ||v - cb[idx]||^2 / g, i.e. the quantizer's MSE
     (rotated coordinates of a Gaussian group are ~N(0,1) after dividing by the norm).
@@ -125,10 +149,10 @@ def test_reconstruction_error_matches_lloyd_max_mse(b):
 def test_reconstruction_norm_identity_and_fwht_route():
     cb = fitted_cb28()
     W = weights(16, 512, seed=3, outliers=True)
-    for b in (1, 2, 3, 4):
+    for b in (1, 2, 3, 4, 5):
         packed, norms = cq_encode(W, b, cb)
         W_hat = cq_reconstruct(packed, norms, b, cb).reshape(16, 4, 128)
-        idx = unpack_indices(packed, b)
+        idx = unpack_indices(packed, field_bits(b))
         lv = codebook_levels(cb, b).astype(np.float64)
         nrm = norms.view(np.float16).astype(np.float64)
         # ||w_hat_g|| = norm / sqrt(g) * ||cb[idx]||  (H is orthonormal)
@@ -145,5 +169,5 @@ def test_encode_rejects_bad_shapes():
     with pytest.raises(ValueError):
         cq_encode(np.zeros((2, 100), np.float32), 4, cb)
     with pytest.raises(ValueError):
-        cq_encode(np.zeros((2, 128), np.float32), 5, cb)
+        cq_encode(np.zeros((2, 128), np.float32), 6, cb)   # 5 is the ternary code
     assert GROUP == 128

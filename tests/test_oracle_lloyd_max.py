@@ -14,7 +14,8 @@ import numpy as np
 import pytest
 
 from gemm_cq_gemv_gb300.synth import gaussian_samples
-from oracle import ONE_BIT_LEVEL, gaussian_quantile_init, lloyd_max_gaussian_fit
+from oracle import (ONE_BIT_LEVEL, TERNARY_LEVEL, gaussian_quantile_init, lloyd_max_gaussian_fit,
+                    ternary_gaussian_level)
 
 
 def _phi(x):
@@ -128,3 +129,32 @@ def test_committed_codebook_matches_oracle_fit(golden_dir, fitted):
     for b, L in ((2, 4), (3, 8), (4, 16)):
         hexes = [format(int(v), "08x") for v in fits[L].view(np.uint32)]
         assert hexes == cb[f"cb{b}_f32_hex"]
+
+
+def test_ternary_level_matches_textbook(textbook):
+    """The ternary c (mmap page, bits = 5; the page gives no value) is the three-level
+    Lloyd-Max Gaussian level: Max's N = 3 row prints 0, +-1.224, thresholds +-0.6120 and
+    MSE 0.1902 (4 figures)."""
+    row = textbook["three_level"]
+    c = TERNARY_LEVEL
+    assert abs(c - row["levels_positive"][1]) < 5e-4
+    assert abs(c / 2 - row["thresholds_positive"][0]) < 5e-4
+    assert abs(_closed_form_mse([-c, 0.0, c]) - row["mse"]) < 5e-4
+
+
+def test_ternary_level_is_the_three_level_lloyd_solution():
+    """Against the general closed-form Lloyd iteration of this file (free middle level,
+    asymmetric start): it converges to [-c, 0, c] with the oracle's c."""
+    lv = _closed_form_lloyd(3)
+    assert abs(lv[1]) < 1e-12 and abs(lv[0] + lv[2]) < 1e-12
+    assert abs(lv[2] - TERNARY_LEVEL) < 1e-9
+    assert ternary_gaussian_level() == TERNARY_LEVEL
+
+
+def test_ternary_level_minimises_the_mse():
+    """Among symmetric codebooks {-a, 0, a} with midpoint thresholds, a = c has the least
+    mean-squared error (a wrong threshold or centroid rule would move the minimum)."""
+    c = TERNARY_LEVEL
+    best = _closed_form_mse([-c, 0.0, c])
+    for d in (1e-3, -1e-3, 1e-2, -1e-2):
+        assert _closed_form_mse([-(c + d), 0.0, c + d]) > best
