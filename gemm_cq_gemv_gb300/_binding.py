@@ -52,6 +52,7 @@ SIGNATURES = {
     "cq_status_string": (ctypes.c_char_p, [_INT]),
     "cq_last_cuda_error": (_INT, []),
     "cq_abi_version": (_INT, []),
+    "cq_levels": (_INT, [_INT, ctypes.POINTER(cq_codebook), _P]),
     "cq_codebook_fit": (_INT, [_P, _I64, _INT, _INT, _P, _P]),
     "cq_encode": (_INT, [_P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _P]),
     "a8_quantize": (_INT, [_P, _I64, _I64, _P, _P, _P]),
@@ -144,6 +145,15 @@ def cq_abi_version() -> int:
     return lib().cq_abi_version()
 
 
+def cq_levels(b, cb=None):
+    """The 16-entry float32 level table the CQ kernels use for code ``b`` (host only), as a
+    list of 16 Python floats (each exactly a float32 value)."""
+    out = (ctypes.c_float * 16)()
+    c = ctypes.byref(_cbk(cb)) if cb is not None else None
+    _check("cq_levels", lib().cq_levels(b, c, ctypes.cast(out, ctypes.c_void_p)))
+    return list(out)
+
+
 def cq_codebook_fit(samples, L, iters=200, levels_out=None, stream=None):
     """A1: Lloyd-Max levels (float32 [L]) from float64 samples on the GPU."""
     s = _ptr(samples, torch.float64, "samples")
@@ -155,12 +165,23 @@ def cq_codebook_fit(samples, L, iters=200, levels_out=None, stream=None):
     return levels_out
 
 
+# CQ_TERNARY of the C header: bits = 5 selects the fixed codebook {-c, 0, +c}, whose
+# indices are stored in 2-bit fields.
+CQ_TERNARY = 5
+
+
+def cq_field_bits(b: int) -> int:
+    """Bits of one packed index field of code ``b`` (a group holds ``16 * field`` bytes)."""
+    return 2 if b == CQ_TERNARY else b
+
+
 def cq_encode(W, b, cb, packed=None, norms=None, g=128, stream=None):
-    """A2: CQ-encode W [N, K] float32 -> (packed uint8 [N, K/128, 16b], norms int16 [N, K/128])."""
+    """A2: CQ-encode W [N, K] float32 -> (packed uint8 [N, K/128, 16 f], norms int16 [N, K/128]),
+    f = ``cq_field_bits(b)``."""
     N, K = W.shape
     wp = _ptr(W, torch.float32, "W", 2)
     if packed is None:
-        packed = torch.empty((N, K // 128, 16 * b), dtype=torch.uint8, device=W.device)
+        packed = torch.empty((N, K // 128, 16 * cq_field_bits(b)), dtype=torch.uint8, device=W.device)
     if norms is None:
         norms = torch.empty((N, K // 128), dtype=torch.int16, device=W.device)
     c = _cbk(cb)

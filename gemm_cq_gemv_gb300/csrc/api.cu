@@ -41,6 +41,15 @@ extern "C" int cq_last_cuda_error(void) { return cq::g_last_cuda_error; }
 
 extern "C" int cq_abi_version(void) { return CQGEMV_ABI_VERSION; }
 
+extern "C" cq_status cq_levels(int b, const cq_codebook* cbk, float* levels_out) {
+    if (!levels_out || !cq::cq_code_valid(b)) return CQ_ERR_INVALID_ARG;
+    if (!cbk && b != 1 && b != CQ_TERNARY) return CQ_ERR_INVALID_ARG;
+    float lv[16];
+    cq::cq_host_levels(lv, b, cbk);
+    for (int t = 0; t < 16; ++t) levels_out[t] = lv[t];
+    return CQ_OK;
+}
+
 extern "C" cq_status cq_device_error(void* stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -25,6 +25,38 @@ inline cq_status check_launch() {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// CQ codes: b = 1..4 index bits (2^b Lloyd-Max levels), or CQ_TERNARY = 5, the fixed
+// three-level codebook {-c, 0, +c} of the Needle mmap page whose indices 0, 1, 2 sit in
+// 2-bit fields.
+inline bool cq_code_valid(int b) { return (b >= 1 && b <= 4) || b == CQ_TERNARY; }
+// Bits of one packed index field (a group holds 16 * field bytes).
+inline int cq_field_bits(int b) { return b == CQ_TERNARY ? 2 : b; }
+
+// The level table a kernel reads for code b (ascending; unused entries 0).
+//  b = 1: the fixed +-sqrt(2/pi) (Needle mmap page: mean of |N(0,1)|).
+//  b = 5: the fixed {-c, 0, +c}.  The page gives no c; c is the three-level Lloyd-Max
+//         level of N(0,1), the root of c = phi(c/2) / (1 - Phi(c/2)) (thresholds at
+//         +-c/2, the outer level the mean of the tail beyond them).  Entry 3 of the 2-bit
+//         field never occurs in an encoding and reads as 0.
+//  b = 2..4: cb2 | cb3 | cb4 of the caller's table.
+inline void cq_host_levels(float (&lv)[16], int b, const cq_codebook* cbk) {
+    for (int t = 0; t < 16; ++t) lv[t] = 0.0f;
+    if (b == 1) {
+        const float c = 0.797884560802865355879892119868763737f;   // sqrt(2/pi)
+        lv[0] = -c; lv[1] = c;
+        return;
+    }
+    if (b == CQ_TERNARY) {
+        const float c = 1.224006361924961521136180602132438972f;
+        lv[0] = -c; lv[1] = 0.0f; lv[2] = c;
+        return;
+    }
+    const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
+    for (int t = 0; t < (1 << b); ++t) lv[t] = cbk->cb[off + t];
+}
+// Number of levels of code b.
+inline int cq_num_levels(int b) { return b == CQ_TERNARY ? 3 : 1 << b; }
+
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Programmatic dependent launch.  A kernel launched with launch_pdl may start while the

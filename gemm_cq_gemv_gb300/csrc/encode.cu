@@ -82,7 +82,8 @@ struct EncodeParams {
     uint8_t* packed;
     uint16_t* norms;
     int64_t groups;   // N * K / 128
-    int bits;
+    int bits;         // bits of one packed index field
+    int nlev;         // levels searched (2^bits, or 3 for the ternary code)
     float lv[16];
 };
 
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kEncThreads) cq_encode_kernel(const EncodePara
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int64_t warp = ((int64_t)blockIdx.x * kEncThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kEncThreads) >> 5;
-    const int L = 1 << p.bits;
+    const int L = p.nlev;
     for (int64_t gi = warp; gi < p.groups; gi += nwarps) {
         const float4 w4 = *reinterpret_cast<const float4*>(p.W + gi * kGroup + 4 * lane);
         *reinterpret_cast<float4*>(&wbuf[wid][4 * lane]) = w4;
@@ -319,20 +320,14 @@ extern "C" cq_status cq_encode(const float* W, int64_t N, int64_t K, int g, int 
                                const cq_codebook* cbk, uint8_t* packed, uint16_t* norms,
                                void* stream) {
     if (!W || !cbk || !packed || !norms || N < 1 || K < 1) return CQ_ERR_INVALID_ARG;
-    if (g != kGroup || K % kGroup != 0 || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
+    if (g != kGroup || K % kGroup != 0 || !cq_code_valid(b)) return CQ_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned16(packed) || !aligned16(norms)) return CQ_ERR_ALIGNMENT;
     EncodeParams p;
     p.W = W; p.packed = packed; p.norms = norms;
     p.groups = N * (K / kGroup);
-    p.bits = b;
-    for (int t = 0; t < 16; ++t) p.lv[t] = 0.0f;
-    if (b == 1) {
-        const float c = 0.797884560802865355879892119868763737f;  // sqrt(2/pi)
-        p.lv[0] = -c; p.lv[1] = c;
-    } else {
-        const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
-        for (int t = 0; t < (1 << b); ++t) p.lv[t] = cbk->cb[off + t];
-    }
+    p.bits = cq_field_bits(b);
+    p.nlev = cq_num_levels(b);
+    cq_host_levels(p.lv, b, cbk);
     const int grid = blocks_for(p.groups, kEncThreads / 32, sm_count() * 64);
     cq_encode_kernel<<<grid, kEncThreads, 0, as_stream(stream)>>>(p);
     return check_launch();

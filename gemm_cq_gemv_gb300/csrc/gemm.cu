@@ -1001,17 +1001,6 @@ void choose_split(GemmProblem& gp, int tiles_m, int align) {
     }
 }
 
-void fill_levels(float (&lv)[16], int b, const cq_codebook* cbk) {
-    for (int t = 0; t < 16; ++t) lv[t] = 0.0f;
-    if (b == 1) {   // the fixed 1-bit codebook, +-sqrt(2 / pi)
-        const float c = 0.797884560802865355879892119868763737f;
-        lv[0] = -c; lv[1] = c;
-        return;
-    }
-    const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
-    for (int t = 0; t < (1 << b); ++t) lv[t] = cbk->cb[off + t];
-}
-
 }  // namespace
 
 // Failure-detection probe for the pipeline's wait: one thread waits on a barrier phase that
@@ -1181,7 +1170,7 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
         prm.M = (int)M;
         prm.tiles_m = tiles_m;
         prm.total_tiles = tiles;
-        fill_levels(prm.lv, b, cbk);
+        cq_host_levels(prm.lv, b, cbk);
         prm.err = err;
         prm.timeout_ns = 2000000000ull;   // 2 s per wait
         const size_t smem = (size_t)kGemmSmem;
@@ -1197,7 +1186,7 @@ extern "C" cq_status cq_gemm_grouped(const cq_gemm_problem* probs, int count, in
                                      int b, const cq_codebook* cbk, void* workspace,
                                      size_t workspace_bytes, void* stream) {
     if (!probs || count < 1 || !cbk || M < 1 || M > (1 << 30)) return CQ_ERR_INVALID_ARG;
-    if (g != kGroup || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
+    if (g != kGroup || !cq_code_valid(b)) return CQ_ERR_INVALID_ARG;
     if (b != 4) return CQ_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i) {
         const cq_gemm_problem& q = probs[i];
@@ -1246,6 +1235,8 @@ cq_status gemv_tensor(const uint8_t* packed, const uint16_t* norms, int64_t N, i
         case 2: return run_grouped<Decode2Cfg>(&q, 1, B, 2, cbk, workspace, st);
         case 3: return run_grouped<Decode3Cfg>(&q, 1, B, 3, cbk, workspace, st);
         case 4: return run_grouped<DecodeCfg>(&q, 1, B, 4, cbk, workspace, st);
+        // ternary: 2-bit fields, the level table {-c, 0, +c, 0}
+        case CQ_TERNARY: return run_grouped<Decode2Cfg>(&q, 1, B, CQ_TERNARY, cbk, workspace, st);
         default: return CQ_ERR_UNSUPPORTED;
     }
 }

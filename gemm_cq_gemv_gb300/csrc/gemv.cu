@@ -1061,7 +1061,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
                              size_t workspace_bytes, void* stream) {
     if (!packed || !norms || !cbk || !Xq || !scale || !Y || N < 1 || K < 1 || B < 1)
         return CQ_ERR_INVALID_ARG;
-    if (g != kGroup || K % kGroup != 0 || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
+    if (g != kGroup || K % kGroup != 0 || !cq_code_valid(b)) return CQ_ERR_INVALID_ARG;
     if (K > (1 << 24) || N > kMaxGemvRows || B > (1 << 30)) return CQ_ERR_UNSUPPORTED;
     if (!aligned16(packed) || !aligned16(norms) || !aligned16(Xq) || !aligned16(scale) ||
         !aligned16(Y))
@@ -1082,6 +1082,7 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     // a single pass rotates the activations in its prologue; several passes share one
     // rotation kernel's output in the workspace
     const bool fused = B <= tb;
+    const int f = cq_field_bits(b);
     float* xr = reinterpret_cast<float*>(workspace);
     if (!fused) {
         const int64_t groups = B * (K / kGroup);
@@ -1105,9 +1106,9 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     p.N = N; p.K = (int)K; p.nseg = nseg;
     {
         // packed rows as 32-bit words (rows are 16 b-byte groups long, so 16-byte strides)
-        const uint64_t rowbytes = (uint64_t)(K / kGroup) * 16u * (uint64_t)b;
+        const uint64_t rowbytes = (uint64_t)(K / kGroup) * 16u * (uint64_t)f;
         cq_status se = encode_map(&p.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, packed, rowbytes / 4,
-                                  (uint64_t)N, rowbytes, 32u * (uint32_t)b, kUnitRows);
+                                  (uint64_t)N, rowbytes, 32u * (uint32_t)f, kUnitRows);
         if (se != CQ_OK) return se;
         if (K % kSeg == 0) {   // norm rows of 8-group segments: 16-byte strides and boxes
             se = encode_map(&p.nmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, norms, (uint64_t)(K / kGroup),
@@ -1115,20 +1116,13 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
             if (se != CQ_OK) return se;
         }
     }
-    for (int t = 0; t < 16; ++t) p.lv[t] = 0.0f;
-    if (b == 1) {
-        const float c = 0.797884560802865355879892119868763737f;  // sqrt(2/pi)
-        p.lv[0] = -c; p.lv[1] = c;
-    } else {
-        const int off = (b == 2) ? 0 : (b == 3) ? 4 : 12;
-        for (int t = 0; t < (1 << b); ++t) p.lv[t] = cbk->cb[off + t];
-    }
+    cq_host_levels(p.lv, b, cbk);
     p.rg = row_groups(p.nseg);
     for (int64_t t0 = 0; t0 < B; t0 += tb) {
         p.t0 = (int)t0;
         p.ntok = (int)((B - t0) < tb ? (B - t0) : tb);
         cq_status s;
-        switch (b) {
+        switch (f) {   // the ternary code runs the 2-bit kernel on its own level table
             case 1: s = dispatch_cq<1>(p, tb, spw, st); break;
             case 2: s = dispatch_cq<2>(p, tb, spw, st); break;
             case 3: s = dispatch_cq<3>(p, tb, spw, st); break;
@@ -1240,7 +1234,7 @@ extern "C" cq_status cq_gemv_noalloc(const uint8_t* packed, const uint16_t* norm
                                      void* stream) {
     if (!packed || !norms || !cbk || !Xq || !scale || !Y || N < 1 || K < 1 || B < 1)
         return CQ_ERR_INVALID_ARG;
-    if (g != kGroup || K % kGroup != 0 || b < 1 || b > 4) return CQ_ERR_INVALID_ARG;
+    if (g != kGroup || K % kGroup != 0 || !cq_code_valid(b)) return CQ_ERR_INVALID_ARG;
     if (B > (int64_t)CQ_GEMV_NOALLOC_MAX_ELEMS || K > (int64_t)CQ_GEMV_NOALLOC_MAX_ELEMS ||
         B * K > (int64_t)CQ_GEMV_NOALLOC_MAX_ELEMS)
         return CQ_ERR_WORKSPACE;

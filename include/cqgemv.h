@@ -8,8 +8,8 @@
  *    a matmul weight W is stored pre-transposed [out = N, in = K]; each row is cut into
  *    groups of g = 128 along K; each group is rotated by the normalised Walsh-Hadamard
  *    transform, every rotated coordinate is replaced by the index of the nearest
- *    Lloyd-Max Gaussian codeword (b = 1..4 bits), and the group's L2 norm is kept in
- *    FP16.  Reconstruction: w_group = (cb[idx] * norm / sqrt(g)) @ H, H = Hu / sqrt(g)
+ *    Lloyd-Max Gaussian codeword (b = 1..4 bits, or the ternary code b = 5), and the
+ *    group's L2 norm is kept in FP16.  Reconstruction: w_group = (cb[idx] * norm / sqrt(g)) @ H, H = Hu / sqrt(g)
  *    (Hu the Sylvester Hadamard matrix, entries +-1).  Activations are int8 per token.
  *
  *  Q4_0 (Minueza-32M -> KMCU v1 page, §2 "Q4_0 量化" and §3 "行对齐到 32"):
@@ -43,10 +43,17 @@ extern "C" {
 #define CQ_GROUP 128            /* CQ group size along K (Needle .cact page, §一) */
 #define Q4_0_BLOCK 32           /* weights per Q4_0 block (KMCU page, §2)          */
 #define Q4_0_BLOCK_BYTES 18     /* bytes per Q4_0 block  (KMCU page, §2)          */
+/* The ternary CQ code (Needle mmap page, section "mmap 之下张量按偏移直读": bits = 5 selects
+ * the fixed codebook {-c, 0, +c}).  The page gives no c; this library uses the
+ * three-level Lloyd-Max level of N(0,1), c = 1.2240063619... (the root of
+ * c = phi(c/2) / (1 - Phi(c/2))).  Indices 0, 1, 2 (-c, 0, +c) are stored in 2-bit fields
+ * of the LSB-first stream, so a group takes 32 bytes, like b = 2; a field holding 3 never
+ * comes out of cq_encode and reads as level 0. */
+#define CQ_TERNARY 5
 
 typedef enum cq_status {
     CQ_OK = 0,
-    CQ_ERR_INVALID_ARG = 1,     /* bad shape, NULL pointer, g != 128, b not in 1..4, ... */
+    CQ_ERR_INVALID_ARG = 1,     /* bad shape, NULL pointer, g != 128, b not in 1..5, ... */
     CQ_ERR_ALIGNMENT = 2,       /* a pointer is not 16-byte aligned                      */
     CQ_ERR_UNSUPPORTED = 3,     /* no sm_103 device, or a size the kernels do not cover  */
     CQ_ERR_CUDA = 4,            /* CUDA runtime / launch error (see cq_last_cuda_error)  */
@@ -56,8 +63,8 @@ typedef enum cq_status {
 
 /* Codebook table: cb2[4] | cb3[8] | cb4[16], each ascending, in N(0,1) units - the
  * header table of the Needle .cact page, §一.  b = 1 ignores it and uses the analytic
- * +-sqrt(2/pi) of the Needle mmap page.  Passed by pointer to HOST memory; copied by
- * value into kernel parameters. */
+ * +-sqrt(2/pi) of the Needle mmap page; b = CQ_TERNARY ignores it and uses {-c, 0, +c}.
+ * Passed by pointer to HOST memory; copied by value into kernel parameters. */
 typedef struct cq_codebook {
     float cb[28];
 } cq_codebook;
@@ -68,6 +75,14 @@ const char* cq_status_string(cq_status s);
 int cq_last_cuda_error(void);
 /* CQGEMV_ABI_VERSION of the loaded library. */
 int cq_abi_version(void);
+
+/* The level table the CQ kernels use for code b (Needle .cact page, §一: cb2 | cb3 | cb4
+ * indexed by bit width; Needle mmap page: the fixed 1-bit and ternary codebooks), written
+ * to levels_out [16] float32 in HOST memory: levels in index order, unused entries 0
+ * (b = 1: -sqrt(2/pi), +sqrt(2/pi); b = CQ_TERNARY: -c, 0, +c, then 0 for the unused field
+ * value 3; b = 2..4: the b-bit part of *cbk).  Host only: touches no device.
+ * Errors: INVALID_ARG (b not in 1..5, levels_out NULL, cbk NULL for b = 2..4). */
+cq_status cq_levels(int b, const cq_codebook* cbk, float* levels_out);
 
 /* ---- A1: Lloyd-Max Gaussian codebook fit (Needle .cact page, §一: Lloyd-Max on
  * 400k Gaussian samples, 200 iterations).  Levels start at the N(0,1) quantiles
@@ -88,11 +103,12 @@ cq_status cq_codebook_fit(const double* samples, int64_t n, int L, int iters,
  *   (float64; ties -> lowest index; n == 0 -> all indices 0), norm = fp16(n) (one
  *   round-to-nearest-even step from float64).
  *   W       [N][K] float32 ([out, in])
- *   packed  [N][K/128][16*b] uint8: index i of a group in bits [b*i, b*i+b) of the
- *           group's little-endian bytes (b = 4: low nibble = even column)
+ *   packed  [N][K/128][16*f] uint8 with f = b (f = 2 for b = CQ_TERNARY): index i of a
+ *           group in bits [f*i, f*i+f) of the group's little-endian bytes (b = 4: low
+ *           nibble = even column)
  *   norms   [N][K/128] uint16 (IEEE binary16 bits)
  * Bit-exact with the CPU oracle.  Errors: INVALID_ARG (K % 128, g != 128, b not in
- * 1..4, N or K < 1, NULL), ALIGNMENT. */
+ * 1..5, N or K < 1, NULL), ALIGNMENT. */
 cq_status cq_encode(const float* W, int64_t N, int64_t K, int g, int b,
                     const cq_codebook* cbk, uint8_t* packed, uint16_t* norms, void* stream);
 
@@ -128,7 +144,7 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  *   - B <= 2, or N not a multiple of 16: the CUDA-core GEMV, fp32 products and
  *     accumulation; at B <= 2 the rotation happens inside the kernel, otherwise once per
  *     call into `workspace`, shared by every row.
- *   - B >= 3, N a multiple of 16 (any b): the tensor-core pipeline of cq_gemm with
+ *   - B >= 3, N a multiple of 16 (any code): the tensor-core pipeline of cq_gemm with
  *     32-token tiles (4- and 2-bit rows reach shared memory per 64-index stage, 1- and
  *     3-bit rows per 128-index slab).  The weights are decoded once for all tokens; the operands are fp16
  *     (cb * norm, and xr * s_t / 128 in `workspace`), the accumulation fp32.  The
@@ -136,7 +152,8 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  *     max |X[t][k]| <= 65504 (fp16 range).  When the row tiles are too few to occupy the
  *     GPU, K is split in two: Y is zeroed on `stream` and both halves add their fp32
  *     partials into it (two addends on zero: the same sum in either order).
- *   packed, norms  as written by cq_encode
+ *   packed, norms  as written by cq_encode (b = 1..4, or CQ_TERNARY: its 2-bit fields
+ *                  run the 2-bit kernels on the level table {-c, 0, +c, 0})
  *   Xq [B][K] int8, scale [B] float32 (as written by a8_quantize)
  *   Y  [B][N] float32
  *   workspace      device scratch of at least cq_gemv_workspace_bytes(B, K) bytes
@@ -155,7 +172,7 @@ cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64
  *   Y[t][o] = bf16( s_t / 128 * sum_k bf16(xr[t][k]) * bf16(cb[idx[o][k]] * norm[o][k/128]) )
  * with xr = Hu @ Xq per group (rotated once per call into `workspace`, bf16), tcgen05
  * MMA with fp32 accumulation in tensor memory.  Only b = 4 is implemented
- * (CQ_ERR_UNSUPPORTED otherwise).  N must be a multiple of 16 (INVALID_ARG); N and K
+ * (CQ_ERR_UNSUPPORTED for b = 1..3 and CQ_TERNARY).  N must be a multiple of 16 (INVALID_ARG); N and K
  * are limited to 2^24 (INVALID_ARG above), M to 2^30 (INVALID_ARG), and
  * ceil(M / 192) * ceil(N / 128) output tiles to 2^23 (UNSUPPORTED above).
  *   Xq [M][K] int8, scale [M] float32 (a8_quantize), Y [M][N] bf16 (uint16 bits)

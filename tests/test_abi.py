@@ -66,7 +66,8 @@ def test_encode_validation(lib):
     assert lib.cq_encode(A, 4, 100, 128, 4, _cb(), A, A, None) == INV     # K % 128
     assert lib.cq_encode(A, 4, 128, 64, 4, _cb(), A, A, None) == INV      # g != 128
     assert lib.cq_encode(A, 4, 128, 128, 0, _cb(), A, A, None) == INV     # b = 0
-    assert lib.cq_encode(A, 4, 128, 128, 5, _cb(), A, A, None) == INV     # b = 5
+    assert lib.cq_encode(A, 4, 128, 128, 6, _cb(), A, A, None) == INV     # b = 6 (5 is ternary)
+    assert lib.cq_encode(M, 4, 128, 128, 5, _cb(), A, A, None) == ALN     # ternary accepted
     assert lib.cq_encode(None, 4, 128, 128, 4, _cb(), A, A, None) == INV  # NULL
     assert lib.cq_encode(A, 0, 128, 128, 4, _cb(), A, A, None) == INV     # N = 0
     assert lib.cq_encode(M, 4, 128, 128, 4, _cb(), A, A, None) == ALN
@@ -87,6 +88,9 @@ def test_gemv_validation(lib):
     f = lib.cq_gemv
     assert f(A, A, 8, 100, 128, 4, _cb(), A, A, 1, A, A, 1 << 20, None) == INV
     assert f(A, A, 8, 128, 128, 7, _cb(), A, A, 1, A, A, 1 << 20, None) == INV
+    assert f(A, A, 8, 128, 128, 6, _cb(), A, A, 1, A, A, 1 << 20, None) == INV
+    assert f(A, A, 8, 128, 128, 5, _cb(), A, A, 1, M, A, 1 << 20, None) == ALN   # ternary accepted
+    assert lib.cq_gemv_noalloc(A, A, 8, 128, 128, 6, _cb(), A, A, 1, A, None) == INV
     assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 0, A, A, 1 << 20, None) == INV
     assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 1, M, A, 1 << 20, None) == ALN
     assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 2, A, A, 16, None) == WS
@@ -109,6 +113,8 @@ def test_gemm_validation(lib):
     f = lib.cq_gemm
     big = 1 << 30
     assert f(A, A, 256, 512, 128, 3, _cb(), A, A, 256, A, A, big, None) == UNS   # only b = 4
+    assert f(A, A, 256, 512, 128, 5, _cb(), A, A, 256, A, A, big, None) == UNS   # ternary
+    assert f(A, A, 256, 512, 128, 6, _cb(), A, A, 256, A, A, big, None) == INV
     assert f(A, A, 250, 512, 128, 4, _cb(), A, A, 256, A, A, big, None) == INV   # N % 16
     assert f(A, A, 256, 500, 128, 4, _cb(), A, A, 256, A, A, big, None) == INV   # K % 128
     assert f(A, A, 256, 512, 128, 4, _cb(), A, A, 0, A, A, big, None) == INV     # M = 0
@@ -153,3 +159,23 @@ def test_a8_groups_validation(lib):
     assert lib.a8_quantize_groups(M, 4, 96, 32, A, A, None) == ALN
     assert lib.a8_fake_quant_groups(A, 4, 96, 32, None, None) == INV
     assert lib.a8_fake_quant_groups(A, 4, 96, 32, M, None) == ALN
+
+
+def test_kernel_level_tables_match_oracle(lib):
+    """The level table every CQ kernel receives (cq_levels, host only) equals the oracle's
+    codebook_levels bit for bit for every code, including the fixed 1-bit +-sqrt(2/pi) and
+    the ternary {-c, 0, +c} of the Needle mmap page (c: the three-level Lloyd-Max level)."""
+    import numpy as np
+    import oracle
+    from util import fitted_cb28
+    cb = fitted_cb28()
+    for b in (1, 2, 3, 4, 5):
+        want = oracle.codebook_levels(cb, b)
+        got = np.array(cq.cq_levels(b, cb), dtype=np.float32)
+        L = want.shape[0]
+        assert got[:L].view(np.uint32).tolist() == want.view(np.uint32).tolist(), b
+        assert not got[L:].any(), b
+    assert cq.cq_levels(5) == cq.cq_levels(5, cb)          # the fixed codes ignore the table
+    assert lib.cq_levels(6, None, A) == 1
+    assert lib.cq_levels(2, None, A) == 1                   # b = 2..4 need the caller's table
+    assert lib.cq_levels(1, None, None) == 1
