@@ -63,6 +63,8 @@ SIGNATURES = {
                        _P, _P, _SZ, _P]),
     "cq_gemv_noalloc": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P,
                                _P, _I64, _P, _P]),
+    "cq_gemv_lut": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P,
+                           _I64, _P, _P]),
     "cq_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "cq_gemm": (_INT, [_P, _P, _I64, _I64, _INT, _INT, ctypes.POINTER(cq_codebook), _P, _P, _I64,
                        _P, _P, _SZ, _P]),
@@ -247,6 +249,20 @@ def cq_gemv(packed, norms, N, K, b, cb, Xq, scale, Y=None, workspace=None, g=128
                                     B, _ptr(Y, torch.float32, "Y"),
                                     _ptr(workspace, torch.uint8, "workspace"),
                                     workspace.numel(), _stream(stream)))
+    return Y
+
+
+def cq_gemv_lut(packed, norms, N, K, b, cb, Xq, scale, Y=None, g=128, stream=None):
+    """A4+A5 by table lookup (b = 1, 2 or ternary): Y [B, N] float32, no workspace."""
+    B = Xq.shape[0]
+    if Y is None:
+        Y = torch.empty((B, N), dtype=torch.float32, device=Xq.device)
+    c = _cbk(cb)
+    _check("cq_gemv_lut", lib().cq_gemv_lut(_ptr(packed, torch.uint8, "packed"),
+                                            _ptr(norms, torch.int16, "norms"), N, K, g, b,
+                                            ctypes.byref(c), _ptr(Xq, torch.int8, "Xq"),
+                                            _ptr(scale, torch.float32, "scale"), B,
+                                            _ptr(Y, torch.float32, "Y"), _stream(stream)))
     return Y
 
 

@@ -167,6 +167,25 @@ cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64
                   const float* scale, int64_t B, float* Y, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* ---- A4 + A5 by table lookup, for narrow codes (b = 1, 2 or CQ_TERNARY): the 1-bit
+ * lookup-table kernel of the smolmaxxing page (kernel table, Four-Russians / T-MAC style:
+ * a 16-entry table per 4 activations) carried over to this format.  The same Y as cq_gemv:
+ *   Y[t][o] = s_t * sum_j (norm[o][j] / 128) * sum_i cb[idx[o][j][i]] * xr[t][128 j + i].
+ * For each token, every CTA rotates the activations (xr = Hu @ Xq per group) into shared
+ * memory and tabulates, for every 4-bit nibble of the packed stream (four 1-bit or two
+ * 2-bit indices), the 16 possible partial sums cb * xr over the positions it covers; a row
+ * then costs one lookup and one fp32 add per nibble.  Sums in fp32 in a fixed order
+ * (deterministic); the result is within 1e-3 of the exact product like cq_gemv's.
+ *   packed, norms  as written by cq_encode for b = 1, 2 or CQ_TERNARY
+ *   Xq [B][K] int8, scale [B] float32, Y [B][N] float32; all 16-byte aligned
+ * No workspace.  Each token is one launch that reads the weights once (meant for batches
+ * of 1 or 2).  K is limited to 2^24, N to 2^40, B to 2^30.
+ * Errors: INVALID_ARG (NULL, g != 128, K % 128, b not in 1..5), UNSUPPORTED (b = 3 or 4,
+ * sizes above the limits), ALIGNMENT, CUDA. */
+cq_status cq_gemv_lut(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K, int g,
+                      int b, const cq_codebook* cbk, const int8_t* Xq, const float* scale,
+                      int64_t B, float* Y, void* stream);
+
 /* ---- A4 + A6: prefill GEMM on the tensor cores (Needle .cact page, §三: prefill is a
  * GEMM over the same [out, in] rows; §一: reconstruction formula).  Computes
  *   Y[t][o] = bf16( s_t / 128 * sum_k bf16(xr[t][k]) * bf16(cb[idx[o][k]] * norm[o][k/128]) )

@@ -102,6 +102,21 @@ def test_gemv_validation(lib):
     assert lib.q4_0_gemv(A, 1, 32, A, (1 << 30) + 1, A, None) == UNS
 
 
+def test_gemv_lut_validation(lib):
+    INV, ALN, UNS = 1, 2, 3
+    f = lib.cq_gemv_lut
+    assert f(A, A, 8, 128, 128, 4, _cb(), A, A, 1, A, None) == UNS    # 4-bit: use cq_gemv
+    assert f(A, A, 8, 128, 128, 3, _cb(), A, A, 1, A, None) == UNS
+    assert f(A, A, 8, 128, 128, 6, _cb(), A, A, 1, A, None) == INV
+    assert f(A, A, 8, 100, 128, 1, _cb(), A, A, 1, A, None) == INV    # K % 128
+    assert f(A, A, 8, 128, 64, 1, _cb(), A, A, 1, A, None) == INV     # g
+    assert f(A, A, 0, 128, 128, 1, _cb(), A, A, 1, A, None) == INV    # N = 0
+    assert f(A, A, 8, 128, 128, 2, None, A, A, 1, A, None) == INV     # no codebook
+    assert f(A, None, 8, 128, 128, 1, _cb(), A, A, 1, A, None) == INV
+    assert f(A, A, 8, 128, 128, 1, _cb(), A, A, 1, M, None) == ALN
+    assert f(A, A, 8, 1 << 25, 128, 5, _cb(), A, A, 1, A, None) == UNS   # K above 2^24
+
+
 def test_codebook_fit_validation(lib):
     assert lib.cq_codebook_fit(A, 100, 1, 10, A, None) == 1
     assert lib.cq_codebook_fit(A, 100, 17, 10, A, None) == 1
