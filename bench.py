@@ -15,7 +15,9 @@ norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step tim
 The line also reports, beside the headline, the grouped prefill GEMM of the 20-layer
 model (``prefill``, TFLOP/s) and decode batches of 8 and 32 tokens on the tensor cores
 (``batched``: ``cq_gemv`` at 4 bits and ``q4_0_gemm``, GB/s of weights, each call timed
-alone after an L2 flush).
+alone after an L2 flush) and batch-1 decode of 1-bit, 2-bit and ternary rows through
+``cq_gemv`` and the table-lookup ``cq_gemv_lut`` (``narrow``, timed in a child process
+after everything else).
 
 ``--impl reference`` times the CPU oracle as it stands on a bounded sample of the same
 workload.  ``--gpus N`` (under torchrun) runs N independent replicas, one per GPU:
@@ -341,6 +343,84 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 3
     return out
 
 
+def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
+    """Batch-1 decode of 1-bit, 2-bit and ternary rows on the large shapes: ``cq_gemv``
+    against the table-lookup ``cq_gemv_lut``, each call timed alone after an L2 flush, plus
+    the largest relative difference between the two outputs (both compute the same product)."""
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def one(fn):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    out = {"workload": "large-shape decode, batch 1, 1-bit / 2-bit / ternary CQ rows",
+           "timing": "per call, CUDA events, L2 flushed before each call",
+           "unit": "us per call; GB/s of algorithmic bytes over the four matrices"}
+    for b, name in ((1, "b1"), (2, "b2"), (cq.CQ_TERNARY, "ternary")):
+        res = {"cq_gemv": {"us": {}, "ms": 0.0}, "cq_gemv_lut": {"us": {}, "ms": 0.0}}
+        nbytes = 0
+        diff = 0.0
+        for i, m in enumerate(synth.LARGE):
+            g = torch.Generator(device=dev)
+            g.manual_seed(synth.weight_seed(4, i))
+            W = torch.randn((m.N, m.K), device=dev, generator=g) * 0.02
+            packed, norms = cq.cq_encode(W, b, cb)
+            del W
+            gx = torch.Generator(device=dev)
+            gx.manual_seed(synth.activation_seed(4, 1) + i)
+            Xq, sc = cq.a8_quantize(torch.randn((1, m.K), device=dev, generator=gx))
+            ws = torch.empty((cq.cq_gemv_workspace_bytes(1, m.K),), dtype=torch.uint8, device=dev)
+            Yg = torch.empty((1, m.N), dtype=torch.float32, device=dev)
+            Yl = torch.empty((1, m.N), dtype=torch.float32, device=dev)
+            for key, fn in (("cq_gemv", lambda: cq.cq_gemv(packed, norms, m.N, m.K, b, cb, Xq, sc, Y=Yg,
+                                                           workspace=ws)),
+                            ("cq_gemv_lut", lambda: cq.cq_gemv_lut(packed, norms, m.N, m.K, b, cb, Xq, sc,
+                                                                   Y=Yl))):
+                ms = one(fn)
+                res[key]["us"][m.name] = round(ms * 1e3, 1)
+                res[key]["ms"] += ms
+            nbytes += packed.numel() + 2 * norms.numel() + m.K + 4 + 4 * m.N
+            den = float(Yg.abs().max())
+            diff = max(diff, float((Yl - Yg).abs().max()) / (den if den > 0 else 1.0))
+            del packed, norms
+            torch.cuda.empty_cache()
+        out[name] = {k: {"us": v["us"], "GBps": round(nbytes / (v["ms"] * 1e-3) / 1e9, 1)}
+                     for k, v in res.items()}
+        out[name]["max_rel_diff"] = float(f"{diff:.3g}")
+    cq.cq_device_error()
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def narrow_child(args, local_rank):
+    """Runs narrow_report in a child process, so that a failure of the newer kernel can
+    only cost this entry, never the rest of the line.  The child is a single-rank run on
+    this process's GPU (no process group)."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--narrow-only", "--warmup", str(args.warmup)]
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK=str(local_rank))
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env)
+    except subprocess.TimeoutExpired:
+        return {"error": "timed out after 600 s"}
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    if r.returncode != 0 or not lines:
+        tail = (r.stderr or r.stdout).strip().splitlines()[-3:]
+        return {"error": f"exit {r.returncode}: " + " | ".join(tail)}
+    return json.loads(lines[-1])
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
     import gemm_cq_gemv_gb300 as cq
@@ -353,6 +433,9 @@ def gpu_arm(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     cb = cq.make_codebook(load_codebook())
+    if args.narrow_only:
+        print(json.dumps(narrow_report(dev, cb, torch, cq, synth, 10, args.warmup)), flush=True)
+        return
     if args.prefill_only:
         pf = build_prefill(dev, cb, torch, cq, synth, args.prefill_m)
         ms = time_prefill(pf, cb, cq, torch, args.steps, args.warmup)
@@ -506,6 +589,8 @@ def gpu_arm(args, rank, world, local_rank):
                                              args.warmup, peaks, kind)
         if not args.no_batched:
             line["batched"] = batched_report(mats, cb, torch, cq, synth, dev, 10, 3, kinds=kinds)
+        if not args.no_narrow and world == 1:
+            line["narrow"] = narrow_child(args, local_rank)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
         print(json.dumps(line), flush=True)
@@ -614,6 +699,10 @@ def main(argv=None):
     ap.add_argument("--batched-only", action="store_true",
                     help="time only the tensor-core decode batch of --batch tokens (profiling runs)")
     ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--no-narrow", action="store_true",
+                    help="skip the 1-bit / 2-bit / ternary decode report (cq_gemv vs cq_gemv_lut)")
+    ap.add_argument("--narrow-only", action="store_true",
+                    help="print only that report (the child process the full run starts)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")
