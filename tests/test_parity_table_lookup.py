@@ -7,6 +7,8 @@ tables of partial sums over 4 activations).  Tolerance: max relative error 1e-3 
 output vector, as for cq_gemv.  The oracle encodes its own copy of the weights.
 """
 
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -27,9 +29,16 @@ def _gpu():
     require_gpu()
 
 
+@functools.lru_cache(maxsize=1)
+def _weights(N, K, seed, outliers):
+    """Seeded weights, kept for the next case of the same shape (the large shape takes
+    ~20 s to draw on the host)."""
+    return synth.weights(N, K, seed=seed, outliers=outliers)
+
+
 def _case(N, K, b, B, wseed, xseed, rows=None, outliers=True):
     cb = fitted_cb28()
-    W = synth.weights(N, K, seed=wseed, outliers=outliers)
+    W = _weights(N, K, wseed, outliers)
     X = synth.activations(B, K, seed=xseed)
     packed, norms = cq.cq_encode(to_dev(W), b, cb)
     q, s = cq.a8_quantize(to_dev(X))

@@ -9,6 +9,8 @@ of >= 3 tokens) are within max relative error 1e-3 of the float64 oracle, per ou
 vector.  The oracle encodes its own copy of the weights.
 """
 
+import functools
+
 import numpy as np
 import pytest
 
@@ -63,9 +65,16 @@ def test_ternary_encode_special_groups():
     assert np.all(idx[3, 1, 1::2] == 1)
 
 
+@functools.lru_cache(maxsize=1)
+def _weights(N, K, seed, outliers):
+    """Seeded weights, kept for the next case of the same shape (the large shape takes
+    ~20 s to draw on the host)."""
+    return synth.weights(N, K, seed=seed, outliers=outliers)
+
+
 def _case(N, K, B, wseed, xseed, outliers=True, rows=None):
     cb = fitted_cb28()
-    W = synth.weights(N, K, seed=wseed, outliers=outliers)
+    W = _weights(N, K, wseed, outliers)
     X = synth.activations(B, K, seed=xseed)
     packed, norms = cq.cq_encode(to_dev(W), TER, cb)
     q, s = cq.a8_quantize(to_dev(X))
