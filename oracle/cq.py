@@ -33,7 +33,8 @@ Readings taken (the pages are silent or inconsistent):
   * ternary (bits = 5): ``c`` is the three-level Lloyd-Max Gaussian level (see
     ``lloyd_max.ternary_gaussian_level``), the levels ``[-c, 0, +c]`` take indices
     0, 1, 2, and an index is stored in a 2-bit field of the same LSB-first stream (the
-    smallest field that holds three values), so a group is 32 bytes.
+    smallest field that holds three values, and the ternary layout the smolmaxxing page
+    chooses over base-3 packing for speed, kernel table E76/E77), so a group is 32 bytes.
 """
 
 import numpy as np
