@@ -15,7 +15,9 @@ norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step tim
 The line also reports, beside the headline, the grouped prefill GEMM of the 20-layer
 model (``prefill``, TFLOP/s) and decode batches of 8 and 32 tokens on the tensor cores
 (``batched``: ``cq_gemv`` at 4 bits and ``q4_0_gemm``, GB/s of weights, each call timed
-alone after an L2 flush) and batch-1 decode of 1-bit, 2-bit and ternary rows through
+alone after an L2 flush), the two small workloads (``small``: CQ-W4A8 512 x 512 and one
+Minueza Q4_0 layer, each as single-call latency and as streamed GB/s over weight copies
+spanning 4x the L2) and batch-1 decode of 1-bit, 2-bit and ternary rows through
 ``cq_gemv`` and the table-lookup ``cq_gemv_lut`` (``narrow``, timed in a child process
 after everything else).
 
@@ -343,6 +345,133 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 3
     return out
 
 
+def _capture(torch, fn):
+    """``fn``'s launches captured as a CUDA graph (replayed on the current stream)."""
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def small_report(dev, cb, torch, cq, synth, steps, warmup):
+    """The two small workloads, each reported twice: the latency of one call (one Minueza
+    layer: its 8 Q4_0 GEMVs) replayed as a CUDA graph after an L2 flush, and the streamed
+    throughput of back-to-back calls over distinct copies of the weights spanning 4x the
+    L2 (one graph of all copies).  Both use the batch-1 GEMVs of the decode step."""
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+
+    def latency(fn):
+        g = _capture(torch, fn)
+        ts = []
+        for i in range(warmup + steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= warmup:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def streamed(fn, reps=3):
+        g = _capture(torch, fn)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def copies_of(t, n):
+        """``n`` copies of ``t`` in one buffer, each starting at a 256-byte boundary."""
+        per = t.numel() * t.element_size()
+        stride = -(-per // 256) * 256
+        flat = torch.empty((n * stride,), dtype=torch.uint8, device=dev)
+        src = t.contiguous().view(torch.uint8).reshape(-1)
+        views = []
+        for c in range(n):
+            v = flat[c * stride:c * stride + per]
+            v.copy_(src)
+            views.append(v.view(t.dtype).view(t.shape))
+        return views
+
+    def gen(shape, seed):
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        return torch.randn(shape, device=dev, generator=g)
+
+    out = {"timing": "latency: one call (one layer) as a CUDA graph after an L2 flush, median; "
+                     "streamed: one graph over distinct weight copies spanning 4x L2",
+           "l2_bytes": l2}
+    # CQ-W4A8 512 x 512, batch 1
+    N = K = 512
+    packed, norms = cq.cq_encode(gen((N, K), synth.weight_seed(0, 0)) * 0.02, 4, cb)
+    Xq, sc = cq.a8_quantize(gen((1, K), synth.activation_seed(0, 1)))
+    ws = torch.empty((cq.cq_gemv_workspace_bytes(1, K),), dtype=torch.uint8, device=dev)
+    Y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    nbytes = packed.numel() + 2 * norms.numel() + K + 4 + 4 * N
+    us = latency(lambda: cq.cq_gemv(packed, norms, N, K, 4, cb, Xq, sc, Y=Y, workspace=ws)) * 1e3
+    copies = -(-4 * l2 // nbytes)
+    P = copies_of(packed, copies)
+    Q = copies_of(norms, copies)
+
+    def stream_cq():
+        for c in range(copies):
+            cq.cq_gemv(P[c], Q[c], N, K, 4, cb, Xq, sc, Y=Y, workspace=ws)
+
+    ms = streamed(stream_cq)
+    out["cq_w4a8_512x512"] = {"latency_us": round(us, 1), "bytes_per_call": nbytes,
+                              "copies": copies, "streamed_us_per_call": round(ms * 1e3 / copies, 2),
+                              "streamed_GBps": round(copies * nbytes / (ms * 1e-3) / 1e9, 1),
+                              "streamed_Gweights_per_s": round(copies * N * K / (ms * 1e-3) / 1e9, 2)}
+    del P, Q, packed, norms
+    # one Minueza layer in Q4_0 (8 matrices with the tied lm_head), batch 1
+    layer = []
+    xs = {}
+    for i, m in enumerate(synth.MINUEZA_LAYER):
+        blocks = cq.q4_0_quantize(gen((m.N, m.K), synth.weight_seed(1, i)) * 0.02)
+        if m.K not in xs:
+            xs[m.K] = gen((1, m.K), synth.activation_seed(1, 1) + m.K)
+        layer.append((m, blocks, torch.empty((1, m.N), dtype=torch.float32, device=dev)))
+    lbytes = sum(b.numel() + 4 * m.K + 4 * m.N for m, b, _ in layer)
+    lweights = sum(m.N * m.K for m, _, _ in layer)
+
+    def one_layer():
+        for m, b, y in layer:
+            cq.q4_0_gemv(b, m.N, m.K, xs[m.K], Y=y)
+
+    us = latency(one_layer) * 1e3
+    copies = -(-4 * l2 // lbytes)
+    reps = [(m, copies_of(b, copies), y) for m, b, y in layer]
+
+    def stream_layers():
+        for c in range(copies):
+            for m, b, y in reps:
+                cq.q4_0_gemv(b[c], m.N, m.K, xs[m.K], Y=y)
+
+    ms = streamed(stream_layers)
+    out["minueza_q4_0_layer"] = {"latency_us": round(us, 1), "launches": len(layer),
+                                 "bytes_per_layer": lbytes, "copies": copies,
+                                 "streamed_us_per_layer": round(ms * 1e3 / copies, 2),
+                                 "streamed_GBps": round(copies * lbytes / (ms * 1e-3) / 1e9, 1),
+                                 "streamed_Gweights_per_s": round(copies * lweights / (ms * 1e-3) / 1e9, 2)}
+    cq.cq_device_error()
+    del reps, layer, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
     """Batch-1 decode of 1-bit, 2-bit and ternary rows on the large shapes: ``cq_gemv``
     against the table-lookup ``cq_gemv_lut``, each call timed alone after an L2 flush, plus
@@ -589,6 +718,11 @@ def gpu_arm(args, rank, world, local_rank):
                                              args.warmup, peaks, kind)
         if not args.no_batched:
             line["batched"] = batched_report(mats, cb, torch, cq, synth, dev, 10, 3, kinds=kinds)
+        if not args.no_small:
+            try:
+                line["small"] = small_report(dev, cb, torch, cq, synth, 10, 3)
+            except Exception as e:   # report, never lose the line
+                line["small"] = {"error": f"{type(e).__name__}: {e}"[:300]}
         if not args.no_narrow and world == 1:
             line["narrow"] = narrow_child(args, local_rank)
         if not args.no_cpu_baseline:
@@ -699,6 +833,8 @@ def main(argv=None):
     ap.add_argument("--batched-only", action="store_true",
                     help="time only the tensor-core decode batch of --batch tokens (profiling runs)")
     ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--no-small", action="store_true",
+                    help="skip the small-workload report (CQ 512x512, one Minueza Q4_0 layer)")
     ap.add_argument("--no-narrow", action="store_true",
                     help="skip the 1-bit / 2-bit / ternary decode report (cq_gemv vs cq_gemv_lut)")
     ap.add_argument("--narrow-only", action="store_true",
