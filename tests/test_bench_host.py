@@ -1,0 +1,161 @@
+"""Host logic of bench.py, without a GPU.
+
+The bench runs its GPU reports only on a GPU, where a slip in their Python would cost the
+whole line; these tests drive the reporting functions through stand-ins for the CUDA
+calls (events, graphs and the library's entry points) to check their shapes, the buffers
+they hand to the library and the JSON they produce.  The reference arm (the CPU oracle)
+runs for real on a small sample.
+"""
+
+import contextlib
+import io
+import json
+import os
+import sys
+import types
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import gemm_cq_gemv_gb300 as cqlib  # noqa: E402
+from gemm_cq_gemv_gb300 import synth  # noqa: E402
+
+
+class _Event:
+    def __init__(self, enable_timing=True):
+        pass
+
+    def record(self, *a):
+        pass
+
+    def elapsed_time(self, other):
+        return 0.25
+
+
+class _Graph:
+    def __init__(self):
+        self.fn = None
+
+    def replay(self):
+        self.fn()
+
+
+def _fake_torch():
+    @contextlib.contextmanager
+    def graph(g, stream=None):
+        yield
+
+    cuda = types.SimpleNamespace(
+        Event=_Event, synchronize=lambda: None, empty_cache=lambda: None,
+        Stream=lambda *a, **k: types.SimpleNamespace(wait_stream=lambda o: None),
+        current_stream=lambda: None, CUDAGraph=_Graph, graph=graph,
+        get_device_properties=lambda d: types.SimpleNamespace(L2_cache_size=4 << 20))
+    ft = types.SimpleNamespace(**{k: getattr(torch, k) for k in
+                                  ("empty", "uint8", "float32", "randn", "Generator", "int8", "int16")})
+    ft.cuda = cuda
+    return ft
+
+
+class _FakeLib:
+    """Stand-in for the library's entry points: checks what the bench hands over."""
+
+    CQ_TERNARY = cqlib.CQ_TERNARY
+    cq_gemv_workspace_bytes = staticmethod(cqlib.cq_gemv_workspace_bytes)
+
+    def __init__(self):
+        self.calls = {}
+
+    def _count(self, name):
+        self.calls[name] = self.calls.get(name, 0) + 1
+
+    @staticmethod
+    def _ok(t):
+        assert t.is_contiguous() and t.data_ptr() % 16 == 0
+
+    def cq_encode(self, W, b, cb):
+        N, K = W.shape
+        f = cqlib.cq_field_bits(b)
+        return (torch.zeros((N, K // 128, 16 * f), dtype=torch.uint8),
+                torch.zeros((N, K // 128), dtype=torch.int16))
+
+    def a8_quantize(self, X):
+        return torch.zeros(X.shape, dtype=torch.int8), torch.ones(X.shape[0])
+
+    def cq_gemv(self, packed, norms, N, K, b, cb, Xq, s, Y=None, workspace=None):
+        self._ok(packed), self._ok(norms)
+        assert packed.shape == (N, K // 128, 16 * cqlib.cq_field_bits(b))
+        assert Y.shape == (Xq.shape[0], N)
+        Y.fill_(1.0)
+        self._count("cq_gemv")
+
+    def cq_gemv_lut(self, packed, norms, N, K, b, cb, Xq, s, Y=None):
+        self._ok(packed), self._ok(norms)
+        assert b in (1, 2, cqlib.CQ_TERNARY)
+        Y.fill_(1.0)
+        self._count("cq_gemv_lut")
+
+    def q4_0_quantize(self, W):
+        N, K = W.shape
+        return torch.zeros((N, -(-K // 32) * 18), dtype=torch.uint8)
+
+    def q4_0_gemv(self, blocks, N, K, X, Y=None):
+        self._ok(blocks)
+        assert blocks.shape == (N, -(-K // 32) * 18) and X.shape[1] == K
+        self._count("q4_0_gemv")
+
+    def cq_device_error(self):
+        pass
+
+
+def test_small_report_shapes_and_copies(monkeypatch):
+    def capture(torch_, fn):
+        g = _Graph()
+        g.fn = fn
+        fn()
+        return g
+
+    monkeypatch.setattr(bench, "_capture", capture)
+    lib = _FakeLib()
+    out = bench.small_report("cpu", None, _fake_torch(), lib, synth, 2, 1)
+    a, b = out["cq_w4a8_512x512"], out["minueza_q4_0_layer"]
+    assert a["bytes_per_call"] == 512 * 512 // 2 + 2 * 512 * 4 + 512 + 4 + 4 * 512
+    assert a["copies"] * a["bytes_per_call"] >= 4 * out["l2_bytes"]
+    assert b["launches"] == 8 and b["copies"] * b["bytes_per_layer"] >= 4 * out["l2_bytes"]
+    assert b["bytes_per_layer"] >= 6_499_800            # the layer's Q4_0 blocks alone
+    # latency: capture + (warmup + steps) replays; streamed: capture + 1 + 3 replays
+    assert lib.calls["cq_gemv"] == 1 + 3 + (1 + 1 + 3) * a["copies"]
+    assert lib.calls["q4_0_gemv"] == 8 * (1 + 3) + 8 * (1 + 1 + 3) * b["copies"]
+    json.dumps(out)
+
+
+def test_narrow_report_covers_every_code_and_shape():
+    lib = _FakeLib()
+    small = tuple(types.SimpleNamespace(name=m.name, N=m.N // 128, K=m.K) for m in synth.LARGE)
+    fs = types.SimpleNamespace(LARGE=small, weight_seed=synth.weight_seed,
+                               activation_seed=synth.activation_seed)
+    out = bench.narrow_report("cpu", None, _fake_torch(), lib, fs, 2, 3)
+    for key in ("b1", "b2", "ternary"):
+        assert set(out[key]["cq_gemv"]["us"]) == {m.name for m in small}
+        assert out[key]["cq_gemv_lut"]["GBps"] > 0
+        assert out[key]["max_rel_diff"] == 0.0
+    assert lib.calls["cq_gemv"] == lib.calls["cq_gemv_lut"] == 3 * 4 * (3 + 2)
+    json.dumps(out)
+
+
+def test_reference_arm_line():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--cpu-rows", "4"])
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["metric"] == bench.METRIC and line["higher_is_better"] is True
+
+
+def test_warmup_below_three_is_refused():
+    with pytest.raises(SystemExit):
+        bench.main(["--steps", "1", "--warmup", "2"])
