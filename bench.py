@@ -726,7 +726,7 @@ def gpu_arm(args, rank, world, local_rank):
         if not args.no_narrow and world == 1:
             line["narrow"] = narrow_child(args, local_rank)
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+            line["cpu_baseline"] = cpu_baseline_report(args.cpu_rows)
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -758,7 +758,19 @@ def oracle_state(rows, cb, synth, oracle):
     return state
 
 
-def cpu_baseline(rows):
+_BLAS_THREAD_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def blas_threads():
+    """Threads NumPy's BLAS runs with: the pinning variable if one is set, else every core
+    (the OpenBLAS default)."""
+    for v in _BLAS_THREAD_VARS:
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+def cpu_baseline(rows, seconds=10.0):
     import oracle
     from gemm_cq_gemv_gb300 import synth
     cb = load_codebook()
@@ -767,14 +779,30 @@ def cpu_baseline(rows):
     # repeat the sample for about ten seconds of CPU work
     reps, nbytes = 0, 0
     a = time.perf_counter()
-    while reps == 0 or time.perf_counter() - a < 10.0:
+    while reps == 0 or time.perf_counter() - a < seconds:
         nbytes += oracle_sample_step(rows, cb, synth, oracle, state)
         reps += 1
     dt = time.perf_counter() - a
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(),
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
             "kind": "oracle",
             "sample": f"{reps} x {rows} rows of each large matrix, CQ-W4A8 and Q4_0, batch 1 "
                       f"(float64 reconstruction + product), {dt:.1f} s"}
+
+
+def cpu_baseline_report(rows):
+    """The oracle timed twice: with BLAS on every core (this process) and pinned to one
+    thread (a child process, since BLAS reads its thread count when NumPy loads)."""
+    out = cpu_baseline(rows)
+    env = dict(os.environ, **{v: "1" for v in _BLAS_THREAD_VARS})
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--cpu-rows", str(rows)]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env)
+        lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+        out["one_thread"] = (json.loads(lines[-1]) if r.returncode == 0 and lines
+                             else {"error": f"exit {r.returncode}"})
+    except subprocess.TimeoutExpired:
+        out["one_thread"] = {"error": "timed out after 300 s"}
+    return out
 
 
 def reference_arm(args, rank, world):
@@ -802,7 +830,7 @@ def reference_arm(args, rank, world):
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
         "config": {"workload": WORKLOAD, "batch": 1, "group": 128, "cq_bits": 4,
                    "parallelism": "cpu oracle, rank 0"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": blas_threads(),
                          "kind": "oracle",
                          "sample": f"{rows} rows of each large matrix per step, both formats"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -820,6 +848,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows", type=int, default=256,
                     help="rows per matrix in the oracle sample (CPU baseline / reference arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-only", action="store_true",
+                    help="print only the CPU oracle timing (the one-thread child of a full run)")
     ap.add_argument("--no-e2e", action="store_true",
                     help="time the device step only and print a short line (profiling runs)")
     ap.add_argument("--case", nargs="*", default=None,
@@ -845,7 +875,9 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.cpu_baseline_only:
+        print(json.dumps(cpu_baseline(args.cpu_rows)), flush=True)
+    elif args.impl == "reference":
         reference_arm(args, rank, world)
     else:
         gpu_arm(args, rank, world, local_rank)

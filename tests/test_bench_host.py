@@ -159,3 +159,20 @@ def test_reference_arm_line():
 def test_warmup_below_three_is_refused():
     with pytest.raises(SystemExit):
         bench.main(["--steps", "1", "--warmup", "2"])
+
+
+def test_blas_thread_count(monkeypatch):
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        monkeypatch.delenv(v, raising=False)
+    assert bench.blas_threads() == os.cpu_count()
+    monkeypatch.setenv("OMP_NUM_THREADS", "1")
+    assert bench.blas_threads() == 1
+
+
+def test_cpu_baseline_only_entry(monkeypatch):
+    """The one-thread child of a full run prints exactly the oracle timing as JSON."""
+    monkeypatch.setattr(bench, "cpu_baseline", lambda rows: {"value": 1.0, "rows": rows})
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--cpu-baseline-only", "--cpu-rows", "3"])
+    assert json.loads(buf.getvalue()) == {"value": 1.0, "rows": 3}
