@@ -774,7 +774,13 @@ def cpu_baseline(rows, seconds=10.0):
     import oracle
     from gemm_cq_gemv_gb300 import synth
     cb = load_codebook()
-    state = oracle_state(rows, cb, synth, oracle)
+    t0 = time.perf_counter()
+    state = oracle_state(rows, cb, synth, oracle)          # draws and encodes the sample
+    t1 = time.perf_counter()
+    for d in state:
+        oracle.cq_reconstruct(d["p"], d["n"], 4, cb)
+        oracle.q4_0_dequantize(d["b"], d["m"].K)
+    t2 = time.perf_counter()
     oracle_sample_step(rows, cb, synth, oracle, state)
     # repeat the sample for about ten seconds of CPU work
     reps, nbytes = 0, 0
@@ -786,7 +792,9 @@ def cpu_baseline(rows, seconds=10.0):
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
             "kind": "oracle",
             "sample": f"{reps} x {rows} rows of each large matrix, CQ-W4A8 and Q4_0, batch 1 "
-                      f"(float64 reconstruction + product), {dt:.1f} s"}
+                      f"(float64 reconstruction + product), {dt:.1f} s",
+            "phases_s": {"draw_and_encode": round(t1 - t0, 3), "reconstruct": round(t2 - t1, 3),
+                         "note": f"once over the same {rows}-row sample, both formats"}}
 
 
 def cpu_baseline_report(rows):
