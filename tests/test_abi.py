@@ -100,6 +100,9 @@ def test_gemv_validation(lib):
     # tensor-core path: ceil(B / 32) * ceil(N / 128) = 2^15 * 2^17 output tiles > 2^23
     assert f(A, A, 1 << 24, 128, 128, 2, _cb(), A, A, 1 << 20, A, A, 1 << 40, None) == UNS
     assert lib.q4_0_gemv(A, 1, 32, A, (1 << 30) + 1, A, None) == UNS
+    # K beyond two 1024-position segments per warp (32768)
+    assert f(A, A, 8, 32768 + 128, 128, 4, _cb(), A, A, 1, A, A, 1 << 40, None) == UNS
+    assert lib.q4_0_gemv(A, 1, 32768 + 32, A, 1, A, None) == UNS
 
 
 def test_gemv_lut_validation(lib):
