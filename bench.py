@@ -287,6 +287,24 @@ def prefill_report(dev, cb, torch, cq, synth, steps, warmup, peaks, kind):
     return out
 
 
+def flushed_call_ms(torch, flush, fn, steps, warmup):
+    """Median device time of ``fn`` over ``steps`` calls (after ``warmup``), each call alone
+    between CUDA events with the L2 flushed (``flush`` larger than the L2 is zeroed) first."""
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
 def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 32), kinds=("cq", "q4_0")):
     """Decode batches on the tensor cores: cq_gemv (4-bit, B >= 3 takes the tcgen05 path) and
     q4_0_gemm, per large matrix, each call timed alone with CUDA events after an L2 flush
@@ -297,20 +315,9 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 3
            "timing": "per call, CUDA events, L2 flushed before each call"}
 
     def one(fn):
-        for _ in range(warmup):
-            fn()
-        ts = []
-        for _ in range(steps):
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
+        ms = flushed_call_ms(torch, flush, fn, steps, warmup)
         cq.cq_device_error()
-        return statistics.median(ts)
+        return ms
 
     for B in batches:
         res = {k: {"us": {}, "bytes": 0, "ms": 0.0} for k in kinds}
@@ -366,19 +373,7 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
 
     def latency(fn):
-        g = _capture(torch, fn)
-        ts = []
-        for i in range(warmup + steps):
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            g.replay()
-            e1.record()
-            torch.cuda.synchronize()
-            if i >= warmup:
-                ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        return flushed_call_ms(torch, flush, _capture(torch, fn).replay, steps, warmup)
 
     def streamed(fn, reps=3):
         g = _capture(torch, fn)
@@ -479,19 +474,7 @@ def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
 
     def one(fn):
-        for _ in range(warmup):
-            fn()
-        ts = []
-        for _ in range(steps):
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        return flushed_call_ms(torch, flush, fn, steps, warmup)
 
     out = {"workload": "large-shape decode, batch 1, 1-bit / 2-bit / ternary CQ rows",
            "timing": "per call, CUDA events, L2 flushed before each call",

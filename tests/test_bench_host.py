@@ -107,6 +107,14 @@ class _FakeLib:
         assert blocks.shape == (N, -(-K // 32) * 18) and X.shape[1] == K
         self._count("q4_0_gemv")
 
+    def q4_0_gemm_workspace_bytes(self, M, K):
+        return M * (-(-K // 32) * 32) * 2
+
+    def q4_0_gemm(self, blocks, N, K, X, Y=None, workspace=None):
+        self._ok(blocks), self._ok(workspace)
+        assert Y.shape == (X.shape[0], N) and workspace.numel() >= self.q4_0_gemm_workspace_bytes(*X.shape)
+        self._count("q4_0_gemm")
+
     def cq_device_error(self):
         pass
 
@@ -176,3 +184,20 @@ def test_cpu_baseline_only_entry(monkeypatch):
     with contextlib.redirect_stdout(buf):
         bench.main(["--cpu-baseline-only", "--cpu-rows", "3"])
     assert json.loads(buf.getvalue()) == {"value": 1.0, "rows": 3}
+
+
+def test_batched_report_shapes():
+    lib = _FakeLib()
+    ft = _fake_torch()
+    small = tuple(types.SimpleNamespace(name=m.name, N=m.N // 256, K=m.K) for m in synth.LARGE)
+    mats = []
+    for m in small:
+        W = torch.zeros((m.N, m.K))
+        packed, norms = lib.cq_encode(W, 4, None)
+        mats.append(dict(m=m, packed=packed, norms=norms, blocks=lib.q4_0_quantize(W)))
+    out = bench.batched_report(mats, None, ft, lib, synth, "cpu", 2, 1, batches=(8, 32))
+    for B in (8, 32):
+        assert set(out[f"B{B}"]) == {"cq_gemv", "q4_0_gemm"}
+        assert set(out[f"B{B}"]["cq_gemv"]["us"]) == {m.name for m in small}
+    assert lib.calls["cq_gemv"] == lib.calls["q4_0_gemm"] == 2 * 4 * (1 + 2)
+    json.dumps(out)
