@@ -530,7 +530,10 @@ def narrow_child(args, local_rank):
     if r.returncode != 0 or not lines:
         tail = (r.stderr or r.stdout).strip().splitlines()[-3:]
         return {"error": f"exit {r.returncode}: " + " | ".join(tail)}
-    return json.loads(lines[-1])
+    try:
+        return json.loads(lines[-1])
+    except ValueError as e:
+        return {"error": f"unreadable report: {e}"[:300]}
 
 
 def gpu_arm(args, rank, world, local_rank):
@@ -793,6 +796,8 @@ def cpu_baseline_report(rows):
                              else {"error": f"exit {r.returncode}"})
     except subprocess.TimeoutExpired:
         out["one_thread"] = {"error": "timed out after 300 s"}
+    except ValueError as e:
+        out["one_thread"] = {"error": f"unreadable report: {e}"[:300]}
     return out
 
 
