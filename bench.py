@@ -712,7 +712,10 @@ def gpu_arm(args, rank, world, local_rank):
         if not args.no_narrow and world == 1:
             line["narrow"] = narrow_child(args, local_rank)
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline_report(args.cpu_rows)
+            try:
+                line["cpu_baseline"] = cpu_baseline_report(args.cpu_rows)
+            except Exception as e:   # report, never lose the line
+                line["cpu_baseline"] = {"error": f"{type(e).__name__}: {e}"[:300], "kind": "oracle"}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
