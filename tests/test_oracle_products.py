@@ -5,8 +5,8 @@ dequantised Q4_0 blocks (Minueza -> KMCU v1 page §2)."""
 import numpy as np
 
 from gemm_cq_gemv_gb300.synth import activations, weights
-from oracle import (a8_quantize, codebook_levels, cq_encode, cq_gemv_ref, cq_reconstruct,
-                    q4_0_dequantize, q4_0_gemv_ref, q4_0_quantize, sylvester_hadamard,
+from oracle import (TERNARY, a8_quantize, codebook_levels, cq_encode, cq_gemv_ref, cq_reconstruct,
+                    field_bits, q4_0_dequantize, q4_0_gemv_ref, q4_0_quantize, sylvester_hadamard,
                     unpack_indices)
 from util import fitted_cb28
 
@@ -31,9 +31,9 @@ def test_rotation_identity_route():
     X = activations(3, 384, seed=13)
     q, s = a8_quantize(X)
     Hu = sylvester_hadamard(128)
-    for b in (1, 2, 3, 4):
+    for b in (1, 2, 3, 4, TERNARY):
         packed, norms = cq_encode(W, b, cb)
-        idx = unpack_indices(packed, b)
+        idx = unpack_indices(packed, field_bits(b))
         lv = codebook_levels(cb, b).astype(np.float64)
         nrm = norms.view(np.float16).astype(np.float64)
         y = np.zeros((3, 6))
