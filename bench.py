@@ -476,7 +476,10 @@ def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
     def one(fn):
         return flushed_call_ms(torch, flush, fn, steps, warmup)
 
+    peaks, kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
     out = {"workload": "large-shape decode, batch 1, 1-bit / 2-bit / ternary CQ rows",
+           "peak": {"hbm_gbs": hbm, "source": f"{kind} (hbm_gbs)"},
            "timing": "per call, CUDA events, L2 flushed before each call",
            "unit": "us per call; GB/s of algorithmic bytes over the four matrices"}
     for b, name in ((1, "b1"), (2, "b2"), (cq.CQ_TERNARY, "ternary")):
@@ -507,7 +510,8 @@ def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
             diff = max(diff, float((Yl - Yg).abs().max()) / (den if den > 0 else 1.0))
             del packed, norms
             torch.cuda.empty_cache()
-        out[name] = {k: {"us": v["us"], "GBps": round(nbytes / (v["ms"] * 1e-3) / 1e9, 1)}
+        out[name] = {k: {"us": v["us"], "GBps": round(nbytes / (v["ms"] * 1e-3) / 1e9, 1),
+                         "frac_of_hbm": round(nbytes / (v["ms"] * 1e-3) / 1e9 / hbm, 4)}
                      for k, v in res.items()}
         out[name]["max_rel_diff"] = float(f"{diff:.3g}")
     cq.cq_device_error()
