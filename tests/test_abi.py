@@ -197,3 +197,16 @@ def test_kernel_level_tables_match_oracle(lib):
     assert lib.cq_levels(6, None, A) == 1
     assert lib.cq_levels(2, None, A) == 1                   # b = 2..4 need the caller's table
     assert lib.cq_levels(1, None, None) == 1
+
+
+def test_header_is_plain_c():
+    """include/cqgemv.h is a C ABI: it compiles as strict C99 on its own."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                            "-fsyntax-only", "-x", "c", h], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
