@@ -708,14 +708,14 @@ def gpu_arm(args, rank, world, local_rank):
                                              args.warmup, peaks, kind)
         if not args.no_batched:
             line["batched"] = batched_report(mats, cb, torch, cq, synth, dev, 10, 3, kinds=kinds)
-        if not args.no_small:
+        if not args.no_small and world == 1:
             try:
                 line["small"] = small_report(dev, cb, torch, cq, synth, 10, 3)
             except Exception as e:   # report, never lose the line
                 line["small"] = {"error": f"{type(e).__name__}: {e}"[:300]}
         if not args.no_narrow and world == 1:
             line["narrow"] = narrow_child(args, local_rank)
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:   # the oracle is timed at N = 1 only
             try:
                 line["cpu_baseline"] = cpu_baseline_report(args.cpu_rows)
             except Exception as e:   # report, never lose the line
