@@ -12,14 +12,20 @@ times behind ``roofline`` come from a second pass of the same steps with events 
 each launch).  ``value`` is algorithmic GB/s: packed indices +
 norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step time.
 
-The line also reports, beside the headline, the grouped prefill GEMM of the 20-layer
-model (``prefill``, TFLOP/s) and decode batches of 8 and 32 tokens on the tensor cores
-(``batched``: ``cq_gemv`` at 4 bits and ``q4_0_gemm``, GB/s of weights, each call timed
-alone after an L2 flush), the two small workloads (``small``: CQ-W4A8 512 x 512 and one
-Minueza Q4_0 layer, each as single-call latency and as streamed GB/s over weight copies
-spanning 4x the L2) and batch-1 decode of 1-bit, 2-bit and ternary rows through
-``cq_gemv`` and the table-lookup ``cq_gemv_lut`` (``narrow``, timed in a child process
-after everything else).
+The line also reports every other workload of the path:
+  * ``prefill`` (config 4): the grouped prefill GEMM of the 20-layer model, TFLOP/s and the
+    fraction of the bf16 peak as flat keys per M;
+  * ``batched`` (config 5 at batches 2, 8, 32): ``cq_gemv`` at 4 bits, ``q4_0_gemv`` (B = 2)
+    and ``q4_0_gemm`` (B >= 8), GB/s, each call timed alone after an L2 flush;
+  * ``mixed`` (config 3): ``cq_gemv`` at b = 1..4 on [4096, 4096] and [11008, 4096] with
+    outliers, batches 1 / 4 / 16;
+  * ``small`` (configs 1 and 2): CQ-W4A8 512 x 512 and one Minueza Q4_0 layer, each as
+    single-call latency and as streamed GB/s over weight copies spanning 4x the L2;
+  * ``narrow``: batch-1 decode of 1-bit, 2-bit and ternary rows through ``cq_gemv`` and the
+    table-lookup ``cq_gemv_lut`` (timed in a child process after everything else);
+  * ``cpu_baseline``: the oracle timed on the host cores, on sampled rows of the timed
+    step's own encoded weights, with its outputs checked against the GPU's (``parity``);
+  * ``summary`` (last): the headline number of every workload as flat keys.
 
 ``--impl reference`` times the CPU oracle as it stands on a bounded sample of the same
 workload.  ``--gpus N`` (under torchrun) runs N independent replicas, one per GPU:
@@ -267,23 +273,24 @@ def time_prefill(pf, cb, cq, torch, steps, warmup):
 
 
 def prefill_report(dev, cb, torch, cq, synth, steps, warmup, peaks, kind):
+    """Config 4: the grouped prefill GEMM of the 20-layer model at each M, as flat scalar
+    keys (``M512_tflops``, ``M512_frac``, ...) so that every number sits one level deep."""
+    peak = float(peaks["bf16_tflops"])
     out = {"workload": "20-layer 45M-parameter model (q,o 512x512; k,v 128x512; up 1536x512; "
                        "down 512x1536), CQ-W4A8, one grouped launch of 120 matrices",
-           "dtype": "bf16 MMA, fp32 accumulate, bf16 out"}
-    peak = float(peaks["bf16_tflops"])
+           "dtype": "bf16 MMA, fp32 accumulate, bf16 out",
+           "kernel": "cq_gemm_kernel", "bound": "tensor", "unit": "TFLOP/s", "peak_tflops": peak,
+           "peak_source": f"{kind} bf16_tflops (burst; the GEMM is timed alone)"}
     for M in synth.PREFILL_TOKENS:
         pf = build_prefill(dev, cb, torch, cq, synth, M)
         ms = time_prefill(pf, cb, cq, torch, steps, warmup)
         tf = pf["flops"] / (ms * 1e-3) / 1e12
-        out[f"M{M}"] = {"ms": round(ms, 4), "tflops": round(tf, 1), "gflop": round(pf["flops"] / 1e9, 2),
-                        "frac": round(tf / peak, 4)}
+        out[f"M{M}_ms"] = round(ms, 4)
+        out[f"M{M}_gflop"] = round(pf["flops"] / 1e9, 2)
+        out[f"M{M}_tflops"] = round(tf, 1)
+        out[f"M{M}_frac"] = round(tf / peak, 4)
         del pf
         torch.cuda.empty_cache()
-    big = out[f"M{synth.PREFILL_TOKENS[-1]}"]
-    out["roofline"] = {"kernel": "cq_gemm_kernel", "bound": "tensor", "achieved": big["tflops"],
-                       "peak": peak, "unit": "TFLOP/s", "frac": big["frac"],
-                       "peak_source": (f"{kind} bf16_tflops (burst; the GEMM is timed alone)"),
-                       "workload": f"M={synth.PREFILL_TOKENS[-1]}"}
     return out
 
 
@@ -305,13 +312,16 @@ def flushed_call_ms(torch, flush, fn, steps, warmup):
     return statistics.median(ts)
 
 
-def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 32), kinds=("cq", "q4_0")):
-    """Decode batches on the tensor cores: cq_gemv (4-bit, B >= 3 takes the tcgen05 path) and
-    q4_0_gemm, per large matrix, each call timed alone with CUDA events after an L2 flush
-    (the [8192, 8192] weights would otherwise stay in the 129 MB L2)."""
+def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(2, 8, 32),
+                   kinds=("cq", "q4_0"), hbm=None):
+    """Config 5 at batches above 1: ``cq_gemv`` at 4 bits (B >= 3 takes the tcgen05 path, B = 2
+    one two-token CUDA-core pass) and, for Q4_0, ``q4_0_gemv`` at B = 2 and ``q4_0_gemm`` on
+    the tensor cores at larger batches; per large matrix, each call timed alone with CUDA
+    events after an L2 flush (the [8192, 8192] weights would otherwise stay in the 129 MB L2).
+    GB/s counts the algorithmic bytes (weights once, activations and outputs)."""
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
     out = {"workload": "large-shape decode batches, weights read once per call for all tokens",
-           "dtype": "fp16 MMA operands, fp32 accumulate, fp32 out",
+           "dtype": "B=2: fp32 (CUDA cores); B>=8: fp16 MMA operands, fp32 accumulate, fp32 out",
            "timing": "per call, CUDA events, L2 flushed before each call"}
 
     def one(fn):
@@ -320,6 +330,7 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 3
         return ms
 
     for B in batches:
+        q4_name = "q4_0_gemv" if B <= 2 else "q4_0_gemm"
         res = {k: {"us": {}, "bytes": 0, "ms": 0.0} for k in kinds}
         for i, d in enumerate(mats):
             m = d["m"]
@@ -337,16 +348,64 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(8, 3
                 r["ms"] += ms
                 r["bytes"] += d["packed"].numel() + 2 * d["norms"].numel() + B * m.K + 4 * B * (1 + m.N)
             if "q4_0" in kinds:
-                ws = torch.empty((max(cq.q4_0_gemm_workspace_bytes(B, m.K), 256),), dtype=torch.uint8,
-                                 device=dev)
-                ms = one(lambda: cq.q4_0_gemm(d["blocks"], m.N, m.K, X, Y=Y, workspace=ws))
+                if B <= 2:
+                    ms = one(lambda: cq.q4_0_gemv(d["blocks"], m.N, m.K, X, Y=Y))
+                else:
+                    ws = torch.empty((max(cq.q4_0_gemm_workspace_bytes(B, m.K), 256),), dtype=torch.uint8,
+                                     device=dev)
+                    ms = one(lambda: cq.q4_0_gemm(d["blocks"], m.N, m.K, X, Y=Y, workspace=ws))
                 r = res["q4_0"]
                 r["us"][m.name] = round(ms * 1e3, 1)
                 r["ms"] += ms
                 r["bytes"] += d["blocks"].numel() + 4 * B * m.K + 4 * B * m.N
-        out[f"B{B}"] = {("cq_gemv" if k == "cq" else "q4_0_gemm"):
-                        {"us": v["us"], "GBps": round(v["bytes"] / (v["ms"] * 1e-3) / 1e9, 1)}
-                        for k, v in res.items()}
+        rep = {}
+        for k, v in res.items():
+            gbps = v["bytes"] / (v["ms"] * 1e-3) / 1e9
+            e = {"us": v["us"], "GBps": round(gbps, 1)}
+            if hbm:
+                e["frac_of_hbm"] = round(gbps / hbm, 4)
+            rep["cq_gemv" if k == "cq" else q4_name] = e
+        out[f"B{B}"] = rep
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def mixed_report(dev, cb, torch, cq, synth, steps, warmup, hbm):
+    """Config 3: CQ at every width b = 1..4 on [4096, 4096] and [11008, 4096] (weights with
+    1 % x10 outliers), batches 1 / 4 / 16, each ``cq_gemv`` call timed alone after an L2 flush.
+    Keys ``<matrix>_b<b>_B<B>_{us,GBps,Gwps,frac}``; GB/s counts packed indices, norms,
+    activations, scales and outputs."""
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    out = {"workload": "CQ mixed widths: [4096,4096] (sq) and [11008,4096] (up), b=1..4, "
+                       "batch 1/4/16, 1% x10 outliers",
+           "timing": "per call, CUDA events, L2 flushed before each call", "peak_hbm_gbs": hbm}
+    for i, m in enumerate(synth.CQ_MIXED):
+        g = torch.Generator(device=dev)
+        g.manual_seed(synth.weight_seed(2, i))
+        W = torch.randn((m.N, m.K), device=dev, generator=g) * 0.02
+        W = torch.where(torch.rand((m.N, m.K), device=dev, generator=g) < 0.01, W * 10.0, W)
+        for b in synth.CQ_MIXED_BITS:
+            packed, norms = cq.cq_encode(W, b, cb)
+            for B in synth.CQ_MIXED_BATCHES:
+                gx = torch.Generator(device=dev)
+                gx.manual_seed(synth.activation_seed(2, B) + i)
+                Xq, sc = cq.a8_quantize(torch.randn((B, m.K), device=dev, generator=gx))
+                ws = torch.empty((cq.cq_gemv_workspace_bytes(B, m.K),), dtype=torch.uint8, device=dev)
+                Y = torch.empty((B, m.N), dtype=torch.float32, device=dev)
+                ms = flushed_call_ms(torch, flush, lambda: cq.cq_gemv(packed, norms, m.N, m.K, b, cb, Xq, sc,
+                                                                      Y=Y, workspace=ws), steps, warmup)
+                nbytes = packed.numel() + 2 * norms.numel() + B * m.K + 4 * B + 4 * B * m.N
+                gbps = nbytes / (ms * 1e-3) / 1e9
+                key = f"{m.name}_b{b}_B{B}"
+                out[key + "_us"] = round(ms * 1e3, 1)
+                out[key + "_GBps"] = round(gbps, 1)
+                out[key + "_Gwps"] = round(m.N * m.K / (ms * 1e-3) / 1e9, 1)
+                out[key + "_frac"] = round(gbps / hbm, 4)
+            del packed, norms
+        del W
+        torch.cuda.empty_cache()
+    cq.cq_device_error()
     del flush
     torch.cuda.empty_cache()
     return out
@@ -703,11 +762,20 @@ def gpu_arm(args, rank, world, local_rank):
                                  "q4_0_gemv kernel per Q4_0 matrix",
             "clocks": clocks,
         }
+        # host copies of sampled rows of the timed step (encoded bytes, activations, the
+        # GPU's outputs) for the oracle check of the CPU-baseline leg below
+        sample = (gpu_sample(mats, args.cpu_rows)
+                  if not args.no_cpu_baseline and world == 1 and set(kinds) == {"cq", "q4_0"} else None)
         if not args.no_prefill:
             line["prefill"] = prefill_report(dev, cb, torch, cq, synth, max(3, args.steps // 5),
                                              args.warmup, peaks, kind)
         if not args.no_batched:
-            line["batched"] = batched_report(mats, cb, torch, cq, synth, dev, 10, 3, kinds=kinds)
+            line["batched"] = batched_report(mats, cb, torch, cq, synth, dev, 10, 3, kinds=kinds, hbm=hbm)
+        if not args.no_mixed and world == 1 and "cq" in kinds:
+            try:
+                line["mixed"] = mixed_report(dev, cb, torch, cq, synth, 10, 3, hbm)
+            except Exception as e:   # report, never lose the line
+                line["mixed"] = {"error": f"{type(e).__name__}: {e}"[:300]}
         if not args.no_small and world == 1:
             try:
                 line["small"] = small_report(dev, cb, torch, cq, synth, 10, 3)
@@ -717,26 +785,69 @@ def gpu_arm(args, rank, world, local_rank):
             line["narrow"] = narrow_child(args, local_rank)
         if not args.no_cpu_baseline and world == 1:   # the oracle is timed at N = 1 only
             try:
-                line["cpu_baseline"] = cpu_baseline_report(args.cpu_rows)
+                line["cpu_baseline"] = cpu_baseline_report(args.cpu_rows, sample=sample)
             except Exception as e:   # report, never lose the line
                 line["cpu_baseline"] = {"error": f"{type(e).__name__}: {e}"[:300], "kind": "oracle"}
+        line["summary"] = summary_of(line, hbm)   # last, so that it ends the printed line
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
 
 
+def summary_of(line, hbm):
+    """Every workload's headline numbers as flat scalar keys: c1/c2 the small workloads
+    (latency, streamed GB/s and its fraction of HBM), c3 the mixed-width sweep's fractions,
+    c4 the prefill GEMM, c5 the large-shape decode at each batch, plus the oracle check."""
+    out = {}
+    sm = line.get("small") or {}
+    for key, name in (("c1", "cq_w4a8_512x512"), ("c2", "minueza_q4_0_layer")):
+        r = sm.get(name)
+        if isinstance(r, dict):
+            out[f"{key}_latency_us"] = r.get("latency_us")
+            out[f"{key}_streamed_GBps"] = r.get("streamed_GBps")
+            if r.get("streamed_GBps"):
+                out[f"{key}_streamed_frac"] = round(r["streamed_GBps"] / hbm, 4)
+    mx = line.get("mixed") or {}
+    for k, v in mx.items():
+        if k.endswith("_frac"):
+            out["c3_" + k] = v
+    pf = line.get("prefill") or {}
+    for k in ("M512_tflops", "M512_frac", "M2048_tflops", "M2048_frac"):
+        if k in pf:
+            out["c4_" + k] = pf[k]
+    for k, v in (line.get("kernels") or {}).items():
+        out[f"c5_B1_{k}_GBps"] = v.get("GBps")
+        if v.get("GBps"):
+            out[f"c5_B1_{k}_frac"] = round(v["GBps"] / hbm, 4)
+    for bk, rep in (line.get("batched") or {}).items():
+        if bk.startswith("B") and isinstance(rep, dict):
+            for kern, v in rep.items():
+                if isinstance(v, dict) and "GBps" in v:
+                    out[f"c5_{bk}_{kern}_GBps"] = v["GBps"]
+                    out[f"c5_{bk}_{kern}_frac"] = round(v["GBps"] / hbm, 4)
+    par = (line.get("cpu_baseline") or {}).get("parity")
+    if par:
+        out["oracle_check_ok"] = par["ok"]
+        out["oracle_check_cq"] = par["cq_gemv_max_rel_err"]
+        out["oracle_check_q4_0"] = par["q4_0_gemv_max_rel_err"]
+    return out
+
+
 # ------------------------------------------------------------------------------------
 # The oracle arm (CPU): the oracle as it stands, on a bounded sample of the workload
 # ------------------------------------------------------------------------------------
-def oracle_sample_step(rows, cb, synth, oracle, state):
-    """Oracle GEMV of ``rows`` rows of every large matrix (both formats); returns bytes."""
+def oracle_sample_step(rows, cb, synth, oracle, state, outputs=None):
+    """Oracle GEMV of ``rows`` rows of every large matrix (both formats); returns bytes.
+    With ``outputs`` (a list), appends each matrix's (cq, q4_0) oracle outputs to it."""
     nbytes = 0
     for d in state:
         m = d["m"]
         nbytes += d["p"].nbytes + d["n"].nbytes + m.K + 4 + 4 * rows
-        oracle.cq_gemv_ref(d["p"], d["n"], 4, cb, d["q"], d["s"])
+        ycq = oracle.cq_gemv_ref(d["p"], d["n"], 4, cb, d["q"], d["s"])
         nbytes += d["b"].nbytes + 4 * m.K + 4 * rows
-        oracle.q4_0_gemv_ref(d["b"], m.K, d["X"])
+        yq4 = oracle.q4_0_gemv_ref(d["b"], m.K, d["X"])
+        if outputs is not None:
+            outputs.append((ycq, yq4))
     return nbytes
 
 
@@ -751,6 +862,29 @@ def oracle_state(rows, cb, synth, oracle):
     return state
 
 
+def gpu_sample(mats, rows):
+    """Host copies of the first ``rows`` rows of every matrix of the timed decode step: the
+    encoded weights the GPU streamed, the step's activations and the GPU's outputs for those
+    rows (taken after the timed region; no arithmetic)."""
+    out = []
+    for d in mats:
+        r = min(rows, d["m"].N)
+        out.append(dict(m=d["m"], p=d["packed"][:r].cpu().numpy(),
+                        n=d["norms"][:r].cpu().numpy().view("uint16"),
+                        b=d["blocks"][:r].cpu().numpy(), q=d["Xq"].cpu().numpy(),
+                        s=d["s"].cpu().numpy(), X=d["X"].cpu().numpy(),
+                        y_cq=d["Ycq"][:, :r].cpu().numpy(), y_q4=d["Yq4"][:, :r].cpu().numpy()))
+    return out
+
+
+def _max_rel(y, ref):
+    """max |y - ref| / max |ref| over one output vector (the sampled rows of it)."""
+    y = np.asarray(y, np.float64).ravel()
+    ref = np.asarray(ref, np.float64).ravel()
+    den = float(np.max(np.abs(ref)))
+    return float(np.max(np.abs(y - ref)) / (den if den > 0 else 1.0))
+
+
 _BLAS_THREAD_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
@@ -763,18 +897,26 @@ def blas_threads():
     return os.cpu_count()
 
 
-def cpu_baseline(rows, seconds=10.0):
+def cpu_baseline(rows, seconds=10.0, sample=None):
+    """The oracle as it stands, timed on ``rows`` rows of each large matrix (both formats).
+
+    With ``sample`` (``gpu_sample`` of the timed decode step) the oracle runs on exactly the
+    bytes the GPU streamed, and its outputs are compared with the GPU's for those rows
+    (``parity``: the float32-accumulation tolerance 1e-3 of the GEMV parity tests).
+    Without it (the one-thread child, the reference arm) the sample is drawn and encoded
+    here from the same seeds."""
     import oracle
     from gemm_cq_gemv_gb300 import synth
     cb = load_codebook()
     t0 = time.perf_counter()
-    state = oracle_state(rows, cb, synth, oracle)          # draws and encodes the sample
+    state = sample if sample is not None else oracle_state(rows, cb, synth, oracle)
     t1 = time.perf_counter()
     for d in state:
         oracle.cq_reconstruct(d["p"], d["n"], 4, cb)
         oracle.q4_0_dequantize(d["b"], d["m"].K)
     t2 = time.perf_counter()
-    oracle_sample_step(rows, cb, synth, oracle, state)
+    outputs = []
+    oracle_sample_step(rows, cb, synth, oracle, state, outputs)
     # repeat the sample for about ten seconds of CPU work
     reps, nbytes = 0, 0
     a = time.perf_counter()
@@ -782,18 +924,29 @@ def cpu_baseline(rows, seconds=10.0):
         nbytes += oracle_sample_step(rows, cb, synth, oracle, state)
         reps += 1
     dt = time.perf_counter() - a
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": f"{reps} x {rows} rows of each large matrix, CQ-W4A8 and Q4_0, batch 1 "
-                      f"(float64 reconstruction + product), {dt:.1f} s",
-            "phases_s": {"draw_and_encode": round(t1 - t0, 3), "reconstruct": round(t2 - t1, 3),
-                         "note": f"once over the same {rows}-row sample, both formats"}}
+    out = {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": blas_threads(),
+           "kind": "oracle",
+           "sample": f"{reps} x {rows} rows of each large matrix, CQ-W4A8 and Q4_0, batch 1 "
+                     f"(float64 reconstruction + product), {dt:.1f} s",
+           "phases_s": {("copy_sample" if sample is not None else "draw_and_encode"): round(t1 - t0, 3),
+                        "reconstruct": round(t2 - t1, 3),
+                        "note": f"once over the same {rows}-row sample, both formats"}}
+    if sample is not None:
+        e_cq = max(_max_rel(d["y_cq"], o[0]) for d, o in zip(state, outputs))
+        e_q4 = max(_max_rel(d["y_q4"], o[1]) for d, o in zip(state, outputs))
+        out["parity"] = {"rows_per_matrix": rows, "cq_gemv_max_rel_err": float(f"{e_cq:.3g}"),
+                         "q4_0_gemv_max_rel_err": float(f"{e_q4:.3g}"), "tol": 1e-3,
+                         "ok": bool(e_cq < 1e-3 and e_q4 < 1e-3),
+                         "what": "the timed step's outputs for these rows against the oracle "
+                                 "on the same encoded bytes and activations"}
+    return out
 
 
-def cpu_baseline_report(rows):
-    """The oracle timed twice: with BLAS on every core (this process) and pinned to one
-    thread (a child process, since BLAS reads its thread count when NumPy loads)."""
-    out = cpu_baseline(rows)
+def cpu_baseline_report(rows, sample=None):
+    """The oracle timed twice: with BLAS on every core (this process, on ``sample`` when
+    given) and pinned to one thread (a child process, since BLAS reads its thread count
+    when NumPy loads)."""
+    out = cpu_baseline(rows, sample=sample)
     env = dict(os.environ, **{v: "1" for v in _BLAS_THREAD_VARS})
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--cpu-rows", str(rows)]
     try:
@@ -863,6 +1016,7 @@ def main(argv=None):
                     help="time only the grouped prefill GEMM (profiling runs)")
     ap.add_argument("--prefill-m", type=int, default=2048)
     ap.add_argument("--no-batched", action="store_true", help="skip the decode-batch report")
+    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-width CQ sweep (config 3)")
     ap.add_argument("--batched-only", action="store_true",
                     help="time only the tensor-core decode batch of --batch tokens (profiling runs)")
     ap.add_argument("--batch", type=int, default=32)

@@ -676,10 +676,16 @@ __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint3
             }
         }
     }
-    // sum (nib - 8) x = sum (128 + nib) x - 136 sum x
+    // sum (nib - 8) x = sum (128 + nib) x - 136 sum x.  A block whose nibbles are all 8
+    // (every weight 0, e.g. an all-zero row: KMCU page, §2) contributes exactly 0 by the
+    // definition; the two terms above would leave a rounding residue, so its scale is
+    // replaced by 0 (the bracket is finite, and 0 times it is exactly 0)
+    const uint32_t off8 = ((nw[0] ^ 0x88888888u) | (nw[1] ^ 0x88888888u)) |
+                          ((nw[2] ^ 0x88888888u) | (nw[3] ^ 0x88888888u));
+    const float dd = off8 ? d : 0.0f;
 #pragma unroll
     for (int t = 0; t < TB; ++t)
-        acc[t][r] = fmaf(d, ((a4[t][0] + a4[t][2]) + (a4[t][1] + a4[t][3])) - cblk[t], acc[t][r]);
+        acc[t][r] = fmaf(dd, ((a4[t][0] + a4[t][2]) + (a4[t][1] + a4[t][3])) - cblk[t], acc[t][r]);
 }
 
 // Activation pairs of this lane's blocks and their block sums (x 136), zero outside K;

@@ -201,3 +201,74 @@ def test_batched_report_shapes():
         assert set(out[f"B{B}"]["cq_gemv"]["us"]) == {m.name for m in small}
     assert lib.calls["cq_gemv"] == lib.calls["q4_0_gemm"] == 2 * 4 * (1 + 2)
     json.dumps(out)
+
+
+def test_batched_report_batch_two_uses_the_gemvs():
+    lib = _FakeLib()
+    ft = _fake_torch()
+    small = tuple(types.SimpleNamespace(name=m.name, N=m.N // 256, K=m.K) for m in synth.LARGE)
+    mats = []
+    for m in small:
+        W = torch.zeros((m.N, m.K))
+        packed, norms = lib.cq_encode(W, 4, None)
+        mats.append(dict(m=m, packed=packed, norms=norms, blocks=lib.q4_0_quantize(W)))
+    out = bench.batched_report(mats, None, ft, lib, synth, "cpu", 2, 1, batches=(2,), hbm=1000.0)
+    assert set(out["B2"]) == {"cq_gemv", "q4_0_gemv"}
+    assert out["B2"]["q4_0_gemv"]["frac_of_hbm"] > 0
+    assert "q4_0_gemm" not in lib.calls and lib.calls["q4_0_gemv"] == 4 * (1 + 2)
+
+
+def test_mixed_report_covers_every_width_shape_and_batch():
+    lib = _FakeLib()
+    small = tuple(types.SimpleNamespace(name=m.name, N=m.N // 64, K=m.K // 8) for m in synth.CQ_MIXED)
+    fs = types.SimpleNamespace(CQ_MIXED=small, CQ_MIXED_BITS=synth.CQ_MIXED_BITS,
+                               CQ_MIXED_BATCHES=synth.CQ_MIXED_BATCHES,
+                               weight_seed=synth.weight_seed, activation_seed=synth.activation_seed)
+    ft = _fake_torch()
+    ft.rand = torch.rand
+    ft.where = torch.where
+    out = bench.mixed_report("cpu", None, ft, lib, fs, 2, 3, 1e-3)
+    for m in small:
+        for b in (1, 2, 3, 4):
+            for B in (1, 4, 16):
+                k = f"{m.name}_b{b}_B{B}"
+                assert out[k + "_us"] > 0 and out[k + "_frac"] > 0 and out[k + "_Gwps"] > 0
+    assert lib.calls["cq_gemv"] == 2 * 4 * 3 * (3 + 2)
+    json.dumps(out)
+
+
+def test_summary_flattens_every_workload():
+    line = {"small": {"cq_w4a8_512x512": {"latency_us": 5.0, "streamed_GBps": 100.0},
+                      "minueza_q4_0_layer": {"latency_us": 20.0, "streamed_GBps": 200.0}},
+            "mixed": {"sq_b4_B1_frac": 0.5, "sq_b4_B1_us": 3.0},
+            "prefill": {"M512_tflops": 700.0, "M512_frac": 0.36, "M2048_tflops": 1000.0,
+                        "M2048_frac": 0.52},
+            "kernels": {"cq_gemv": {"GBps": 500.0}},
+            "batched": {"B2": {"cq_gemv": {"GBps": 400.0}}, "workload": "x"},
+            "cpu_baseline": {"parity": {"ok": True, "cq_gemv_max_rel_err": 1e-7,
+                                        "q4_0_gemv_max_rel_err": 2e-6}}}
+    s = bench.summary_of(line, 1000.0)
+    assert s["c1_streamed_frac"] == 0.1 and s["c2_latency_us"] == 20.0
+    assert s["c3_sq_b4_B1_frac"] == 0.5 and "c3_sq_b4_B1_us" not in s
+    assert s["c4_M2048_frac"] == 0.52 and s["c5_B1_cq_gemv_frac"] == 0.5
+    assert s["c5_B2_cq_gemv_frac"] == 0.4 and s["oracle_check_ok"] is True
+    assert all(not isinstance(v, dict) for v in s.values())
+
+
+def test_cpu_baseline_checks_a_gpu_sample():
+    """The oracle leg run on sampled rows of the step, with the GPU outputs replaced by the
+    oracle's own (ok) and by a perturbed copy (not ok)."""
+    import numpy as np
+    import oracle
+    from tests.util import fitted_cb28
+    rows = 4
+    state = bench.oracle_state(rows, fitted_cb28(), synth, oracle)
+    outs = []
+    bench.oracle_sample_step(rows, fitted_cb28(), synth, oracle, state, outs)
+    sample = [dict(d, y_cq=o[0].astype(np.float32), y_q4=o[1].astype(np.float32))
+              for d, o in zip(state, outs)]
+    r = bench.cpu_baseline(rows, seconds=0.01, sample=sample)
+    assert r["parity"]["ok"] and r["parity"]["cq_gemv_max_rel_err"] < 1e-6
+    sample[0]["y_q4"] = sample[0]["y_q4"] * 1.01
+    r = bench.cpu_baseline(rows, seconds=0.01, sample=sample)
+    assert not r["parity"]["ok"] and r["parity"]["q4_0_gemv_max_rel_err"] > 5e-3

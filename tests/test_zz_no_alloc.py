@@ -48,19 +48,30 @@ def _call_noalloc(lib, packed, norms, N, K, b, cbk, q, s, Y):
                                Y.data_ptr(), st)
 
 
+# (N, K, B, b, seed): the branches of the decode GEMV, in a sequence whose shapes change
+# from call to call, so that each call reuses a scratch that still holds the previous
+# call's activations:
+#   * several CUDA-core passes sharing one rotation in the scratch (B = 3, N % 16 != 0);
+#   * the same at another width and shape (2-bit, B = 5);
+#   * the tensor-core batch, whose fp16 activations live in the scratch (B >= 3, N % 16 == 0);
+#   * one fused pass, which rotates in its prologue and does not touch the scratch (B = 1);
+#   * the tensor-core batch again, after the scratch was last written by another shape.
+SEQUENCE = ((1000, 4096, 3, 4, 11), (257, 1536, 5, 2, 23), (1024, 4096, 8, 4, 31),
+            (512, 2048, 1, 4, 37), (2048, 1024, 16, 4, 41))
+
+
 def test_noalloc_matches_workspace_gemv_twice(lib):
     cbk = cq.make_codebook(fitted_cb28())
-    # two calls in a row with different shapes: the second call reuses the scratch
-    # that still holds the first call's rotated activations
-    for (N, K, B, b, seed) in ((1000, 4096, 3, 4, 11), (257, 1536, 5, 2, 23)):
-        packed, norms, q, s = _operands(N, K, B, b, seed, cbk)
-        ref = cq.cq_gemv(packed, norms, N, K, b, cbk, q, s)
-        Y = torch.full((B, N), float("nan"), dtype=torch.float32, device=q.device)
-        assert _call_noalloc(lib, packed, norms, N, K, b, cbk, q, s, Y) == 0
-        torch.cuda.synchronize()
-        got, want = Y.cpu().numpy(), ref.cpu().numpy()
-        assert np.isfinite(got).all()
-        assert max_rel_err(got, want) < TOL
+    for _ in range(2):   # the whole sequence twice in a row
+        for (N, K, B, b, seed) in SEQUENCE:
+            packed, norms, q, s = _operands(N, K, B, b, seed, cbk)
+            ref = cq.cq_gemv(packed, norms, N, K, b, cbk, q, s)
+            Y = torch.full((B, N), float("nan"), dtype=torch.float32, device=q.device)
+            assert _call_noalloc(lib, packed, norms, N, K, b, cbk, q, s, Y) == 0
+            torch.cuda.synchronize()
+            got, want = Y.cpu().numpy(), ref.cpu().numpy()
+            assert np.isfinite(got).all()
+            assert max_rel_err(got, want) < TOL, (N, K, B, b)
 
 
 def test_noalloc_rejects_sizes_beyond_the_scratch(lib):
