@@ -16,13 +16,14 @@
 
 #include <mutex>
 
-#include "common.cuh"
+#include "gemv_pipe.cuh"
 
 namespace cq {
 namespace {
 
+using namespace pipe;
+
 constexpr int kThreads = 256;   // 8 warps
-constexpr int kRows = 8;        // output rows per warp tile
 constexpr int kSeg = 1024;      // positions per segment (32 lanes x 32)
 
 // ---------------------------------------------------------------------------------
@@ -57,28 +58,6 @@ rotate_act_kernel(const int8_t* __restrict__ Xq, int64_t groups, float* __restri
     }
 }
 
-// Butterfly reduction of 8 per-lane row partials: afterwards every lane holds the full
-// sum of row ((lane >> 2) & 7).
-__device__ __forceinline__ float reduce_rows8(const float (&a)[kRows], int lane) {
-    float b[4], c[2];
-    const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float send = u4 ? a[k] : a[k + 4];
-        const float keep = u4 ? a[k + 4] : a[k];
-        b[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const float send = u3 ? b[k] : b[k + 2];
-        const float keep = u3 ? b[k + 2] : b[k];
-        c[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float v = (u2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, u2 ? c[0] : c[1], 4);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    return v;
-}
 
 // ---------------------------------------------------------------------------------
 // Shared pieces of the two GEMV kernels.
@@ -94,128 +73,7 @@ __device__ __forceinline__ float reduce_rows8(const float (&a)[kRows], int lane)
 // one, so no warp stalls the streaming of the others.
 // ---------------------------------------------------------------------------------
 constexpr int kWarps2 = 16;
-constexpr int kSlots = 16;
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b))
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
-                     smem_u32(b)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    // with a suspend-time hint the waiting thread sleeps until the phase completes (or
-    // the hint elapses) instead of spinning and taking issue slots from working warps
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity), "r"(1000000u)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Bounded wait (2 s by default): on expiry raise the device error flag and give up (the
-// result of the call is then undefined and cq_device_error() reports the timeout).
-__device__ __forceinline__ void mbar_wait(uint64_t* b, uint32_t parity, unsigned int* err,
-                                          unsigned long long timeout_ns = 2000000000ull) {
-    if (mbar_try(b, parity)) return;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try(b, parity)) return;
-        if ((i & 255u) == 0u && global_ns() - t0 > timeout_ns) {
-            atomicOr(err, 2u);
-            return;
-        }
-    }
-}
-
-struct Reduce {
-    float* part;        // [kSlots][16][TB][8]
-    uint32_t* count;    // [kSlots] arrivals (cumulative)
-    uint64_t* empty;    // [kSlots] completes when the slot's tile has been reduced
-};
-
-__device__ __forceinline__ uint32_t atomic_add_acq_rel_shared(uint32_t* a, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
-                 : "=r"(old)
-                 : "r"(smem_u32(a)), "r"(v)
-                 : "memory");
-    return old;
-}
-
-// Stores this warp's row partials of tile number `it`; the last of the `nbusy` warps to
-// arrive reduces the tile.  `fin(t, rr, sum)` receives the sum for token t of tile row rr.
-template <int TB, typename Fin>
-__device__ __forceinline__ void tile_reduce(const Reduce& rd, const float (&acc)[TB][kRows], int it,
-                                            int w, int lane, int nsl, uint32_t nbusy, int tile_rows,
-                                            int ntok, unsigned int* err, Fin fin) {
-    const int slot = it % kSlots;
-    const uint32_t ph = (uint32_t)((it / kSlots) & 1);
-    float v[TB];
-#pragma unroll
-    for (int t = 0; t < TB; ++t) v[t] = reduce_rows8(acc[t], lane);
-    mbar_wait(&rd.empty[slot], ph ^ 1u, err);
-    if ((lane & 3) == 0) {
-#pragma unroll
-        for (int t = 0; t < TB; ++t)
-            rd.part[((slot * kWarps2 + w) * TB + t) * kRows + ((lane >> 2) & 7)] = v[t];
-    }
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0) old = atomic_add_acq_rel_shared(&rd.count[slot], 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old % nbusy == nbusy - 1u) {
-        __syncwarp();
-        for (int idx = lane; idx < TB * tile_rows; idx += 32) {
-            const int t = idx / tile_rows, rr = idx % tile_rows;
-            const int g = rr / kRows, r = rr % kRows;
-            if (t < ntok) {
-                float sum = 0.0f;
-                for (int ss = 0; ss < nsl; ++ss)
-                    sum += rd.part[((slot * kWarps2 + g * nsl + ss) * TB + t) * kRows + r];
-                fin(t, rr, sum);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rd.empty[slot]);
-    }
-}
-
-__device__ __forceinline__ void init_reduce(const Reduce& rd) {
-    for (int s = 0; s < kSlots; ++s) {
-        rd.count[s] = 0u;
-        mbar_init(&rd.empty[s], 1);
-    }
-}
-
-// bytes of the reduction area: partials, then the barriers (8-byte aligned), then counters
-__host__ __device__ constexpr size_t reduce_bytes(int tb) {
-    return (size_t)kSlots * kWarps2 * tb * kRows * sizeof(float) + kSlots * sizeof(uint64_t) +
-           kSlots * sizeof(uint32_t);
-}
-
-__device__ __forceinline__ Reduce carve_reduce(void* base, int tb) {
-    Reduce rd;
-    rd.part = reinterpret_cast<float*>(base);
-    rd.empty = reinterpret_cast<uint64_t*>(rd.part + kSlots * kWarps2 * tb * kRows);
-    rd.count = reinterpret_cast<uint32_t*>(rd.empty + kSlots);
-    return rd;
-}
 
 // ---------------------------------------------------------------------------------
 // Per-warp staging ring.  Each warp streams its own rows through kRing slots of shared
@@ -232,37 +90,6 @@ constexpr int64_t kMaxGemvRows = ((int64_t)1 << 31) - 1024;
 constexpr int kRing = 4;       // a power of two (slot = unit & 3, phase = unit >> 2)
 static_assert(kRing == 4, "ring slot and phase arithmetic assume 4 slots");
 
-// 2-D tensor copy of one box (rows outside the tensor and columns past its end read as
-// zero and still count toward the transaction bytes)
-__device__ __forceinline__ void tma_box(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-// orders this thread's earlier shared-memory reads before later bulk copies into them
-__device__ __forceinline__ void fence_proxy_async() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Bump allocator over (at most) two free ranges of the shared window; every thread runs
-// it identically, so all agree on the layout.
-struct SmemCarve {
-    uint32_t a, a_end, b, b_end;
-    bool ok;
-    __device__ __forceinline__ uint32_t take(uint32_t size, uint32_t align) {
-        const uint32_t pa = (a + align - 1) & ~(align - 1);
-        if (pa + size <= a_end) { a = pa + size; return pa; }
-        const uint32_t pb = (b + align - 1) & ~(align - 1);
-        if (pb + size <= b_end) { b = pb + size; return pb; }
-        ok = false;
-        return b;
-    }
-};
 
 // ---------------------------------------------------------------------------------
 // A5: CQ GEMV.  Y[t][o] = s_t / 128 * sum_j norm[o][j] * sum_i cb[idx] * xr[t][128 j + i]
@@ -346,7 +173,7 @@ struct CqPlan {
 template <int BITS>
 size_t cq_smem_bytes(int tb) {
     using P = CqPlan<BITS>;
-    const size_t rest = reduce_bytes(tb) + 16 + kWarps2 * kRing * 8 + 8 + 64 + 16 +
+    const size_t rest = reduce_bytes<kWarps2>(tb) + 16 + kWarps2 * kRing * 8 + 8 + 64 + 16 +
                         (size_t)kWarps2 * (P::ring + 128);
     // 4-bit: the table is 64 KB aligned; the space below it may be too small to use
     if (BITS == 4) return 227 * 1024;
@@ -398,7 +225,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
         cv.a = cv.a_end = tbase + P::table; cv.b = cv.a; cv.b_end = send;
     }
     if (tbase + P::table > send) cv.ok = false;
-    const uint32_t red_at = cv.take((uint32_t)reduce_bytes(TB), 16);
+    const uint32_t red_at = cv.take((uint32_t)reduce_bytes<kWarps2>(TB), 16);
     const uint32_t bar_at = cv.take(kWarps2 * kRing * 8, 8);
     const uint32_t lv_at = cv.take(16 * sizeof(float), 16);
     uint32_t ring_at = 0;
@@ -412,7 +239,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
     }
     auto gen = [&](uint32_t a) { return smem_c + (a - sbase); };
     float2* lut2 = reinterpret_cast<float2*>(gen(tbase));                 // [E][32]
-    const Reduce rd = carve_reduce(gen(red_at), TB);
+    const Reduce rd = carve_reduce<kWarps2>(gen(red_at), TB);
     uint64_t* rfull = reinterpret_cast<uint64_t*>(gen(bar_at)) + w * kRing;
     float* slv = reinterpret_cast<float*>(gen(lv_at));
     uint8_t* ring = gen(ring_at);
@@ -595,7 +422,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
                 }
             }
         }
-        tile_reduce<TB>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
+        tile_reduce<TB, kWarps2>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
                         [&](int t, int rr, float sum) {
                             const int64_t row = tile * tile_rows + rr;
                             if (row < p.N) {
@@ -734,7 +561,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
     constexpr int kSlotB = kUnitRows * kQSeg;
     uint8_t* rings = smem_q;                                                   // [16][kRing][4][576]
     uint64_t* rbar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kRing * kSlotB);  // [16][kRing]
-    const Reduce rd = carve_reduce(rbar + kWarps2 * kRing, TB);
+    const Reduce rd = carve_reduce<kWarps2>(rbar + kWarps2 * kRing, TB);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     pdl_trigger();
     if (tid == 0) prefetch_tensormap(&p.bmap);
@@ -814,7 +641,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
                         q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, h * kUnitRows + r);
             }
         }
-        tile_reduce<TB>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
+        tile_reduce<TB, kWarps2>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
                         [&](int t, int rr, float sum) {
                             const int64_t row = tile * tile_rows + rr;
                             if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
@@ -828,7 +655,7 @@ template <int TB, int SPW>
 __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_rows_kernel(const Q40GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem_q[];
     uint8_t* stage = smem_q;                                              // [16][8][608]
-    const Reduce rd = carve_reduce(smem_q + kWarps2 * kRows * kStage, TB);
+    const Reduce rd = carve_reduce<kWarps2>(smem_q + kWarps2 * kRows * kStage, TB);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     pdl_trigger();
     if (tid == 0) init_reduce(rd);
@@ -903,7 +730,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_rows_kernel(const Q
                 }
             }
         }
-        tile_reduce<TB>(rd, acc, it, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
+        tile_reduce<TB, kWarps2>(rd, acc, it, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
                         [&](int t, int rr, float sum) {
                             const int64_t row = tile * tile_rows + rr;
                             if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
@@ -917,6 +744,9 @@ static __device__ unsigned int g_gemv_err;
 std::mutex g_err_mu;
 unsigned int* g_gemv_err_ptr[64] = {nullptr};
 
+}  // namespace
+
+namespace pipe {
 // Cached device address of this unit's error word on the current device.
 cq_status device_error_word(unsigned int** out) {
     int dev = 0;
@@ -933,6 +763,9 @@ cq_status device_error_word(unsigned int** out) {
     *out = g_gemv_err_ptr[dev];
     return CQ_OK;
 }
+}  // namespace pipe
+
+namespace {
 
 // Failure-detection probe: one thread waits, with this unit's bounded wait, on a barrier
 // phase that nothing completes.  The wait gives up after `timeout_ns`, raises the error
@@ -946,6 +779,9 @@ __global__ void bounded_wait_probe_kernel(unsigned int* err, unsigned long long 
     }
 }
 
+}  // namespace
+
+namespace pipe {
 // cuTensorMapEncodeTiled from the driver (cached; no link against libcuda)
 std::mutex g_enc_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
@@ -976,6 +812,9 @@ cq_status encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
     if (r != CUDA_SUCCESS) { set_last_cuda_error((int)r); return CQ_ERR_CUDA; }
     return CQ_OK;
 }
+}  // namespace pipe
+
+namespace {
 
 // `attr`: one flag per device (the shared-memory attribute is set per device context)
 template <typename Kern>
@@ -1020,8 +859,8 @@ template <int TB, int SPW, bool RING>
 cq_status run_q4_0_gemv(Q40GemvParams p, cudaStream_t st) {
     static bool attr[64] = {};
     auto kern = RING ? q4_0_gemv_ring_kernel<TB, SPW> : q4_0_gemv_rows_kernel<TB, SPW>;
-    const size_t smem = RING ? (size_t)kWarps2 * kRing * kUnitRows * kQSeg + kWarps2 * kRing * 8 + reduce_bytes(TB)
-                             : (size_t)kWarps2 * kRows * kStage + reduce_bytes(TB);
+    const size_t smem = RING ? (size_t)kWarps2 * kRing * kUnitRows * kQSeg + kWarps2 * kRing * 8 + reduce_bytes<kWarps2>(TB)
+                             : (size_t)kWarps2 * kRows * kStage + reduce_bytes<kWarps2>(TB);
     const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int grid = 0;
     const cq_status s = launch_once(kern, smem, ntiles, st, attr, &grid);
@@ -1080,6 +919,13 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
     // tokens (the workspace, B * K * 4 bytes, holds the fp16 activations)
     if (B >= kTensorMinBatch && N % 16 == 0)
         return gemv_tensor(packed, norms, N, K, b, cbk, Xq, scale, B, Y, workspace, st);
+    // one or two tokens of 4-bit rows: 16-bit integer codewords (half the shared-memory
+    // bytes per lookup), for at least 16 rows (fewer rows keep the fp32 codewords: one
+    // small output of a short vector would magnify the codeword rounding)
+    if (b == 4 && B <= 2 && N >= 16 && K % 1024 == 0) {
+        const cq_status s = cq4_gemv_fx(packed, norms, N, K, cbk, Xq, scale, B, Y, st);
+        if (s != CQ_ERR_UNSUPPORTED) return s;
+    }
     // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
     // tokens per pass when each warp owns a single segment
     const int nseg = (int)((K + kSeg - 1) / kSeg);

@@ -1,0 +1,407 @@
+// CQ GEMV for 4-bit indices on 16-bit integer codewords (A4 + A5 at batch 1 and 2).
+//
+// The product of one row with one token is ("14MB 装下 45M 参数…", §一 and §三, with the
+// rotation identity dot(w_g, x_g) = (norm / 128) * dot(cb[idx], Hu x_g)):
+//
+//   y[t][o] = s_t / 128 * sum_j norm[o][j] * sum_i cb[idx[o][j][i]] * xr[t][128 j + i]
+//
+// where xr = Hu q is the rotated int8 activation, an integer with |xr| <= 128 * 127.
+//
+// What sets the pace on the CUDA cores is the lookup of the codewords, not the bytes: a
+// pair of fp32 codewords per lookup moves 4 bytes of shared memory per weight, which at
+// 128 bytes per clock per SM caps a batch-1 4-bit GEMV near 0.62 of the GB300's copy
+// bandwidth.  Here a lookup moves 2 bytes per weight and the sums are exact integers:
+//
+//   * the codewords enter as 16-bit fixed-point integers C = rint(cb * S), S =
+//     floor(32767 / max |cb|);
+//   * a shared table holds, for every byte of packed indices (a pair of 4-bit indices
+//     a = low nibble, b = high nibble), the word [lo(C_a), lo(C_b), hi(C_a), hi(C_b)]
+//     (lo the unsigned low byte, hi the signed high byte, C = 256 hi + lo), one copy per
+//     lane so that every lookup is free of bank conflicts;
+//   * the activations sit in registers as pairs (xr_a, xr_b) of int16;
+//   * dp2a.lo adds xr_a lo(C_a) + xr_b lo(C_b) and dp2a.hi adds xr_a hi(C_a) + xr_b hi(C_b);
+//   * a lane's 32 positions lie inside one 128-group, so its sum 256 H + L is scaled once
+//     by the group's fp16 norm and accumulated in fp32.
+//
+// The only departure from fp32 codewords is the rounding of each codeword to the 16-bit
+// grid, at most 0.5 / S (<= 4.2e-5 for the Lloyd-Max tables), well inside the 1e-3
+// bound of the product; the host sends rows fewer than 16 (where one small output could
+// magnify it) to the fp32-codeword kernel.
+//
+// Layout of the work: one CTA of NW warps per SM (32 for one token, 16 for two, whose
+// activations take twice the registers), persistent over row tiles.  Warp w owns the
+// K-segment (w mod nsl) of 1024 positions - lane l the positions [32 l, 32 l + 32) - and
+// the row group w / nsl of every tile (8 rows per group).  Packed rows arrive through a
+// per-warp ring of kFxRing slots of 2 rows x one segment (1 KB), each filled by one
+// tensor copy issued by one lane.  The tensor-copy unit starts at most ~47 copies per
+// microsecond per SM (measured), so the copies are whole units and nothing else: the
+// group norms of a tile (8 rows x 8 groups of a segment, 128 bytes) come with one 4-byte
+// load per lane, issued a tile ahead, and reach the lanes that need them by warp
+// shuffles.  Tiles are summed across warps by the deterministic slot reduction of
+// gemv_pipe.cuh.
+
+#include <mutex>
+
+#include "gemv_pipe.cuh"
+
+namespace cq {
+namespace {
+
+using namespace pipe;
+
+constexpr int kFxSeg = 1024;                 // positions per warp segment
+constexpr int kFxUnitRows = 2;               // rows per staged unit
+constexpr int kFxRing = 4;                   // slots per warp ring (slot = unit & 3)
+constexpr uint32_t kFxSegBytes = 512;        // a 4-bit row segment
+constexpr uint32_t kFxSlot = kFxUnitRows * kFxSegBytes;   // packed rows of one unit (1 KB)
+constexpr uint32_t kFxTable = 65536;         // 256 entries x 256-byte stride (lanes use 128)
+constexpr size_t kFxSmem = 227 * 1024;
+static_assert(kFxRing == 4, "slot and phase arithmetic assume 4 slots");
+static_assert(kRows % kFxUnitRows == 0, "a tile is a whole number of units");
+// The lanes' copies of a table entry fill the first 128 bytes of its 256-byte stride; the
+// other 128 bytes of the 256 entries ("holes", 128-byte aligned) hold the partial sums of
+// the cross-warp reduction (holes 128 .. 255, four 8-float partials each).
+__host__ __device__ constexpr uint32_t hole(uint32_t i) { return i * 256u + 128u; }
+constexpr uint32_t kFxPartHole = 128;
+template <int NW, int TB>
+constexpr bool holes_fit() { return kSlots * NW * TB <= 4 * 128; }
+
+struct Cq4FxParams {
+    CUtensorMap pmap;        // packed rows as [N][K / 8] uint32, box 128 x kFxUnitRows
+    const uint16_t* norms;   // [N][K / 128] fp16
+    const int8_t* xq;        // [B][K] int8 activations, rotated in the prologue
+    const float* scale;      // [B]
+    float* Y;                // [B][N]
+    unsigned int* err;       // device error word
+    int64_t N;
+    int K;
+    int nseg;                // K / 1024
+    int rg;                  // row groups per tile
+    int t0;                  // first token of this pass
+    int ntok;                // tokens in this pass (<= TB)
+    uint32_t smem_bytes;     // dynamic shared memory of the launch
+    float out_scale;         // 1 / (128 S)
+    int cw[16];              // the 16-bit codewords C_t
+};
+
+// shared address of (pair entry = byte J of wv, this lane): base | byte << 8 | lane << 2
+template <int J>
+__device__ __forceinline__ uint32_t entry_addr(uint32_t wv, uint32_t lb) {
+    uint32_t a;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(wv), "r"(lb), "n"(0x7604 | (J << 4)));
+    return a;
+}
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+// xr = Hu q for this lane's 32 positions of a 128-group held by lanes 4g..4g+3, in
+// integers: five butterfly stages inside the lane, the strides of 32 and 64 across lanes
+__device__ __forceinline__ void rotate32_int(int (&v)[32], int lane) {
+#pragma unroll
+    for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if ((j & h) == 0) {
+                const int a = v[j], b = v[j + h];
+                v[j] = a + b;
+                v[j + h] = a - b;
+            }
+#pragma unroll
+    for (int m = 1; m <= 2; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int q = __shfl_xor_sync(0xffffffffu, v[j], m);
+            v[j] = upper ? (q - v[j]) : (v[j] + q);
+        }
+    }
+}
+
+template <int NW, int TB>
+__global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_constant__ Cq4FxParams p) {
+    extern __shared__ __align__(128) unsigned char smem_f[];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    pdl_trigger();
+    // shared plan: the table in a 64 KB aligned window (its address is one byte permute),
+    // everything else first-fit in the space below and above it
+    const uint32_t sbase = smem_u32(smem_f), send = sbase + p.smem_bytes;
+    const uint32_t tbase = (sbase + 65535u) & ~65535u;
+    SmemCarve cv;
+    cv.ok = tbase + kFxTable <= send;
+    cv.a = sbase; cv.a_end = tbase; cv.b = tbase + kFxTable; cv.b_end = send;
+    static_assert(holes_fit<NW, TB>(), "the partials must fit the table's holes");
+    const uint32_t red_at = cv.take(kSlots * (8 + 4), 8);        // slot barriers and counters
+    const uint32_t bar_at = cv.take(NW * kFxRing * 8, 8);
+    const uint32_t cw_at = cv.take(16 * sizeof(int), 16);
+    uint32_t ring_at = 0;
+    for (int v = 0; v < NW; ++v) {
+        const uint32_t at = cv.take(kFxRing * kFxSlot, 128);
+        if (v == w) ring_at = at;
+    }
+    if (!cv.ok) {   // the launch's shared memory cannot hold the plan (host sizing error)
+        if (tid == 0) atomicOr(p.err, 4u);
+        return;
+    }
+    auto gen = [&](uint32_t a) { return smem_f + (a - sbase); };
+    Reduce rd;
+    rd.part = reinterpret_cast<float*>(gen(tbase + hole(kFxPartHole)));
+    rd.pstride = 64;   // 256 bytes from one hole to the next
+    rd.empty = reinterpret_cast<uint64_t*>(gen(red_at));
+    rd.count = reinterpret_cast<uint32_t*>(rd.empty + kSlots);
+    uint64_t* rfull = reinterpret_cast<uint64_t*>(gen(bar_at)) + w * kFxRing;
+    int* scw = reinterpret_cast<int*>(gen(cw_at));
+    uint8_t* ring = gen(ring_at);
+    if (tid == 0) prefetch_tensormap(&p.pmap);
+    if (lane < kFxRing) mbar_init(&rfull[lane], 1);
+    if (tid < kSlots) {
+        rd.count[tid] = 0u;
+        mbar_init(&rd.empty[tid], 1);
+    }
+    if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (tid < 16) {   // the payloads, by an unrolled select (no indexed parameter access)
+        int v = 0;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v = (u == tid) ? p.cw[u] : v;
+        scw[tid] = v;
+    }
+    __syncthreads();
+    // pair table: entry e (a = e & 15, b = e >> 4) = [lo(C_a), lo(C_b), hi(C_a), hi(C_b)]
+    // at tbase + e * 256 + lane * 4
+    for (int i = tid; i < 256 * 32; i += NW * 32) {
+        const int e = i >> 5, l = i & 31;
+        const uint32_t ca = (uint32_t)scw[e & 15], cb = (uint32_t)scw[e >> 4];
+        const uint32_t word = (ca & 0xFFu) | (cb & 0xFFu) << 8 | ((ca >> 8) & 0xFFu) << 16 |
+                              ((cb >> 8) & 0xFFu) << 24;
+        *reinterpret_cast<uint32_t*>(gen(tbase + (uint32_t)e * 256u + (uint32_t)l * 4u)) = word;
+    }
+
+    const int nsl = p.nseg < NW ? p.nseg : NW;
+    const int slot = w % nsl, rgi = w / nsl;
+    const uint32_t nbusy = (uint32_t)(nsl * p.rg);
+    const bool busy = rgi < p.rg;
+    const int tile_rows = kRows * p.rg;
+    const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
+    const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    constexpr int upt = kRows / kFxUnitRows;                    // units per tile
+    const int64_t U = busy ? ntk * upt : 0;
+
+    // cursor of the next unit to issue (units go out strictly in order)
+    int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;
+    int nx_rem = 0;
+    auto issue = [&](int d) {
+        if (lane == 0) {
+            const int y = (int)(nx_base + nx_rem * kFxUnitRows);
+            mbar_arrive_tx(&rfull[d], kFxSlot);
+            tma_box(ring + d * kFxSlot, &p.pmap, slot * (kFxSegBytes / 4), y, &rfull[d]);
+        }
+        if (++nx_rem == upt) {
+            nx_rem = 0;
+            nx_base += (int64_t)gridDim.x * tile_rows;
+        }
+    };
+    pdl_wait();   // the weights and activations may come from the previous kernels
+    if (busy)
+        for (int64_t u = 0; u < kFxRing - 1 && u < U; ++u) issue((int)u);
+    // this lane's activations: int8 -> Hu q (exact integers) -> int16 pairs
+    uint32_t xp[TB][16];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) {
+        const bool ok = busy && t < p.ntok;
+        const int8_t* src = p.xq + (int64_t)(p.t0 + t) * p.K + slot * kFxSeg + lane * 32;
+        int v[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int4 c = ok ? *reinterpret_cast<const int4*>(src + 16 * h) : make_int4(0, 0, 0, 0);
+            const int wv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[16 * h + q] = (int)(int8_t)(wv[q >> 2] >> (8 * (q & 3)));
+        }
+        rotate32_int(v, lane);
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+            xp[t][q] = ((uint32_t)v[2 * q] & 0xFFFFu) | ((uint32_t)v[2 * q + 1] << 16);
+    }
+    __syncthreads();   // the table is complete
+    if (!busy) return;   // warps left over when the segments do not divide 16
+
+    const uint32_t lb = tbase | ((uint32_t)lane << 2);
+    const int grp = lane >> 2;   // this lane's group within a segment's 8
+    // group norms of a tile: lane l holds the two of (row l / 4, groups 2 (l % 4) + 0, 1 of
+    // the segment)
+    const int G = p.K / kGroup;
+    auto load_norms = [&](int64_t k) -> uint32_t {
+        const int64_t row = (blockIdx.x + k * gridDim.x) * (int64_t)tile_rows + (int64_t)rgi * kRows + (lane >> 2);
+        if (k >= ntk || row >= p.N) return 0u;
+        return __ldg(reinterpret_cast<const uint32_t*>(p.norms + row * G + slot * 8 + 2 * (lane & 3)));
+    };
+    uint32_t nrm_next = load_norms(0);
+    int64_t u = 0;
+    for (int64_t k = 0; k < ntk; ++k) {
+        const int64_t tile = blockIdx.x + k * gridDim.x;
+        const uint32_t nrm_tile = nrm_next;
+        nrm_next = load_norms(k + 1);   // a tile ahead
+        float acc[TB][kRows];
+#pragma unroll
+        for (int t = 0; t < TB; ++t)
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) acc[t][r] = 0.0f;
+#pragma unroll
+        for (int h = 0; h < upt; ++h, ++u) {
+            if (u + kFxRing - 1 < U) {
+                __syncwarp();   // every lane is done with the slot about to be refilled
+                if (lane == 0) fence_proxy_async();
+                issue((int)((u + kFxRing - 1) & (kFxRing - 1)));
+            }
+            const int d = (int)(u & (kFxRing - 1));
+            const uint8_t* sp = ring + d * kFxSlot;
+            mbar_wait(&rfull[d], (uint32_t)(u >> 2) & 1u, p.err);
+#pragma unroll
+            for (int r = 0; r < kFxUnitRows; ++r) {
+                const uint4 wq = *reinterpret_cast<const uint4*>(sp + r * kFxSegBytes + lane * 16);
+                const uint32_t wd[4] = {wq.x, wq.y, wq.z, wq.w};
+                int lo[TB][2], hi[TB][2];
+#pragma unroll
+                for (int t = 0; t < TB; ++t) lo[t][0] = lo[t][1] = hi[t][0] = hi[t][1] = 0;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t c0 = lds_u32(entry_addr<0>(wd[kk], lb));
+                    const uint32_t c1 = lds_u32(entry_addr<1>(wd[kk], lb));
+                    const uint32_t c2 = lds_u32(entry_addr<2>(wd[kk], lb));
+                    const uint32_t c3 = lds_u32(entry_addr<3>(wd[kk], lb));
+#pragma unroll
+                    for (int t = 0; t < TB; ++t) {
+                        lo[t][0] = dp2a_lo(xp[t][4 * kk + 0], c0, lo[t][0]);
+                        hi[t][0] = dp2a_hi(xp[t][4 * kk + 0], c0, hi[t][0]);
+                        lo[t][1] = dp2a_lo(xp[t][4 * kk + 1], c1, lo[t][1]);
+                        hi[t][1] = dp2a_hi(xp[t][4 * kk + 1], c1, hi[t][1]);
+                        lo[t][0] = dp2a_lo(xp[t][4 * kk + 2], c2, lo[t][0]);
+                        hi[t][0] = dp2a_hi(xp[t][4 * kk + 2], c2, hi[t][0]);
+                        lo[t][1] = dp2a_lo(xp[t][4 * kk + 3], c3, lo[t][1]);
+                        hi[t][1] = dp2a_hi(xp[t][4 * kk + 3], c3, hi[t][1]);
+                    }
+                }
+                const int row = h * kFxUnitRows + r;
+                const uint32_t nv = __shfl_sync(0xffffffffu, nrm_tile, row * 4 + (grp >> 1));
+                const float nrm = f16_bits_to_f32((uint16_t)((grp & 1) ? (nv >> 16) : nv));
+#pragma unroll
+                for (int t = 0; t < TB; ++t) {
+                    // |lo| <= 32 * 16256 * 255 and |hi| <= 32 * 16256 * 128: no int32 overflow
+                    const float v = fmaf((float)(hi[t][0] + hi[t][1]), 256.0f, (float)(lo[t][0] + lo[t][1]));
+                    acc[t][row] = fmaf(nrm, v, acc[t][row]);
+                }
+            }
+        }
+        tile_reduce<TB, NW>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
+                            [&](int t, int rr, float sum) {
+                                const int64_t row = tile * tile_rows + rr;
+                                if (row < p.N) {
+                                    const int tok = p.t0 + t;
+                                    p.Y[(int64_t)tok * p.N + row] = sum * (p.scale[tok] * p.out_scale);
+                                }
+                            });
+    }
+}
+
+template <int NW, int TB>
+cq_status run_cq4_fx(Cq4FxParams p, cudaStream_t st) {
+    static bool attr[64] = {};
+    static std::mutex mu;
+    auto kern = cq4_gemv_fx_kernel<NW, TB>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch();
+    if (dev < 0 || dev >= 64) return CQ_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr[dev]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFxSmem) !=
+                cudaSuccess)
+                return check_launch();
+            attr[dev] = true;
+        }
+    }
+    p.smem_bytes = (uint32_t)kFxSmem;
+    const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
+    int64_t grid = sm_count();
+    if (ntiles < grid) grid = ntiles;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(NW * 32), kFxSmem, st, p);
+}
+
+}  // namespace
+
+// The 16-bit codeword grid of the 4-bit kernel: S = floor(32767 / max |cb|) and
+// C_t = rint(cb_t * S); false when the levels are not all finite or all zero (the
+// fp32-codeword kernel then runs).
+bool cq4_fx_codewords(const float (&lv)[16], int (&cw)[16], float* out_scale) {
+    double amax = 0.0;
+    for (int t = 0; t < 16; ++t) {
+        const double a = lv[t] < 0 ? -(double)lv[t] : (double)lv[t];
+        if (!(a <= 3.0e38)) return false;   // inf or nan
+        if (a > amax) amax = a;
+    }
+    if (!(amax > 1.0e-30)) return false;
+    double S = __builtin_floor(32767.0 / amax);
+    if (S < 1.0) S = 1.0;
+    for (int t = 0; t < 16; ++t) {
+        const double c = __builtin_rint((double)lv[t] * S);
+        cw[t] = (int)(c > 32767.0 ? 32767.0 : (c < -32767.0 ? -32767.0 : c));
+    }
+    *out_scale = (float)(1.0 / (128.0 * S));
+    return true;
+}
+
+// Batch-1 and batch-2 CQ GEMV of 4-bit rows on 16-bit integer codewords.  Requires
+// K % 1024 == 0, K <= 32768, 16-byte aligned operands (checked by the caller).
+cq_status cq4_gemv_fx(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
+                      const cq_codebook* cbk, const int8_t* Xq, const float* scale, int64_t B,
+                      float* Y, cudaStream_t st) {
+    Cq4FxParams p;
+    float lv[16];
+    cq_host_levels(lv, 4, cbk);
+    if (!cq4_fx_codewords(lv, p.cw, &p.out_scale)) return CQ_ERR_UNSUPPORTED;
+    {
+        unsigned int* err = nullptr;
+        const cq_status se = device_error_word(&err);
+        if (se != CQ_OK) return se;
+        p.err = err;
+    }
+    p.norms = norms; p.xq = Xq; p.scale = scale; p.Y = Y;
+    p.N = N; p.K = (int)K; p.nseg = (int)(K / kFxSeg);
+    {
+        const uint64_t rowbytes = (uint64_t)K / 2u;
+        const cq_status se = encode_map(&p.pmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, packed, rowbytes / 4,
+                                        (uint64_t)N, rowbytes, kFxSegBytes / 4, kFxUnitRows);
+        if (se != CQ_OK) return se;
+    }
+    // two tokens share a pass of the 16-warp kernel when each warp owns one segment
+    // (K <= 16384); otherwise every token is a pass of the 32-warp kernel
+    const int step = (B >= 2 && p.nseg <= 16) ? 2 : 1;
+    for (int64_t t0 = 0; t0 < B; t0 += step) {
+        p.t0 = (int)t0;
+        p.ntok = (int)((B - t0) < step ? (B - t0) : step);
+        cq_status s;
+        if (p.ntok == 2) {
+            p.rg = p.nseg >= 16 ? 1 : 16 / p.nseg;
+            s = run_cq4_fx<16, 2>(p, st);
+        } else {
+            p.rg = p.nseg >= 32 ? 1 : 32 / p.nseg;
+            s = run_cq4_fx<32, 1>(p, st);
+        }
+        if (s != CQ_OK) return s;
+    }
+    return CQ_OK;
+}
+
+}  // namespace cq
