@@ -423,10 +423,13 @@ def _capture(torch, fn):
 
 
 def small_report(dev, cb, torch, cq, synth, steps, warmup):
-    """The two small workloads, each reported twice: the latency of one call (one Minueza
-    layer: its 8 Q4_0 GEMVs) replayed as a CUDA graph after an L2 flush, and the streamed
-    throughput of back-to-back calls over distinct copies of the weights spanning 4x the
-    L2 (one graph of all copies).  Both use the batch-1 GEMVs of the decode step."""
+    """Configs 1 and 2, each reported twice as SURVEY-style measurements ask: the latency
+    of one call, replayed as a CUDA graph after an L2 flush, and the streamed throughput
+    of back-to-back calls over distinct copies of the weights spanning 4x the L2 (one
+    graph of all copies).  The calls are the fused decode chain (``cq_gemv_layer``: int8
+    quantization, rotation and GEMV in one launch; ``q4_0_gemv_layer``: every matrix of the
+    layer in one launch); the per-matrix launches of the unfused path are timed beside
+    them (``unfused_latency_us``)."""
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
@@ -465,31 +468,45 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
         g.manual_seed(seed)
         return torch.randn(shape, device=dev, generator=g)
 
-    out = {"timing": "latency: one call (one layer) as a CUDA graph after an L2 flush, median; "
-                     "streamed: one graph over distinct weight copies spanning 4x L2",
+    out = {"timing": "latency: one call as a CUDA graph after an L2 flush, median; streamed: "
+                     "one graph over distinct weight copies spanning 4x L2",
+           "path": "fused decode chain: cq_gemv_layer (a8 + rotation + GEMV, one launch), "
+                   "q4_0_gemv_layer (all matrices of the layer, one launch)",
            "l2_bytes": l2}
-    # CQ-W4A8 512 x 512, batch 1
+    # CQ-W4A8 512 x 512, batch 1: float32 activations in, one launch
     N = K = 512
     packed, norms = cq.cq_encode(gen((N, K), synth.weight_seed(0, 0)) * 0.02, 4, cb)
-    Xq, sc = cq.a8_quantize(gen((1, K), synth.activation_seed(0, 1)))
-    ws = torch.empty((cq.cq_gemv_workspace_bytes(1, K),), dtype=torch.uint8, device=dev)
+    X = gen((1, K), synth.activation_seed(0, 1))
     Y = torch.empty((1, N), dtype=torch.float32, device=dev)
-    nbytes = packed.numel() + 2 * norms.numel() + K + 4 + 4 * N
-    us = latency(lambda: cq.cq_gemv(packed, norms, N, K, 4, cb, Xq, sc, Y=Y, workspace=ws)) * 1e3
+    ws = torch.empty((cq.cq_gemv_workspace_bytes(1, K),), dtype=torch.uint8, device=dev)
+    Xq = torch.empty((1, K), dtype=torch.int8, device=dev)
+    sc = torch.empty((1,), dtype=torch.float32, device=dev)
+    nbytes = packed.numel() + 2 * norms.numel() + 4 * K + 4 * N
+    one = cq.make_gemv_layer([(packed, norms, N, K, X, Y)])
+    us = latency(lambda: cq.cq_gemv_layer(one, 4, cb)) * 1e3
+
+    def unfused():
+        cq.a8_quantize(X, Xq=Xq, scale=sc)
+        cq.cq_gemv(packed, norms, N, K, 4, cb, Xq, sc, Y=Y, workspace=ws)
+
+    us_unfused = latency(unfused) * 1e3
     copies = -(-4 * l2 // nbytes)
     P = copies_of(packed, copies)
     Q = copies_of(norms, copies)
-
-    def stream_cq():
-        for c in range(copies):
-            cq.cq_gemv(P[c], Q[c], N, K, 4, cb, Xq, sc, Y=Y, workspace=ws)
-
-    ms = streamed(stream_cq)
-    out["cq_w4a8_512x512"] = {"latency_us": round(us, 1), "bytes_per_call": nbytes,
-                              "copies": copies, "streamed_us_per_call": round(ms * 1e3 / copies, 2),
-                              "streamed_GBps": round(copies * nbytes / (ms * 1e-3) / 1e9, 1),
-                              "streamed_Gweights_per_s": round(copies * N * K / (ms * 1e-3) / 1e9, 2)}
-    del P, Q, packed, norms
+    calls = [cq.make_gemv_layer([(P[c], Q[c], N, K, X, Y)]) for c in range(copies)]
+    ms = streamed(lambda: [cq.cq_gemv_layer(c1, 4, cb) for c1 in calls])
+    per = cq.LAYER_MAX_PROBLEMS
+    groups = [cq.make_gemv_layer([(P[c], Q[c], N, K, X, Y) for c in range(c0, min(c0 + per, copies))])
+              for c0 in range(0, copies, per)]
+    ms16 = streamed(lambda: [cq.cq_gemv_layer(g1, 4, cb) for g1 in groups])
+    out["cq_w4a8_512x512"] = {
+        "latency_us": round(us, 1), "unfused_latency_us": round(us_unfused, 1),
+        "launches": 1, "unfused_launches": 2, "bytes_per_call": nbytes, "copies": copies,
+        "streamed_us_per_call": round(ms * 1e3 / copies, 2),
+        "streamed_GBps": round(copies * nbytes / (ms * 1e-3) / 1e9, 1),
+        "streamed_Gweights_per_s": round(copies * N * K / (ms * 1e-3) / 1e9, 2),
+        "streamed_16_per_launch_GBps": round(copies * nbytes / (ms16 * 1e-3) / 1e9, 1)}
+    del P, Q, calls, groups, packed, norms
     # one Minueza layer in Q4_0 (8 matrices with the tied lm_head), batch 1
     layer = []
     xs = {}
@@ -500,28 +517,26 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
         layer.append((m, blocks, torch.empty((1, m.N), dtype=torch.float32, device=dev)))
     lbytes = sum(b.numel() + 4 * m.K + 4 * m.N for m, b, _ in layer)
     lweights = sum(m.N * m.K for m, _, _ in layer)
+    fused = cq.make_q4_0_layer([(b, m.N, m.K, xs[m.K], y) for m, b, y in layer])
+    us = latency(lambda: cq.q4_0_gemv_layer(fused)) * 1e3
 
     def one_layer():
         for m, b, y in layer:
             cq.q4_0_gemv(b, m.N, m.K, xs[m.K], Y=y)
 
-    us = latency(one_layer) * 1e3
+    us_unfused = latency(one_layer) * 1e3
     copies = -(-4 * l2 // lbytes)
     reps = [(m, copies_of(b, copies), y) for m, b, y in layer]
-
-    def stream_layers():
-        for c in range(copies):
-            for m, b, y in reps:
-                cq.q4_0_gemv(b[c], m.N, m.K, xs[m.K], Y=y)
-
-    ms = streamed(stream_layers)
-    out["minueza_q4_0_layer"] = {"latency_us": round(us, 1), "launches": len(layer),
+    lcalls = [cq.make_q4_0_layer([(b[c], m.N, m.K, xs[m.K], y) for m, b, y in reps]) for c in range(copies)]
+    ms = streamed(lambda: [cq.q4_0_gemv_layer(c1) for c1 in lcalls])
+    out["minueza_q4_0_layer"] = {"latency_us": round(us, 1), "unfused_latency_us": round(us_unfused, 1),
+                                 "launches": 1, "unfused_launches": len(layer),
                                  "bytes_per_layer": lbytes, "copies": copies,
                                  "streamed_us_per_layer": round(ms * 1e3 / copies, 2),
                                  "streamed_GBps": round(copies * lbytes / (ms * 1e-3) / 1e9, 1),
                                  "streamed_Gweights_per_s": round(copies * lweights / (ms * 1e-3) / 1e9, 2)}
     cq.cq_device_error()
-    del reps, layer, flush
+    del reps, layer, lcalls, flush
     torch.cuda.empty_cache()
     return out
 

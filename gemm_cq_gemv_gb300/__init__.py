@@ -14,7 +14,9 @@ from ._binding import (CQError, CQ_TERNARY, LIB_PATH, NOALLOC_MAX_ELEMS, SIGNATU
                        cq_gemm_problem, cq_gemm_workspace_bytes, cq_device_error,
                        make_gemm_problems, q4_0_gemm, q4_0_gemm_workspace_bytes,
                        cq_probe_bounded_wait, a8_quantize_groups, a8_fake_quant_groups,
-                       cq_field_bits, cq_levels, cq_gemv_lut)
+                       cq_field_bits, cq_levels, cq_gemv_lut, cq_gemv_problem, q4_0_gemv_problem,
+                       make_gemv_layer, make_q4_0_layer, cq_gemv_layer, q4_0_gemv_layer,
+                       LAYER_MAX_PROBLEMS, LAYER_MAX_K)
 
 __all__ = ["CQError", "CQ_TERNARY", "LIB_PATH", "NOALLOC_MAX_ELEMS", "SIGNATURES", "a8_quantize", "cq_abi_version", "cq_codebook",
            "cq_codebook_fit", "cq_encode", "cq_gemv", "cq_gemv_noalloc", "cq_gemv_workspace_bytes",
@@ -22,4 +24,6 @@ __all__ = ["CQError", "CQ_TERNARY", "LIB_PATH", "NOALLOC_MAX_ELEMS", "SIGNATURES
            "cq_gemm", "cq_gemm_grouped", "cq_gemm_grouped_workspace_bytes", "cq_gemm_problem",
            "cq_gemm_workspace_bytes", "cq_device_error", "make_gemm_problems", "q4_0_gemm",
            "q4_0_gemm_workspace_bytes", "cq_probe_bounded_wait", "a8_quantize_groups",
-           "a8_fake_quant_groups", "cq_field_bits", "cq_levels", "cq_gemv_lut"]
+           "a8_fake_quant_groups", "cq_field_bits", "cq_levels", "cq_gemv_lut", "cq_gemv_problem",
+           "q4_0_gemv_problem", "make_gemv_layer", "make_q4_0_layer", "cq_gemv_layer",
+           "q4_0_gemv_layer", "LAYER_MAX_PROBLEMS", "LAYER_MAX_K"]

@@ -40,6 +40,19 @@ class cq_gemm_problem(ctypes.Structure):
                 ("Y", ctypes.c_void_p)]
 
 
+class cq_gemv_problem(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("norms", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
+
+
+class q4_0_gemv_problem(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("X", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
+
+
+LAYER_MAX_PROBLEMS = 16   # CQ_LAYER_MAX_PROBLEMS
+LAYER_MAX_K = 8192        # CQ_LAYER_MAX_K
+
 _lib = None
 
 _P = ctypes.c_void_p
@@ -77,6 +90,9 @@ SIGNATURES = {
     "q4_0_gemv": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P]),
     "q4_0_gemm_workspace_bytes": (_SZ, [_I64, _I64]),
     "q4_0_gemm": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _SZ, _P]),
+    "cq_gemv_layer": (_INT, [ctypes.POINTER(cq_gemv_problem), _INT, _INT, _INT,
+                             ctypes.POINTER(cq_codebook), _I64, _P]),
+    "q4_0_gemv_layer": (_INT, [ctypes.POINTER(q4_0_gemv_problem), _INT, _I64, _P]),
 }
 
 
@@ -299,6 +315,53 @@ def make_gemm_problems(items):
         arr[i].scale = _ptr(scale, torch.float32, "scale").value
         arr[i].Y = _ptr(Y, torch.bfloat16, "Y").value
     return arr
+
+
+def make_gemv_layer(items):
+    """CQ layer problems from (packed, norms, N, K, X, Y) tuples: X [B][K] float32 and
+    Y [B][N] float32 CUDA tensors.  The array keeps the tensors alive."""
+    arr = (cq_gemv_problem * len(items))()
+    for i, (packed, norms, N, K, X, Y) in enumerate(items):
+        arr[i].packed = _ptr(packed, torch.uint8, "packed").value
+        arr[i].norms = _ptr(norms, torch.int16, "norms").value
+        arr[i].N, arr[i].K = N, K
+        arr[i].X = _ptr(X, torch.float32, "X", 2).value
+        arr[i].Y = _ptr(Y, torch.float32, "Y", 2).value
+        if X.shape[1] != K or Y.shape != (X.shape[0], N):
+            raise ValueError(f"problem {i}: X must be [B, {K}] and Y [B, {N}]")
+    arr._keep = [t for it in items for t in it if isinstance(t, torch.Tensor)]
+    arr._batch = items[0][4].shape[0]
+    return arr
+
+
+def make_q4_0_layer(items):
+    """Q4_0 layer problems from (blocks, N, K, X, Y) tuples (X, Y as for make_gemv_layer)."""
+    arr = (q4_0_gemv_problem * len(items))()
+    for i, (blocks, N, K, X, Y) in enumerate(items):
+        arr[i].blocks = _ptr(blocks, torch.uint8, "blocks").value
+        arr[i].N, arr[i].K = N, K
+        arr[i].X = _ptr(X, torch.float32, "X", 2).value
+        arr[i].Y = _ptr(Y, torch.float32, "Y", 2).value
+        if X.shape[1] != K or Y.shape != (X.shape[0], N):
+            raise ValueError(f"problem {i}: X must be [B, {K}] and Y [B, {N}]")
+    arr._keep = [t for it in items for t in it if isinstance(t, torch.Tensor)]
+    arr._batch = items[0][3].shape[0]
+    return arr
+
+
+def cq_gemv_layer(problems, b, cb, g=128, stream=None):
+    """Fused decode chain: a8 quantization, rotation and the CQ GEMV of every problem of a
+    layer (an array from ``make_gemv_layer``) in one launch."""
+    c = _cbk(cb)
+    _check("cq_gemv_layer", lib().cq_gemv_layer(problems, len(problems), g, b, ctypes.byref(c),
+                                                problems._batch, _stream(stream)))
+
+
+def q4_0_gemv_layer(problems, stream=None):
+    """Fused decode chain: the Q4_0 GEMV of every problem of a layer (an array from
+    ``make_q4_0_layer``) in one launch."""
+    _check("q4_0_gemv_layer", lib().q4_0_gemv_layer(problems, len(problems), problems._batch,
+                                                    _stream(stream)))
 
 
 def cq_gemm_grouped_workspace_bytes(problems, M) -> int:

@@ -926,6 +926,11 @@ extern "C" cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64
         const cq_status s = cq4_gemv_fx(packed, norms, N, K, cbk, Xq, scale, B, Y, st);
         if (s != CQ_ERR_UNSUPPORTED) return s;
     }
+    // one token of 1-bit, 2-bit or ternary rows: the table-lookup kernel (one lookup and
+    // one add per 4-bit nibble, lut.cu) once every SM gets a full block of 16 rows; its
+    // per-CTA table costs more than it saves on fewer rows
+    if ((b == 1 || b == 2 || b == CQ_TERNARY) && B == 1 && N >= 16 * (int64_t)sm_count())
+        return cq_gemv_lut(packed, norms, N, K, g, b, cbk, Xq, scale, B, Y, stream);
     // segments per warp: 1 up to 16 segments (K <= 16384), else 2 (K <= 32768); two
     // tokens per pass when each warp owns a single segment
     const int nseg = (int)((K + kSeg - 1) / kSeg);

@@ -140,10 +140,17 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  *   Y[t][o] = s_t * sum_j (norm[o][j] / 128) * sum_i cb[idx[o][j][i]] * xr[t][128 j + i]
  * with xr = Hu @ Xq per group (the rotated int8 activations, exact integers), which
  * equals (W_hat @ (s * Xq)^T)^T in real arithmetic because Hu is symmetric.
- * Two execution paths, chosen from the arguments:
- *   - B <= 2, or N not a multiple of 16: the CUDA-core GEMV, fp32 products and
- *     accumulation; at B <= 2 the rotation happens inside the kernel, otherwise once per
- *     call into `workspace`, shared by every row.
+ * Four execution paths, chosen from the arguments:
+ *   - b = 4, B <= 2, N >= 16, K a multiple of 1024: the CUDA-core GEMV on 16-bit integer
+ *     codewords, C = rint(cb * S) with S = floor(32767 / max |cb|) (at most 4.2e-5
+ *     absolute rounding of a Lloyd-Max level): exact integer dot products per 32
+ *     positions, scaled by the fp16 group norm and summed in fp32.  The rotation happens
+ *     inside the kernel; `workspace` is not touched.
+ *   - b = 1, 2 or CQ_TERNARY, B = 1, N >= 16 x the number of SMs: the table-lookup kernel
+ *     of cq_gemv_lut (below); `workspace` is not touched.
+ *   - otherwise at B <= 2, or N not a multiple of 16: the CUDA-core GEMV on fp32
+ *     codewords, fp32 products and accumulation; at B <= 2 the rotation happens inside
+ *     the kernel, otherwise once per call into `workspace`, shared by every row.
  *   - B >= 3, N a multiple of 16 (any code): the tensor-core pipeline of cq_gemm with
  *     32-token tiles (4- and 2-bit rows reach shared memory per 64-index stage, 1- and
  *     3-bit rows per 128-index slab).  The weights are decoded once for all tokens; the operands are fp16
@@ -258,6 +265,51 @@ cq_status cq_device_error(void* stream);
 cq_status cq_gemv_noalloc(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K,
                           int g, int b, const cq_codebook* cbk, const int8_t* Xq,
                           const float* scale, int64_t B, float* Y, void* stream);
+
+/* ---- Fused decode chain of one layer (Needle .cact page, §三: a layer's matrices are stored
+ * layer-major, pre-transposed to [out, in], and decode multiplies each by an activation
+ * vector; smolmaxxing page, kernel table: the ragged-N lm_head runs on the same kernel).
+ * One launch covers every problem of `probs` (host array of `count` problems, at most
+ * CQ_LAYER_MAX_PROBLEMS), for B = 1 or 2 tokens:
+ *   cq_gemv_layer: for each problem, the per-token int8 quantization of its float32
+ *     activations (the rule of a8_quantize, bit for bit), the rotation xr = Hu @ q per
+ *     128-group and the product of cq_gemv,
+ *       Y[t][o] = s_t * sum_j (norm[o][j] / 128) * sum_i cb[idx[o][j][i]] * xr[t][128 j + i],
+ *     for any code b (1..4 or CQ_TERNARY), fp32 codewords, products and accumulation;
+ *   q4_0_gemv_layer: for each problem, the product of q4_0_gemv,
+ *       Y[t][o] = sum_blocks fp32(d) * sum_k (nib - 8) * X[t][k], float32.
+ * Meant for the decode of small layers, where a launch per matrix costs more than the
+ * matrix: the grid follows the rows (up to three 256-thread CTAs per SM, each on a
+ * contiguous run of 256 / G-row blocks, G = the power of two of threads per row covering
+ * its 32-position chunks), each CTA prepares the activations of the problems it serves
+ * in shared memory, and no workspace is used.  Every sum has a fixed order, so reruns
+ * are bit-identical.  Problems are independent (their outputs must not overlap their
+ * inputs).
+ *   packed, norms / blocks: as written by cq_encode / q4_0_quantize; N >= 1; K >= 1 with
+ *   K % 128 == 0 for CQ; K <= CQ_LAYER_MAX_K; X [B][K] float32; Y [B][N] float32; every
+ *   pointer 16-byte aligned.
+ * Errors: INVALID_ARG (NULL, count < 1, B < 1, g != 128, K % 128 for CQ, a bad code),
+ * UNSUPPORTED (count, B or K above the limits, N above 2^40), ALIGNMENT, CUDA. */
+#define CQ_LAYER_MAX_PROBLEMS 16
+#define CQ_LAYER_MAX_K 8192
+typedef struct cq_gemv_problem {
+    const uint8_t* packed;
+    const uint16_t* norms;
+    int64_t N;
+    int64_t K;
+    const float* X;
+    float* Y;
+} cq_gemv_problem;
+cq_status cq_gemv_layer(const cq_gemv_problem* probs, int count, int g, int b,
+                        const cq_codebook* cbk, int64_t B, void* stream);
+typedef struct q4_0_gemv_problem {
+    const uint8_t* blocks;
+    int64_t N;
+    int64_t K;
+    const float* X;
+    float* Y;
+} q4_0_gemv_problem;
+cq_status q4_0_gemv_layer(const q4_0_gemv_problem* probs, int count, int64_t B, void* stream);
 
 /* ---- A7: Q4_0 quantize (KMCU page, §2, §3).
  *   W [N][K] float32 -> blocks [N][ceil(K/32) * 18] uint8; per block: d = amax / 8

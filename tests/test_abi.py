@@ -210,3 +210,45 @@ def test_header_is_plain_c():
         r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
                             "-fsyntax-only", "-x", "c", h], capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def _cq_layer(entries):
+    arr = (cq.cq_gemv_problem * len(entries))()
+    for i, (packed, norms, N, K, X, Y) in enumerate(entries):
+        arr[i].packed, arr[i].norms, arr[i].N, arr[i].K, arr[i].X, arr[i].Y = packed, norms, N, K, X, Y
+    return arr
+
+
+def _q4_layer(entries):
+    arr = (cq.q4_0_gemv_problem * len(entries))()
+    for i, (blocks, N, K, X, Y) in enumerate(entries):
+        arr[i].blocks, arr[i].N, arr[i].K, arr[i].X, arr[i].Y = blocks, N, K, X, Y
+    return arr
+
+
+def test_layer_validation(lib):
+    """The fused decode chain rejects every bad argument on the host, before any launch."""
+    INV, ALN, UNS = 1, 2, 3
+    f, q = lib.cq_gemv_layer, lib.q4_0_gemv_layer
+    ok = (A, A, 8, 512, A, A)
+    assert f(_cq_layer([ok]), 0, 128, 4, _cb(), 1, None) == INV              # no problem
+    assert f(None, 1, 128, 4, _cb(), 1, None) == INV
+    assert f(_cq_layer([ok]), 1, 64, 4, _cb(), 1, None) == INV               # g
+    assert f(_cq_layer([ok]), 1, 128, 6, _cb(), 1, None) == INV              # code
+    assert f(_cq_layer([ok]), 1, 128, 4, None, 1, None) == INV               # codebook
+    assert f(_cq_layer([ok]), 1, 128, 4, _cb(), 0, None) == INV              # B
+    assert f(_cq_layer([ok]), 1, 128, 4, _cb(), 3, None) == UNS              # B above 2
+    assert f(_cq_layer([ok, (A, A, 8, 500, A, A)]), 2, 128, 4, _cb(), 1, None) == INV   # K % 128
+    assert f(_cq_layer([ok, (A, A, 0, 512, A, A)]), 2, 128, 4, _cb(), 1, None) == INV   # N
+    assert f(_cq_layer([ok, (A, None, 8, 512, A, A)]), 2, 128, 4, _cb(), 1, None) == INV
+    assert f(_cq_layer([ok, (A, A, 8, 512, M, A)]), 2, 128, 4, _cb(), 1, None) == ALN
+    assert f(_cq_layer([(A, A, 8, cq.LAYER_MAX_K + 128, A, A)]), 1, 128, 4, _cb(), 1, None) == UNS
+    many = _cq_layer([ok] * (cq.LAYER_MAX_PROBLEMS + 1))
+    assert f(many, cq.LAYER_MAX_PROBLEMS + 1, 128, 4, _cb(), 1, None) == UNS
+    okq = (A, 8, 312, A, A)
+    assert q(_q4_layer([okq]), 0, 1, None) == INV
+    assert q(_q4_layer([okq]), 1, 3, None) == UNS
+    assert q(_q4_layer([okq, (A, 8, 0, A, A)]), 2, 1, None) == INV             # K
+    assert q(_q4_layer([okq, (None, 8, 312, A, A)]), 2, 1, None) == INV
+    assert q(_q4_layer([okq, (A, 8, 312, A, M)]), 2, 1, None) == ALN
+    assert q(_q4_layer([(A, 8, cq.LAYER_MAX_K + 1, A, A)]), 1, 1, None) == UNS

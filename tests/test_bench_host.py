@@ -82,8 +82,33 @@ class _FakeLib:
         return (torch.zeros((N, K // 128, 16 * f), dtype=torch.uint8),
                 torch.zeros((N, K // 128), dtype=torch.int16))
 
-    def a8_quantize(self, X):
+    def a8_quantize(self, X, Xq=None, scale=None):
+        self._count("a8_quantize")
         return torch.zeros(X.shape, dtype=torch.int8), torch.ones(X.shape[0])
+
+    LAYER_MAX_PROBLEMS = cqlib.LAYER_MAX_PROBLEMS
+
+    def make_gemv_layer(self, items):
+        for packed, norms, N, K, X, Y in items:
+            self._ok(packed), self._ok(norms)
+            assert packed.shape == (N, K // 128, 64) and X.shape == (1, K) and Y.shape == (1, N)
+        assert len(items) <= self.LAYER_MAX_PROBLEMS
+        return list(items)
+
+    def make_q4_0_layer(self, items):
+        for blocks, N, K, X, Y in items:
+            self._ok(blocks)
+            assert blocks.shape == (N, -(-K // 32) * 18) and X.shape == (1, K) and Y.shape == (1, N)
+        assert len(items) <= self.LAYER_MAX_PROBLEMS
+        return list(items)
+
+    def cq_gemv_layer(self, probs, b, cb):
+        self._count("cq_gemv_layer")
+        self.calls["cq_layer_problems"] = self.calls.get("cq_layer_problems", 0) + len(probs)
+
+    def q4_0_gemv_layer(self, probs):
+        self._count("q4_0_gemv_layer")
+        assert len(probs) == 8
 
     def cq_gemv(self, packed, norms, N, K, b, cb, Xq, s, Y=None, workspace=None):
         self._ok(packed), self._ok(norms)
@@ -130,13 +155,19 @@ def test_small_report_shapes_and_copies(monkeypatch):
     lib = _FakeLib()
     out = bench.small_report("cpu", None, _fake_torch(), lib, synth, 2, 1)
     a, b = out["cq_w4a8_512x512"], out["minueza_q4_0_layer"]
-    assert a["bytes_per_call"] == 512 * 512 // 2 + 2 * 512 * 4 + 512 + 4 + 4 * 512
+    assert a["bytes_per_call"] == 512 * 512 // 2 + 2 * 512 * 4 + 4 * 512 + 4 * 512
     assert a["copies"] * a["bytes_per_call"] >= 4 * out["l2_bytes"]
-    assert b["launches"] == 8 and b["copies"] * b["bytes_per_layer"] >= 4 * out["l2_bytes"]
+    assert a["launches"] == 1 and b["launches"] == 1 and b["unfused_launches"] == 8
+    assert b["copies"] * b["bytes_per_layer"] >= 4 * out["l2_bytes"]
     assert b["bytes_per_layer"] >= 6_499_800            # the layer's Q4_0 blocks alone
-    # latency: capture + (warmup + steps) replays; streamed: capture + 1 + 3 replays
-    assert lib.calls["cq_gemv"] == 1 + 3 + (1 + 1 + 3) * a["copies"]
-    assert lib.calls["q4_0_gemv"] == 8 * (1 + 3) + 8 * (1 + 1 + 3) * b["copies"]
+    # latency: capture + (warmup + steps) replays; streamed: capture + 1 + 3 replays, once
+    # with one call per copy and once with 16 copies per call
+    n16 = -(-a["copies"] // lib.LAYER_MAX_PROBLEMS)
+    assert lib.calls["cq_gemv_layer"] == 1 + 3 + (1 + 1 + 3) * (a["copies"] + n16)
+    assert lib.calls["cq_layer_problems"] == 1 + 3 + (1 + 1 + 3) * 2 * a["copies"]
+    assert lib.calls["cq_gemv"] == lib.calls["a8_quantize"] == 1 + 3     # the unfused latency
+    assert lib.calls["q4_0_gemv_layer"] == 1 + 3 + (1 + 1 + 3) * b["copies"]
+    assert lib.calls["q4_0_gemv"] == 8 * (1 + 3)
     json.dumps(out)
 
 
