@@ -468,8 +468,12 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
         g.manual_seed(seed)
         return torch.randn(shape, device=dev, generator=g)
 
+    tiny = torch.empty((1,), dtype=torch.float32, device=dev)
+    floor_us = latency(lambda: tiny.zero_()) * 1e3   # one trivial kernel, timed the same way
     out = {"timing": "latency: one call as a CUDA graph after an L2 flush, median; streamed: "
                      "one graph over distinct weight copies spanning 4x L2",
+           "launch_floor_us": round(floor_us, 1),
+           "launch_floor": "latency of one trivial kernel (a 1-element fill) measured the same way",
            "path": "fused decode chain: cq_gemv_layer (a8 + rotation + GEMV, one launch), "
                    "q4_0_gemv_layer (all matrices of the layer, one launch)",
            "l2_bytes": l2}
@@ -628,6 +632,9 @@ def gpu_arm(args, rank, world, local_rank):
     cb = cq.make_codebook(load_codebook())
     if args.narrow_only:
         print(json.dumps(narrow_report(dev, cb, torch, cq, synth, 10, args.warmup)), flush=True)
+        return
+    if args.small_only:
+        print(json.dumps(small_report(dev, cb, torch, cq, synth, 10, args.warmup)), flush=True)
         return
     if args.prefill_only:
         pf = build_prefill(dev, cb, torch, cq, synth, args.prefill_m)
@@ -1039,6 +1046,8 @@ def main(argv=None):
                     help="skip the small-workload report (CQ 512x512, one Minueza Q4_0 layer)")
     ap.add_argument("--no-narrow", action="store_true",
                     help="skip the 1-bit / 2-bit / ternary decode report (cq_gemv vs cq_gemv_lut)")
+    ap.add_argument("--small-only", action="store_true",
+                    help="print only the small-workload report (profiling runs)")
     ap.add_argument("--narrow-only", action="store_true",
                     help="print only that report (the child process the full run starts)")
     args = ap.parse_args(argv)

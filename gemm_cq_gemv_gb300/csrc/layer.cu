@@ -148,6 +148,42 @@ __global__ void __launch_bounds__(kLThreads) layer_gemv_kernel(const __grid_cons
         const LayerProblem& pr = p.pr[q];
         const int K = pr.K;
         const int nch = (K + 31) / 32;                    // 32-position chunks (Q4_0 blocks)
+        // this item's rows: rows_per_cta = kLThreads / G, one row per G threads; thread j of
+        // a row takes chunks j, j + G, ...
+        const int G = pr.G;
+        const int rows = kLThreads / G;
+        const int64_t row = (it - pr.item0) * rows + tid / G;
+        const int j = tid & (G - 1);
+        const bool live = row < pr.N && j < nch;
+        // the first chunk's weights are requested before the activations are prepared, so
+        // that the two memory round trips overlap
+        const int f = kCQ ? p.field : 4;
+        const int64_t rowbytes = kCQ ? (int64_t)(K / kGroup) * 16 * f : (int64_t)nch * 18;
+        const uint8_t* wrow = pr.w + (live ? row : 0) * rowbytes;
+        auto load_chunk = [&](int c, uint32_t (&wv)[5], uint32_t& sh, uint16_t& nb) {
+            if (kCQ) {
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(wrow + (int64_t)c * 4 * f);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) wv[k] = k < f ? __ldg(src + k) : 0u;
+                wv[4] = 0u;
+                sh = 0u;
+                nb = __ldg(pr.norms + row * (K / kGroup) + (c >> 2));
+            } else {
+                // the 18-byte block (2-byte aligned) from the aligned words around it: at
+                // offset 0 mod 4 its last two bytes are read as a half word, so that no
+                // byte past the block is touched
+                const uintptr_t a = reinterpret_cast<uintptr_t>(wrow + (int64_t)c * 18);
+                const uint32_t* w4 = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
+                sh = (uint32_t)(a & 3) * 8u;   // 0 or 16
+#pragma unroll
+                for (int k = 0; k < 4; ++k) wv[k] = __ldg(w4 + k);
+                wv[4] = sh ? __ldg(w4 + 4) : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(w4 + 4));
+                nb = 0;
+            }
+        };
+        uint32_t wv0[5] = {0u, 0u, 0u, 0u, 0u}, sh0 = 0u;
+        uint16_t nb0 = 0;
+        if (live) load_chunk(j, wv0, sh0, nb0);
         if (q != cur) {
             // prepare this problem's activations (the previous problem's are no longer read)
             __syncthreads();
@@ -173,31 +209,27 @@ __global__ void __launch_bounds__(kLThreads) layer_gemv_kernel(const __grid_cons
             __syncthreads();
             cur = q;
         }
-        // this item's rows: rows_per_cta = kLThreads / G, one row per G threads
-        const int G = pr.G;
-        const int rows = kLThreads / G;
-        const int64_t row = (it - pr.item0) * rows + tid / G;
-        const int j = tid & (G - 1);
         float accv[kLMaxTB] = {0.0f, 0.0f};
-        if (row < pr.N) {
-            if (kCQ) {
-                const int f = p.field;
-                const int64_t rowbytes = (int64_t)(K / kGroup) * 16 * f;
-                const uint8_t* wr = pr.w + row * rowbytes;
-                const uint16_t* nr = pr.norms + row * (K / kGroup);
-                for (int c = j; c < nch; c += G) {
-                    // 32 indices of f bits = 4 f bytes, 4-byte aligned
-                    uint32_t wd[4];
-                    const uint32_t* src = reinterpret_cast<const uint32_t*>(wr + (int64_t)c * 4 * f);
+        if (live) {
+            for (int c = j; c < nch; c += G) {
+                uint32_t wv[5], sh;
+                uint16_t nb;
+                if (c == j) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) wd[k] = k < f ? __ldg(src + k) : 0u;
-                    const float nrm = f16_bits_to_f32(__ldg(nr + (c >> 2)));
-                    float s0[kLMaxTB] = {0.0f, 0.0f}, s1[kLMaxTB] = {0.0f, 0.0f};
+                    for (int k = 0; k < 5; ++k) wv[k] = wv0[k];
+                    sh = sh0;
+                    nb = nb0;
+                } else {
+                    load_chunk(c, wv, sh, nb);
+                }
+                float s0[kLMaxTB] = {0.0f, 0.0f}, s1[kLMaxTB] = {0.0f, 0.0f};
+                if (kCQ) {
+                    const float nrm = f16_bits_to_f32(nb);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int pos = f * i;
-                        uint32_t v = wd[pos >> 5] >> (pos & 31);
-                        if ((pos & 31) + f > 32) v |= wd[(pos >> 5) + 1] << (32 - (pos & 31));
+                        uint32_t v = wv[pos >> 5] >> (pos & 31);
+                        if ((pos & 31) + f > 32) v |= wv[(pos >> 5) + 1] << (32 - (pos & 31));
                         const float cw = tab[(v & ((1u << f) - 1u)) * 32 + lane];
 #pragma unroll
                         for (int t = 0; t < kLMaxTB; ++t) {
@@ -210,29 +242,14 @@ __global__ void __launch_bounds__(kLThreads) layer_gemv_kernel(const __grid_cons
                     }
 #pragma unroll
                     for (int t = 0; t < kLMaxTB; ++t) accv[t] = fmaf(nrm, s0[t] + s1[t], accv[t]);
-                }
-            } else {
-                const int64_t rowbytes = (int64_t)nch * 18;
-                const uint8_t* base = pr.w + row * rowbytes;
-                for (int c = j; c < nch; c += G) {
-                    // the 18-byte block (2-byte aligned) from the aligned words around it: at
-                    // offset 0 mod 4 its last two bytes are read as a half word, so that no
-                    // byte past the block is touched
-                    const uintptr_t a = reinterpret_cast<uintptr_t>(base + (int64_t)c * 18);
-                    const uint32_t* w4 = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
-                    const uint32_t sh = (uint32_t)(a & 3) * 8u;   // 0 or 16
-                    uint32_t wv[5];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) wv[k] = __ldg(w4 + k);
-                    wv[4] = sh ? __ldg(w4 + 4) : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(w4 + 4));
+                } else {
                     const float d = f16_bits_to_f32((uint16_t)(wv[0] >> sh));
-                    float s0[kLMaxTB] = {0.0f, 0.0f}, s1[kLMaxTB] = {0.0f, 0.0f};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t nw = __funnelshift_rc(wv[k], wv[k + 1], sh + 16u);   // shift 16 or 32
 #pragma unroll
                         for (int b = 0; b < 8; ++b) {
-                            // nibble 8k + b: even index in the low half of byte b / 2
+                            // nibble 8k + b: even index in the low half of byte b / 2;
                             // (2^23 + nib) - (2^23 + 8) = nib - 8, exactly
                             const float wq = __uint_as_float(0x4B000000u | ((nw >> (4 * b)) & 15u)) - 8388616.0f;
 #pragma unroll

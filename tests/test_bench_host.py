@@ -163,6 +163,7 @@ def test_small_report_shapes_and_copies(monkeypatch):
     # latency: capture + (warmup + steps) replays; streamed: capture + 1 + 3 replays, once
     # with one call per copy and once with 16 copies per call
     n16 = -(-a["copies"] // lib.LAYER_MAX_PROBLEMS)
+    assert out["launch_floor_us"] > 0
     assert lib.calls["cq_gemv_layer"] == 1 + 3 + (1 + 1 + 3) * (a["copies"] + n16)
     assert lib.calls["cq_layer_problems"] == 1 + 3 + (1 + 1 + 3) * 2 * a["copies"]
     assert lib.calls["cq_gemv"] == lib.calls["a8_quantize"] == 1 + 3     # the unfused latency
