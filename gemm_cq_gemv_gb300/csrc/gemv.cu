@@ -438,10 +438,10 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) cq_gemv_kernel(const __grid_c
 // every row.  The 18-byte blocks of a row segment are staged in shared memory - through
 // the warp's ring when rows and segments are 16-byte aligned, else by guarded 16-byte
 // loads into one buffer per warp - and each lane reads its block with five aligned
-// 32-bit loads.  A nibble is decoded without a table: one byte permute drops it into
-// the mantissa of 128.0f, giving exactly 128 + nib; an even/odd pair multiplies the
-// activation pair with two scalar FMAs; the constant 128 (and the -8 of the format) is
-// removed per block with a precomputed sum of the activations.
+// 32-bit loads.  The lane's activations of a block become 24-bit fixed-point integers
+// once (q4_fix), split into three byte planes; a block then costs, per packed word of
+// eight nibbles, two masks and six dp4a (nibble bytes times activation bytes, exact in
+// int32), and one scale per block.
 // ---------------------------------------------------------------------------------
 struct Q40GemvParams {
     CUtensorMap bmap;     // blocks as [N][nblk * 18 / 4] uint32, box 144 x kUnitRows (nblk % 8 == 0)
@@ -461,65 +461,124 @@ struct Q40GemvParams {
 constexpr int kStage = 608;     // >= 37 chunks of 16 B, per row (unaligned staging)
 constexpr int kQSeg = 576;      // 32 blocks of 18 B (ring staging)
 
+// A lane's 32 activations of one block as a 24-bit fixed-point integer per position,
+// X_i = rint(x_i * 2^e) with 2^e the power of two that brings the block's largest |x|
+// into [2^21, 2^22): the rounding error is at most 2^-23 of that largest value, the
+// precision of an fp32 mantissa.  X_i = X0_i + 256 X1_i + 65536 X2_i (bytes X0, X1
+// unsigned, X2 signed); plane p packs byte p of the even positions 8k, 8k+2, 8k+4, 8k+6
+// (e[p][k]) and of the odd ones (o[p][k]) in the order of the nibbles of packed word k.
+struct Q4X {
+    uint32_t e[3][4], o[3][4];
+    int c[3];      // 8 * sum_i plane_p(X_i): the -8 of the format, per plane
+    float inv;     // 2^-e (NaN when the block holds a non-finite activation)
+};
+
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// byte P of a, b, c, d -> bytes 0..3
+template <int P>
+__device__ __forceinline__ uint32_t pack_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    uint32_t lo, hi, r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(lo) : "r"(a), "r"(b), "n"(P | ((4 + P) << 4)));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(c), "r"(d), "n"(P | ((4 + P) << 4)));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "n"(0x5410));
+    return r;
+}
+
+__device__ __forceinline__ void q4_fix(const float (&x)[32], Q4X& q) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float a;
+        asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(amax), "f"(fabsf(x[i])));
+        amax = a;
+    }
+    int E = (int)(__float_as_uint(amax) >> 23);   // amax < 2^(E - 126)
+    const bool finite = E < 255;
+    if (E < 22) E = 22;                            // zero or tiny blocks
+    if (E > 254) E = 254;
+    const float sc = __uint_as_float((uint32_t)(275 - E) << 23);    // 2^(148 - E)
+    q.inv = finite ? __uint_as_float((uint32_t)(E - 21) << 23) : __uint_as_float(0x7fc00000u);
+    uint32_t X[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)   // |x sc| < 2^22: 1.5 * 2^23 + x sc rounds x sc to an integer
+        X[i] = (uint32_t)(__float_as_int(fmaf(x[i], sc, 12582912.0f)) - 0x4B400000);
+    int c0 = 0, c1 = 0, c2 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        q.e[0][k] = pack_bytes<0>(X[8 * k], X[8 * k + 2], X[8 * k + 4], X[8 * k + 6]);
+        q.o[0][k] = pack_bytes<0>(X[8 * k + 1], X[8 * k + 3], X[8 * k + 5], X[8 * k + 7]);
+        q.e[1][k] = pack_bytes<1>(X[8 * k], X[8 * k + 2], X[8 * k + 4], X[8 * k + 6]);
+        q.o[1][k] = pack_bytes<1>(X[8 * k + 1], X[8 * k + 3], X[8 * k + 5], X[8 * k + 7]);
+        q.e[2][k] = pack_bytes<2>(X[8 * k], X[8 * k + 2], X[8 * k + 4], X[8 * k + 6]);
+        q.o[2][k] = pack_bytes<2>(X[8 * k + 1], X[8 * k + 3], X[8 * k + 5], X[8 * k + 7]);
+        c0 = dp4a_uu(q.e[0][k], 0x01010101u, dp4a_uu(q.o[0][k], 0x01010101u, c0));
+        c1 = dp4a_uu(q.e[1][k], 0x01010101u, dp4a_uu(q.o[1][k], 0x01010101u, c1));
+        c2 = dp4a_su(q.e[2][k], 0x01010101u, dp4a_su(q.o[2][k], 0x01010101u, c2));
+    }
+    q.c[0] = 8 * c0;
+    q.c[1] = 8 * c1;
+    q.c[2] = 8 * c2;
+}
+
+// One 18-byte block of a row against the fixed-point activations:
+//   sum_i (nib_i - 8) x_i = 2^-e * sum_p 256^p (sum_i nib_i Xp_i - 8 sum_i Xp_i),
+// each plane's sum exact in int32 (dp4a of the nibble bytes and the activation bytes).
+// A block of nibbles all 8 (every weight 0, e.g. an all-zero row: KMCU page, §2) gives
+// exactly 0.
 template <int TB>
 __device__ __forceinline__ void q4_block(const uint32_t* wp, uint32_t dsh, uint32_t nsh,
-                                         const float2 (&xx)[TB][16], const float (&cblk)[TB],
-                                         float (&acc)[TB][kRows], int r) {
+                                         const Q4X (&xq)[TB], float (&acc)[TB][kRows], int r) {
     // wp: the aligned words covering the block; dsh: bit offset of the fp16 scale in
     // word 0 (0 or 16); nsh = dsh + 16: funnel shift that aligns the nibble bytes
     const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2], w3 = wp[3], w4 = wp[4];
     const float d = f16_bits_to_f32((uint16_t)(w0 >> dsh));
     const uint32_t nw[4] = {__funnelshift_rc(w0, w1, nsh), __funnelshift_rc(w1, w2, nsh),
                             __funnelshift_rc(w2, w3, nsh), __funnelshift_rc(w3, w4, nsh)};
-    // scalar FMAs on four chains per token (the integer pipe, not the FMA pipe, binds)
-    float a4[TB][4];
+    int s0[TB], s1[TB], s2[TB];
 #pragma unroll
-    for (int t = 0; t < TB; ++t) a4[t][0] = a4[t][1] = a4[t][2] = a4[t][3] = 0.0f;
+    for (int t = 0; t < TB; ++t) s0[t] = s1[t] = s2[t] = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         // even-index nibbles (low halves of the bytes) and odd-index nibbles, one per byte
         const uint32_t ev = nw[k] & 0x0F0F0F0Fu, od = (nw[k] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            // byte j -> byte 2 of 0x43000000: the float 2^7 * (1 + nib / 2^7) = 128 + nib
-            const uint32_t sel = 0x7044u | ((uint32_t)j << 8);
-            uint32_t fe, fo;
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fe) : "r"(ev), "r"(0x43000000u), "r"(sel));
-            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(fo) : "r"(od), "r"(0x43000000u), "r"(sel));
-            if constexpr (TB == 1) {
-                a4[0][2 * (j & 1)] = fmaf(__uint_as_float(fe), xx[0][4 * k + j].x, a4[0][2 * (j & 1)]);
-                a4[0][2 * (j & 1) + 1] = fmaf(__uint_as_float(fo), xx[0][4 * k + j].y, a4[0][2 * (j & 1) + 1]);
-            } else {
-                // two tokens: the same FMAs as paired fp32 instructions (fewer issue
-                // slots; one pass of two tokens is ~11 % faster, one token gains nothing)
-                const float2 f = make_float2(__uint_as_float(fe), __uint_as_float(fo));
-#pragma unroll
-                for (int t = 0; t < TB; ++t) {
-                    float2 a = make_float2(a4[t][2 * (j & 1)], a4[t][2 * (j & 1) + 1]);
-                    a = __ffma2_rn(f, xx[t][4 * k + j], a);
-                    a4[t][2 * (j & 1)] = a.x;
-                    a4[t][2 * (j & 1) + 1] = a.y;
-                }
-            }
+        for (int t = 0; t < TB; ++t) {
+            s0[t] = dp4a_uu(ev, xq[t].e[0][k], s0[t]);
+            s0[t] = dp4a_uu(od, xq[t].o[0][k], s0[t]);
+            s1[t] = dp4a_uu(ev, xq[t].e[1][k], s1[t]);
+            s1[t] = dp4a_uu(od, xq[t].o[1][k], s1[t]);
+            s2[t] = dp4a_us(ev, xq[t].e[2][k], s2[t]);
+            s2[t] = dp4a_us(od, xq[t].o[2][k], s2[t]);
         }
     }
-    // sum (nib - 8) x = sum (128 + nib) x - 136 sum x.  A block whose nibbles are all 8
-    // (every weight 0, e.g. an all-zero row: KMCU page, §2) contributes exactly 0 by the
-    // definition; the two terms above would leave a rounding residue, so its scale is
-    // replaced by 0 (the bracket is finite, and 0 times it is exactly 0)
-    const uint32_t off8 = ((nw[0] ^ 0x88888888u) | (nw[1] ^ 0x88888888u)) |
-                          ((nw[2] ^ 0x88888888u) | (nw[3] ^ 0x88888888u));
-    const float dd = off8 ? d : 0.0f;
 #pragma unroll
-    for (int t = 0; t < TB; ++t)
-        acc[t][r] = fmaf(dd, ((a4[t][0] + a4[t][2]) + (a4[t][1] + a4[t][3])) - cblk[t], acc[t][r]);
+    for (int t = 0; t < TB; ++t) {
+        // |s0 - c0| < 2^17 and |s1 - c1| < 2^17: the low two planes in int32
+        const int lo = (s0[t] - xq[t].c[0]) + 256 * (s1[t] - xq[t].c[1]);
+        const float v = fmaf(65536.0f, (float)(s2[t] - xq[t].c[2]), (float)lo);
+        acc[t][r] = fmaf(d * xq[t].inv, v, acc[t][r]);
+    }
 }
 
-// Activation pairs of this lane's blocks and their block sums (x 136), zero outside K;
-// 16-byte loads where the block lies inside K and rows of X are 16-byte aligned.
+// This lane's blocks of activations (zero outside K) in fixed point; 16-byte loads where
+// the block lies inside K and rows of X are 16-byte aligned.
 template <int TB, int SPW>
 __device__ __forceinline__ void q4_load_x(const Q40GemvParams& p, int slot, bool busy, int lane,
-                                          float2 (&xx)[SPW][TB][16], float (&cblk)[SPW][TB]) {
+                                          Q4X (&xq)[SPW][TB]) {
 #pragma unroll
     for (int i = 0; i < SPW; ++i) {
         const int seg = slot + i * kWarps2;
@@ -528,28 +587,18 @@ __device__ __forceinline__ void q4_load_x(const Q40GemvParams& p, int slot, bool
         for (int t = 0; t < TB; ++t) {
             const bool ok = busy && seg < p.nseg && blk < p.nblk && t < p.ntok;
             const float* src = p.X + (int64_t)(p.t0 + t) * p.K + blk * 32;
-            float se = 0.0f, so = 0.0f;
+            float x[32];
             if (ok && (p.K & 3) == 0 && blk * 32 + 32 <= p.K) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 v = __ldg(reinterpret_cast<const float4*>(src) + q);
-                    xx[i][t][2 * q] = make_float2(v.x, v.y);
-                    xx[i][t][2 * q + 1] = make_float2(v.z, v.w);
-                    se += v.x + v.z;
-                    so += v.y + v.w;
+                    x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
                 }
             } else {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int k0 = blk * 32 + 2 * q;
-                    const float a = (ok && k0 < p.K) ? src[2 * q] : 0.0f;
-                    const float b = (ok && k0 + 1 < p.K) ? src[2 * q + 1] : 0.0f;
-                    xx[i][t][q] = make_float2(a, b);
-                    se += a;
-                    so += b;
-                }
+                for (int q = 0; q < 32; ++q) x[q] = (ok && blk * 32 + q < p.K) ? src[q] : 0.0f;
             }
-            cblk[i][t] = 136.0f * (se + so);
+            q4_fix(x, xq[i][t]);
         }
     }
 }
@@ -603,9 +652,8 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
     // the first units are in flight while the activations are loaded
     pdl_wait();
     for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
-    float2 xx[SPW][TB][16];
-    float cblk[SPW][TB];
-    q4_load_x<TB, SPW>(p, slot, true, lane, xx, cblk);
+    Q4X xq[SPW][TB];
+    q4_load_x<TB, SPW>(p, slot, true, lane, xq);
 
     // every staged row starts at byte 0: per-lane word offset and shifts
     const int o = lane * 18;
@@ -638,7 +686,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
 #pragma unroll
                 for (int r = 0; r < kUnitRows; ++r)
                     if (r < nv)
-                        q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xx[i], cblk[i], acc, h * kUnitRows + r);
+                        q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xq[i], acc, h * kUnitRows + r);
             }
         }
         tile_reduce<TB, kWarps2>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
@@ -664,9 +712,8 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_rows_kernel(const Q
     const int slot = w % nsl, rgi = w / nsl;
     const bool busy = rgi < p.rg;
     const uint32_t nbusy = (uint32_t)(nsl * p.rg);
-    float2 xx[SPW][TB][16];
-    float cblk[SPW][TB];
-    q4_load_x<TB, SPW>(p, slot, busy, lane, xx, cblk);
+    Q4X xq[SPW][TB];
+    q4_load_x<TB, SPW>(p, slot, busy, lane, xq);
     __syncthreads();
     if (!busy) return;
 
@@ -726,7 +773,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_rows_kernel(const Q
                     const int o = offs[r] + lane * 18;
                     const uint32_t dsh = (uint32_t)(o & 3) * 8u;
                     const uint32_t* wl = reinterpret_cast<const uint32_t*>(mystage + r * kStage) + (o >> 2);
-                    q4_block<TB>(wl, dsh, dsh + 16u, xx[i], cblk[i], acc, r);
+                    q4_block<TB>(wl, dsh, dsh + 16u, xq[i], acc, r);
                 }
             }
         }
