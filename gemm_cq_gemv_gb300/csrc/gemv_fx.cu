@@ -80,6 +80,9 @@ struct Cq4FxParams {
     int t0;                  // first token of this pass
     int ntok;                // tokens in this pass (<= TB)
     uint32_t smem_bytes;     // dynamic shared memory of the launch
+    int share;               // 1: each 128-group rotated once per CTA, shared in shared memory
+    int64_t tiles_base;      // a CTA takes tiles_base tiles, one more if blockIdx.x < tiles_extra
+    int tiles_extra;
     float out_scale;         // 1 / (128 S)
     int cw[16];              // the 16-bit codewords C_t
 };
@@ -130,6 +133,22 @@ __device__ __forceinline__ void rotate32_int(int (&v)[32], int lane) {
     }
 }
 
+// xr = Hu q of one 128-group held by a warp, lane l with positions 4l..4l+3: spans 1 and 2
+// inside the lane, 4..64 across lanes (exact integers)
+__device__ __forceinline__ void rotate128_int(int (&v)[4], int lane) {
+    const int a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+    v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
+#pragma unroll
+    for (int m = 1; m <= 16; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = __shfl_xor_sync(0xffffffffu, v[j], m);
+            v[j] = upper ? (q - v[j]) : (v[j] + q);
+        }
+    }
+}
+
 template <int NW, int TB>
 __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_constant__ Cq4FxParams p) {
     extern __shared__ __align__(128) unsigned char smem_f[];
@@ -145,12 +164,21 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
     static_assert(holes_fit<NW, TB>(), "the partials must fit the table's holes");
     const uint32_t red_at = cv.take(kSlots * (8 + 4), 8);        // slot barriers and counters
     const uint32_t bar_at = cv.take(NW * kFxRing * 8, 8);
-    const uint32_t cw_at = cv.take(16 * sizeof(int), 16);
-    uint32_t ring_at = 0;
-    for (int v = 0; v < NW; ++v) {
-        const uint32_t at = cv.take(kFxRing * kFxSlot, 128);
-        if (v == w) ring_at = at;
+    // the NW rings (equal sizes: first-fit fills the space below the table, then above)
+    uint32_t ring_at;
+    {
+        constexpr uint32_t kRingB = kFxRing * kFxSlot;
+        const uint32_t a0 = (cv.a + 127u) & ~127u, b0 = (cv.b + 127u) & ~127u;
+        const uint32_t na = a0 < cv.a_end ? (cv.a_end - a0) / kRingB : 0u;
+        const uint32_t nb = (uint32_t)NW > na ? (uint32_t)NW - na : 0u;
+        ring_at = (uint32_t)w < na ? a0 + (uint32_t)w * kRingB : b0 + ((uint32_t)w - na) * kRingB;
+        if (na > 0u) cv.a = a0 + (na < (uint32_t)NW ? na : (uint32_t)NW) * kRingB;
+        if (nb > 0u) {
+            cv.b = b0 + nb * kRingB;
+            if (cv.b > cv.b_end) cv.ok = false;
+        }
     }
+    const uint32_t xr_at = p.share ? cv.take((uint32_t)TB * (uint32_t)p.K * 2u, 16) : 0u;
     if (!cv.ok) {   // the launch's shared memory cannot hold the plan (host sizing error)
         if (tid == 0) atomicOr(p.err, 4u);
         return;
@@ -162,39 +190,24 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
     rd.empty = reinterpret_cast<uint64_t*>(gen(red_at));
     rd.count = reinterpret_cast<uint32_t*>(rd.empty + kSlots);
     uint64_t* rfull = reinterpret_cast<uint64_t*>(gen(bar_at)) + w * kFxRing;
-    int* scw = reinterpret_cast<int*>(gen(cw_at));
     uint8_t* ring = gen(ring_at);
     if (tid == 0) prefetch_tensormap(&p.pmap);
+    // a warp's ring barriers are its own: it initialises them and starts its first copies
+    // at once; the table, the activations and the rotation overlap those copies
     if (lane < kFxRing) mbar_init(&rfull[lane], 1);
     if (tid < kSlots) {
         rd.count[tid] = 0u;
         mbar_init(&rd.empty[tid], 1);
     }
     if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (tid < 16) {   // the payloads, by an unrolled select (no indexed parameter access)
-        int v = 0;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) v = (u == tid) ? p.cw[u] : v;
-        scw[tid] = v;
-    }
-    __syncthreads();
-    // pair table: entry e (a = e & 15, b = e >> 4) = [lo(C_a), lo(C_b), hi(C_a), hi(C_b)]
-    // at tbase + e * 256 + lane * 4
-    for (int i = tid; i < 256 * 32; i += NW * 32) {
-        const int e = i >> 5, l = i & 31;
-        const uint32_t ca = (uint32_t)scw[e & 15], cb = (uint32_t)scw[e >> 4];
-        const uint32_t word = (ca & 0xFFu) | (cb & 0xFFu) << 8 | ((ca >> 8) & 0xFFu) << 16 |
-                              ((cb >> 8) & 0xFFu) << 24;
-        *reinterpret_cast<uint32_t*>(gen(tbase + (uint32_t)e * 256u + (uint32_t)l * 4u)) = word;
-    }
+    __syncwarp();
 
     const int nsl = p.nseg < NW ? p.nseg : NW;
     const int slot = w % nsl, rgi = w / nsl;
     const uint32_t nbusy = (uint32_t)(nsl * p.rg);
     const bool busy = rgi < p.rg;
     const int tile_rows = kRows * p.rg;
-    const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
-    const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t ntk = p.tiles_base + ((int)blockIdx.x < p.tiles_extra ? 1 : 0);
     constexpr int upt = kRows / kFxUnitRows;                    // units per tile
     const int64_t U = busy ? ntk * upt : 0;
 
@@ -215,27 +228,73 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
     pdl_wait();   // the weights and activations may come from the previous kernels
     if (busy)
         for (int64_t u = 0; u < kFxRing - 1 && u < U; ++u) issue((int)u);
+
+    // pair table: entry e (a = e & 15, b = e >> 4) = [lo(C_a), lo(C_b), hi(C_a), hi(C_b)]
+    // at tbase + e * 256 + lane * 4; a thread writes one entry's copies for eight lanes
+    // (lane l holds C_(l & 15); 1024 is a multiple of the block, so every lane takes part)
+    const int cwl = p.cw[lane & 15];
+    for (int i = tid; i < 256 * 4; i += NW * 32) {
+        const int e = i >> 2;
+        const uint32_t ca = (uint32_t)__shfl_sync(0xffffffffu, cwl, e & 15);
+        const uint32_t cb = (uint32_t)__shfl_sync(0xffffffffu, cwl, e >> 4);
+        const uint32_t word = (ca & 0xFFu) | (cb & 0xFFu) << 8 | ((ca >> 8) & 0xFFu) << 16 | ((cb >> 8) & 0xFFu) << 24;
+        const uint4 v4 = make_uint4(word, word, word, word);
+        uint4* dst = reinterpret_cast<uint4*>(gen(tbase + (uint32_t)e * 256u + (uint32_t)(i & 3) * 32u));
+        dst[0] = v4;
+        dst[1] = v4;
+    }
     // this lane's activations: int8 -> Hu q (exact integers) -> int16 pairs
     uint32_t xp[TB][16];
+    if (p.share) {
+        // the segment's eight groups are rotated by its p.rg warps, one group at a time,
+        // and land in shared memory as int16; each lane then reads its 32 positions
+        int16_t* xs = reinterpret_cast<int16_t*>(gen(xr_at));
+        if (busy) {
 #pragma unroll
-    for (int t = 0; t < TB; ++t) {
-        const bool ok = busy && t < p.ntok;
-        const int8_t* src = p.xq + (int64_t)(p.t0 + t) * p.K + slot * kFxSeg + lane * 32;
-        int v[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int4 c = ok ? *reinterpret_cast<const int4*>(src + 16 * h) : make_int4(0, 0, 0, 0);
-            const int wv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int q = 0; q < 16; ++q) v[16 * h + q] = (int)(int8_t)(wv[q >> 2] >> (8 * (q & 3)));
+            for (int t = 0; t < TB; ++t) {
+                for (int g = rgi; g < 8; g += p.rg) {
+                    const int pos = slot * kFxSeg + g * kGroup + 4 * lane;
+                    char4 c = make_char4(0, 0, 0, 0);
+                    if (t < p.ntok) c = *reinterpret_cast<const char4*>(p.xq + (int64_t)(p.t0 + t) * p.K + pos);
+                    int v[4] = {c.x, c.y, c.z, c.w};
+                    rotate128_int(v, lane);
+                    const uint2 pr = make_uint2(((uint32_t)v[0] & 0xFFFFu) | ((uint32_t)v[1] << 16),
+                                                ((uint32_t)v[2] & 0xFFFFu) | ((uint32_t)v[3] << 16));
+                    *reinterpret_cast<uint2*>(xs + (size_t)t * p.K + pos) = pr;
+                }
+            }
         }
-        rotate32_int(v, lane);
+        __syncthreads();   // table and rotated groups complete
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            xp[t][q] = ((uint32_t)v[2 * q] & 0xFFFFu) | ((uint32_t)v[2 * q + 1] << 16);
+        for (int t = 0; t < TB; ++t) {
+            const uint4* src = reinterpret_cast<const uint4*>(xs + (size_t)t * p.K + slot * kFxSeg + lane * 32);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const uint4 q = src[h];
+                xp[t][4 * h] = q.x; xp[t][4 * h + 1] = q.y; xp[t][4 * h + 2] = q.z; xp[t][4 * h + 3] = q.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < TB; ++t) {
+            const bool ok = busy && t < p.ntok;
+            const int8_t* src = p.xq + (int64_t)(p.t0 + t) * p.K + slot * kFxSeg + lane * 32;
+            int v[32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int4 c = ok ? *reinterpret_cast<const int4*>(src + 16 * h) : make_int4(0, 0, 0, 0);
+                const int wv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int q = 0; q < 16; ++q) v[16 * h + q] = (int)(int8_t)(wv[q >> 2] >> (8 * (q & 3)));
+            }
+            rotate32_int(v, lane);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                xp[t][q] = ((uint32_t)v[2 * q] & 0xFFFFu) | ((uint32_t)v[2 * q + 1] << 16);
+        }
+        __syncthreads();   // table complete
     }
-    __syncthreads();   // the table is complete
-    if (!busy) return;   // warps left over when the segments do not divide 16
+    if (!busy) return;   // warps left over when the segments do not divide the CTA
 
     const uint32_t lb = tbase | ((uint32_t)lane << 2);
     const int grp = lane >> 2;   // this lane's group within a segment's 8
@@ -336,6 +395,11 @@ cq_status run_cq4_fx(Cq4FxParams p, cudaStream_t st) {
     const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int64_t grid = sm_count();
     if (ntiles < grid) grid = ntiles;
+    p.tiles_base = ntiles / grid;
+    p.tiles_extra = (int)(ntiles % grid);
+    // several warps per segment: rotate each group once and share it (TB * K * 2 bytes of
+    // shared memory beside the rings and the table)
+    p.share = (p.rg >= 2 && p.K <= 8192) ? 1 : 0;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(NW * 32), kFxSmem, st, p);
 }
 
