@@ -29,16 +29,21 @@
 // magnify it) to the fp32-codeword kernel.
 //
 // Layout of the work: one CTA of NW warps per SM (32 for one token, 16 for two, whose
-// activations take twice the registers), persistent over row tiles.  Warp w owns the
-// K-segment (w mod nsl) of 1024 positions - lane l the positions [32 l, 32 l + 32) - and
-// the row group w / nsl of every tile (8 rows per group).  Packed rows arrive through a
-// per-warp ring of kFxRing slots of 2 rows x one segment (1 KB), each filled by one
-// tensor copy issued by one lane.  The tensor-copy unit starts at most ~47 copies per
-// microsecond per SM (measured), so the copies are whole units and nothing else: the
-// group norms of a tile (8 rows x 8 groups of a segment, 128 bytes) come with one 4-byte
-// load per lane, issued a tile ahead, and reach the lanes that need them by warp
-// shuffles.  Tiles are summed across warps by the deterministic slot reduction of
-// gemv_pipe.cuh.
+// activations take twice the registers), persistent over groups of 8 rows.  Warp w owns
+// the K-segment (w mod nsl) of 1024 positions - lane l the positions [32 l, 32 l + 32) -
+// and belongs to warp set w / nsl; the nsl warps of a set share each of its row groups.
+// Row group j goes to CTA j mod G and, in turn, to the CTA's warp sets, so every CTA
+// holds the same number of groups (+-1) and a set that finishes early leaves the SM's
+// issue slots to the others.  Packed rows arrive through a per-warp ring of kFxRing slots
+// of 2 rows x one segment (1 KB), each filled by one tensor copy issued by one lane; a
+// warp starts its first copies as soon as its own ring barriers exist, before the table
+// is built and the activations are rotated.  The tensor-copy unit starts at most ~47
+// copies per microsecond per SM (measured), so the copies are whole units and nothing
+// else: the group norms of a row group (8 rows x 8 groups of a segment, 128 bytes) come
+// with one 4-byte load per lane, issued a group ahead, and reach the lanes that need them
+// by warp shuffles.  The partial sums of a row group are added across its set's warps in
+// warp order (deterministic).  When several warp sets share a segment (K <= 8192), each
+// 128-group of activations is rotated once, by one warp, and shared in shared memory.
 
 #include <mutex>
 
@@ -81,8 +86,8 @@ struct Cq4FxParams {
     int ntok;                // tokens in this pass (<= TB)
     uint32_t smem_bytes;     // dynamic shared memory of the launch
     int share;               // 1: each 128-group rotated once per CTA, shared in shared memory
-    int64_t tiles_base;      // a CTA takes tiles_base tiles, one more if blockIdx.x < tiles_extra
-    int tiles_extra;
+    int64_t groups_base;     // a CTA takes groups_base row groups (8 rows), one more if
+    int groups_extra;        //   blockIdx.x < groups_extra
     float out_scale;         // 1 / (128 S)
     int cw[16];              // the 16-bit codewords C_t
 };
@@ -133,6 +138,43 @@ __device__ __forceinline__ void rotate32_int(int (&v)[32], int lane) {
     }
 }
 
+// Stores this warp's row partials of its k-th row group; the last of the nsl warps of its
+// warp set (the warps sharing the group, one per K-segment) to arrive adds them in warp
+// order (deterministic) and hands fin(t, r, sum) the sums.  Each warp set has its own
+// kSlots counters and barriers; a warp waits only when it runs kSlots groups ahead.
+template <int TB, int NW, typename Fin>
+__device__ __forceinline__ void group_reduce(const Reduce& rd, const float (&acc)[TB][kRows], int k, int w,
+                                             int lane, int nsl, int rgi, int ntok, unsigned int* err, Fin fin) {
+    const int ks = k % kSlots;
+    const int sl = rgi * kSlots + ks;
+    const uint32_t ph = (uint32_t)((k / kSlots) & 1);
+    float v[TB];
+#pragma unroll
+    for (int t = 0; t < TB; ++t) v[t] = reduce_rows8(acc[t], lane);
+    mbar_wait(&rd.empty[sl], ph ^ 1u, err);
+    if ((lane & 3) == 0) {
+#pragma unroll
+        for (int t = 0; t < TB; ++t) rd.at(((ks * NW + w) * TB + t) * kRows + ((lane >> 2) & 7)) = v[t];
+    }
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0) old = atomic_add_acq_rel_shared(&rd.count[sl], 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old % (uint32_t)nsl == (uint32_t)nsl - 1u) {
+        __syncwarp();
+        if (lane < TB * kRows) {
+            const int t = lane / kRows, r = lane % kRows;
+            if (t < ntok) {
+                float sum = 0.0f;
+                for (int ss = 0; ss < nsl; ++ss) sum += rd.at(((ks * NW + rgi * nsl + ss) * TB + t) * kRows + r);
+                fin(t, r, sum);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rd.empty[sl]);
+    }
+}
+
 // xr = Hu q of one 128-group held by a warp, lane l with positions 4l..4l+3: spans 1 and 2
 // inside the lane, 4..64 across lanes (exact integers)
 __device__ __forceinline__ void rotate128_int(int (&v)[4], int lane) {
@@ -162,7 +204,7 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
     cv.ok = tbase + kFxTable <= send;
     cv.a = sbase; cv.a_end = tbase; cv.b = tbase + kFxTable; cv.b_end = send;
     static_assert(holes_fit<NW, TB>(), "the partials must fit the table's holes");
-    const uint32_t red_at = cv.take(kSlots * (8 + 4), 8);        // slot barriers and counters
+    const uint32_t red_at = cv.take((uint32_t)p.rg * kSlots * (8 + 4), 8);   // slot barriers, counters
     const uint32_t bar_at = cv.take(NW * kFxRing * 8, 8);
     // the NW rings (equal sizes: first-fit fills the space below the table, then above)
     uint32_t ring_at;
@@ -188,31 +230,35 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
     rd.part = reinterpret_cast<float*>(gen(tbase + hole(kFxPartHole)));
     rd.pstride = 64;   // 256 bytes from one hole to the next
     rd.empty = reinterpret_cast<uint64_t*>(gen(red_at));
-    rd.count = reinterpret_cast<uint32_t*>(rd.empty + kSlots);
+    rd.count = reinterpret_cast<uint32_t*>(rd.empty + p.rg * kSlots);
     uint64_t* rfull = reinterpret_cast<uint64_t*>(gen(bar_at)) + w * kFxRing;
     uint8_t* ring = gen(ring_at);
     if (tid == 0) prefetch_tensormap(&p.pmap);
     // a warp's ring barriers are its own: it initialises them and starts its first copies
     // at once; the table, the activations and the rotation overlap those copies
     if (lane < kFxRing) mbar_init(&rfull[lane], 1);
-    if (tid < kSlots) {
-        rd.count[tid] = 0u;
-        mbar_init(&rd.empty[tid], 1);
+    for (int i = tid; i < p.rg * kSlots; i += NW * 32) {
+        rd.count[i] = 0u;
+        mbar_init(&rd.empty[i], 1);
     }
     if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncwarp();
 
     const int nsl = p.nseg < NW ? p.nseg : NW;
     const int slot = w % nsl, rgi = w / nsl;
-    const uint32_t nbusy = (uint32_t)(nsl * p.rg);
     const bool busy = rgi < p.rg;
-    const int tile_rows = kRows * p.rg;
-    const int64_t ntk = p.tiles_base + ((int)blockIdx.x < p.tiles_extra ? 1 : 0);
-    constexpr int upt = kRows / kFxUnitRows;                    // units per tile
-    const int64_t U = busy ? ntk * upt : 0;
+    // row group j (rows 8 j .. 8 j + 7) belongs to CTA j mod G; the CTA's m-th group goes
+    // to warp set m mod rg as that set's (m / rg)-th: every CTA holds the same number of
+    // groups (+-1), and sets that finish early leave the SM's issue slots to the others
+    const int64_t ncta = p.groups_base + ((int)blockIdx.x < p.groups_extra ? 1 : 0);
+    const int64_t ngr = busy && ncta > rgi ? (ncta - rgi + p.rg - 1) / p.rg : 0;   // this set's groups
+    const int64_t gstep = (int64_t)kRows * p.rg * gridDim.x;                        // rows between them
+    const int64_t row0 = (int64_t)kRows * (blockIdx.x + (int64_t)rgi * gridDim.x);  // first row
+    constexpr int upt = kRows / kFxUnitRows;                    // units per row group
+    const int64_t U = ngr * upt;
 
     // cursor of the next unit to issue (units go out strictly in order)
-    int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;
+    int64_t nx_base = row0;
     int nx_rem = 0;
     auto issue = [&](int d) {
         if (lane == 0) {
@@ -222,7 +268,7 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
         }
         if (++nx_rem == upt) {
             nx_rem = 0;
-            nx_base += (int64_t)gridDim.x * tile_rows;
+            nx_base += gstep;
         }
     };
     pdl_wait();   // the weights and activations may come from the previous kernels
@@ -302,16 +348,16 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
     // the segment)
     const int G = p.K / kGroup;
     auto load_norms = [&](int64_t k) -> uint32_t {
-        const int64_t row = (blockIdx.x + k * gridDim.x) * (int64_t)tile_rows + (int64_t)rgi * kRows + (lane >> 2);
-        if (k >= ntk || row >= p.N) return 0u;
+        const int64_t row = row0 + k * gstep + (lane >> 2);
+        if (k >= ngr || row >= p.N) return 0u;
         return __ldg(reinterpret_cast<const uint32_t*>(p.norms + row * G + slot * 8 + 2 * (lane & 3)));
     };
     uint32_t nrm_next = load_norms(0);
     int64_t u = 0;
-    for (int64_t k = 0; k < ntk; ++k) {
-        const int64_t tile = blockIdx.x + k * gridDim.x;
+    for (int64_t k = 0; k < ngr; ++k) {
+        const int64_t rbase = row0 + k * gstep;   // the group's first row
         const uint32_t nrm_tile = nrm_next;
-        nrm_next = load_norms(k + 1);   // a tile ahead
+        nrm_next = load_norms(k + 1);   // a group ahead
         float acc[TB][kRows];
 #pragma unroll
         for (int t = 0; t < TB; ++t)
@@ -363,14 +409,14 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
                 }
             }
         }
-        tile_reduce<TB, NW>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
-                            [&](int t, int rr, float sum) {
-                                const int64_t row = tile * tile_rows + rr;
-                                if (row < p.N) {
-                                    const int tok = p.t0 + t;
-                                    p.Y[(int64_t)tok * p.N + row] = sum * (p.scale[tok] * p.out_scale);
-                                }
-                            });
+        group_reduce<TB, NW>(rd, acc, (int)k, w, lane, nsl, rgi, p.ntok, p.err,
+                             [&](int t, int r, float sum) {
+                                 const int64_t row = rbase + r;
+                                 if (row < p.N) {
+                                     const int tok = p.t0 + t;
+                                     p.Y[(int64_t)tok * p.N + row] = sum * (p.scale[tok] * p.out_scale);
+                                 }
+                             });
     }
 }
 
@@ -392,11 +438,11 @@ cq_status run_cq4_fx(Cq4FxParams p, cudaStream_t st) {
         }
     }
     p.smem_bytes = (uint32_t)kFxSmem;
-    const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
+    const int64_t ngroups = (p.N + kRows - 1) / kRows;
     int64_t grid = sm_count();
-    if (ntiles < grid) grid = ntiles;
-    p.tiles_base = ntiles / grid;
-    p.tiles_extra = (int)(ntiles % grid);
+    if (ngroups < grid) grid = ngroups;
+    p.groups_base = ngroups / grid;
+    p.groups_extra = (int)(ngroups % grid);
     // several warps per segment: rotate each group once and share it (TB * K * 2 bytes of
     // shared memory beside the rings and the table)
     p.share = (p.rg >= 2 && p.K <= 8192) ? 1 : 0;
