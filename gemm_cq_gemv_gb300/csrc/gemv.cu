@@ -456,6 +456,8 @@ struct Q40GemvParams {
     int rg;
     int64_t total_bytes;  // N * nblk * 18
     int t0, ntok;
+    int64_t groups_base;  // ring kernel: a CTA takes groups_base row groups (8 rows), one
+    int groups_extra;     //   more if blockIdx.x < groups_extra
 };
 
 constexpr int kStage = 608;     // >= 37 chunks of 16 B, per row (unaligned staging)
@@ -610,32 +612,36 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
     constexpr int kSlotB = kUnitRows * kQSeg;
     uint8_t* rings = smem_q;                                                   // [16][kRing][4][576]
     uint64_t* rbar = reinterpret_cast<uint64_t*>(smem_q + kWarps2 * kRing * kSlotB);  // [16][kRing]
-    const Reduce rd = carve_reduce<kWarps2>(rbar + kWarps2 * kRing, TB);
+    const Reduce rd = carve_reduce_sets<kWarps2>(rbar + kWarps2 * kRing, TB, kWarps2);
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     pdl_trigger();
-    if (tid == 0) prefetch_tensormap(&p.bmap);
-    if (lane < kRing) mbar_init(&rbar[w * kRing + lane], 1);   // each warp its own ring barriers
-    if (tid < kSlots) {
-        rd.count[tid] = 0u;
-        mbar_init(&rd.empty[tid], 1);
-    }
-    if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncthreads();
     const int nsl = p.nseg < kWarps2 ? p.nseg : kWarps2;
     const int slot = w % nsl, rgi = w / nsl;
-    if (rgi >= p.rg) return;   // warps left over when the segments do not divide 16
-    const uint32_t nbusy = (uint32_t)(nsl * p.rg);
-
+    const bool busy = rgi < p.rg;
     uint8_t* ring = rings + w * (kRing * kSlotB);
     uint64_t* rfull = rbar + w * kRing;
-    const int tile_rows = kRows * p.rg;
-    const int64_t ntiles = (p.N + tile_rows - 1) / tile_rows;
-    const int64_t ntk = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // a warp's ring barriers are its own: it initialises them and starts its first copies
+    // at once; the activations are converted while those copies are in flight
+    if (tid == 0) prefetch_tensormap(&p.bmap);
+    if (lane < kRing) mbar_init(&rfull[lane], 1);
+    for (int i = tid; i < p.rg * kSlots; i += kWarps2 * 32) {
+        rd.count[i] = 0u;
+        mbar_init(&rd.empty[i], 1);
+    }
+    if (lane == 0) asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    // row group j (8 rows) belongs to CTA j mod G; the CTA's m-th group goes to warp set
+    // m mod rg (the nsl warps sharing a row group, one per segment)
+    const int64_t ncta = p.groups_base + ((int)blockIdx.x < p.groups_extra ? 1 : 0);
+    const int64_t ngr = busy && ncta > rgi ? (ncta - rgi + p.rg - 1) / p.rg : 0;
+    const int64_t gstep = (int64_t)kRows * p.rg * gridDim.x;
+    const int64_t row0 = (int64_t)kRows * (blockIdx.x + (int64_t)rgi * gridDim.x);
     const int nown = (SPW == 2 && slot + kWarps2 < p.nseg) ? 2 : 1;
     const int upt = 2 * nown;
-    const int64_t U = ntk * upt;
+    const int64_t U = ngr * upt;
 
-    int64_t nx_base = (int64_t)blockIdx.x * tile_rows + (int64_t)rgi * kRows;
+    int64_t nx_base = row0;
     int nx_rem = 0;
     auto issue = [&](int d) {
         if (lane == 0) {
@@ -646,21 +652,22 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
         }
         if (++nx_rem == upt) {
             nx_rem = 0;
-            nx_base += (int64_t)gridDim.x * tile_rows;
+            nx_base += gstep;
         }
     };
-    // the first units are in flight while the activations are loaded
     pdl_wait();
     for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
     Q4X xq[SPW][TB];
-    q4_load_x<TB, SPW>(p, slot, true, lane, xq);
+    q4_load_x<TB, SPW>(p, slot, busy, lane, xq);
+    __syncthreads();   // every warp set's reduction barriers initialised
+    if (!busy) return;   // warps left over when the segments do not divide 16
 
     // every staged row starts at byte 0: per-lane word offset and shifts
     const int o = lane * 18;
     const uint32_t dsh = (uint32_t)(o & 3) * 8u;
     int64_t u = 0;
-    for (int64_t k = 0; k < ntk; ++k) {
-        const int64_t tile = blockIdx.x + k * gridDim.x;
+    for (int64_t k = 0; k < ngr; ++k) {
+        const int64_t rbase = row0 + k * gstep;   // the group's first row
         float acc[TB][kRows];
 #pragma unroll
         for (int t = 0; t < TB; ++t)
@@ -678,7 +685,7 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
                     __syncwarp();
                     issue((int)((u + kRing - 1) & (kRing - 1)));
                 }
-                const int64_t left = p.N - (tile * tile_rows + (int64_t)rgi * kRows + h * kUnitRows);
+                const int64_t left = p.N - (rbase + h * kUnitRows);
                 const int nv = lane >= nb ? 0 : (left >= kUnitRows ? kUnitRows : (int)left);   // rows to add
                 const int d = (int)(u & (kRing - 1));
                 mbar_wait(&rfull[d], (uint32_t)(u >> 2) & 1u, p.err);
@@ -689,11 +696,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
                         q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xq[i], acc, h * kUnitRows + r);
             }
         }
-        tile_reduce<TB, kWarps2>(rd, acc, (int)k, w, lane, nsl, nbusy, tile_rows, p.ntok, p.err,
-                        [&](int t, int rr, float sum) {
-                            const int64_t row = tile * tile_rows + rr;
-                            if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
-                        });
+        group_reduce<TB, kWarps2>(rd, acc, (int)k, w, lane, nsl, rgi, p.ntok, p.err,
+                                  [&](int t, int r, float sum) {
+                                      const int64_t row = rbase + r;
+                                      if (row < p.N) p.Y[(int64_t)(p.t0 + t) * p.N + row] = sum;
+                                  });
     }
 }
 
@@ -906,12 +913,17 @@ template <int TB, int SPW, bool RING>
 cq_status run_q4_0_gemv(Q40GemvParams p, cudaStream_t st) {
     static bool attr[64] = {};
     auto kern = RING ? q4_0_gemv_ring_kernel<TB, SPW> : q4_0_gemv_rows_kernel<TB, SPW>;
-    const size_t smem = RING ? (size_t)kWarps2 * kRing * kUnitRows * kQSeg + kWarps2 * kRing * 8 + reduce_bytes<kWarps2>(TB)
+    const size_t smem = RING ? (size_t)kWarps2 * kRing * kUnitRows * kQSeg + kWarps2 * kRing * 8 +
+                                   reduce_bytes_sets<kWarps2>(TB, kWarps2)
                              : (size_t)kWarps2 * kRows * kStage + reduce_bytes<kWarps2>(TB);
-    const int64_t ntiles = (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
+    // the ring kernel schedules row groups of 8 rows, the row-staged kernel tiles
+    const int64_t nwork = RING ? (p.N + kRows - 1) / kRows
+                               : (p.N + (int64_t)kRows * p.rg - 1) / ((int64_t)kRows * p.rg);
     int grid = 0;
-    const cq_status s = launch_once(kern, smem, ntiles, st, attr, &grid);
+    const cq_status s = launch_once(kern, smem, nwork, st, attr, &grid);
     if (s != CQ_OK) return s;
+    p.groups_base = nwork / grid;
+    p.groups_extra = (int)(nwork % grid);
     return launch_pdl(kern, dim3(grid), dim3(kWarps2 * 32), smem, st, p);
 }
 

@@ -138,43 +138,6 @@ __device__ __forceinline__ void rotate32_int(int (&v)[32], int lane) {
     }
 }
 
-// Stores this warp's row partials of its k-th row group; the last of the nsl warps of its
-// warp set (the warps sharing the group, one per K-segment) to arrive adds them in warp
-// order (deterministic) and hands fin(t, r, sum) the sums.  Each warp set has its own
-// kSlots counters and barriers; a warp waits only when it runs kSlots groups ahead.
-template <int TB, int NW, typename Fin>
-__device__ __forceinline__ void group_reduce(const Reduce& rd, const float (&acc)[TB][kRows], int k, int w,
-                                             int lane, int nsl, int rgi, int ntok, unsigned int* err, Fin fin) {
-    const int ks = k % kSlots;
-    const int sl = rgi * kSlots + ks;
-    const uint32_t ph = (uint32_t)((k / kSlots) & 1);
-    float v[TB];
-#pragma unroll
-    for (int t = 0; t < TB; ++t) v[t] = reduce_rows8(acc[t], lane);
-    mbar_wait(&rd.empty[sl], ph ^ 1u, err);
-    if ((lane & 3) == 0) {
-#pragma unroll
-        for (int t = 0; t < TB; ++t) rd.at(((ks * NW + w) * TB + t) * kRows + ((lane >> 2) & 7)) = v[t];
-    }
-    __syncwarp();
-    uint32_t old = 0;
-    if (lane == 0) old = atomic_add_acq_rel_shared(&rd.count[sl], 1u);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old % (uint32_t)nsl == (uint32_t)nsl - 1u) {
-        __syncwarp();
-        if (lane < TB * kRows) {
-            const int t = lane / kRows, r = lane % kRows;
-            if (t < ntok) {
-                float sum = 0.0f;
-                for (int ss = 0; ss < nsl; ++ss) sum += rd.at(((ks * NW + rgi * nsl + ss) * TB + t) * kRows + r);
-                fin(t, r, sum);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rd.empty[sl]);
-    }
-}
-
 // xr = Hu q of one 128-group held by a warp, lane l with positions 4l..4l+3: spans 1 and 2
 // inside the lane, 4..64 across lanes (exact integers)
 __device__ __forceinline__ void rotate128_int(int (&v)[4], int lane) {
