@@ -73,10 +73,11 @@ def load_codebook():
 
 
 def kernel_source_hash():
-    """Hash of the sources of the decode GEMV kernels (the recorded DRAM traffic is valid
-    only for the sources it was captured on)."""
+    """Hash of the sources the batch-1 decode kernels of the timed step are built from (the
+    4-bit integer-codeword GEMV and the Q4_0 GEMV, with their shared header and dispatch);
+    the recorded DRAM traffic is valid only for the sources it was captured on."""
     h = hashlib.sha256()
-    for name in ("gemv.cu", "gemv_fx.cu", "gemv_pipe.cuh", "lut.cu", "common.cuh"):
+    for name in ("gemv.cu", "gemv_fx.cu", "gemv_pipe.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "gemm_cq_gemv_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
