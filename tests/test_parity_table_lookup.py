@@ -79,17 +79,21 @@ def test_lut_gemv_large_sampled(b):
 
 @pytest.mark.parametrize("b", [1, cq.CQ_TERNARY])
 def test_lut_gemv_row_blocks(b):
-    """Enough rows that every CTA holds more than 2048 (its partial sums are kept for 2048
-    rows at a time): the rows on both sides of every block and CTA boundary are checked."""
+    """Enough rows that every CTA holds more than one block of 256 row groups (one range):
+    the rows around the blocks of several CTAs and a random sample are checked (row group
+    j of 8 rows belongs to CTA j mod G)."""
     N, K = 320_000, 256
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    rpc = max(16, -(-N // sms))
-    assert rpc > 2048
-    edges = []
-    for c0 in range(0, N, rpc):
-        for e in (c0, c0 + 2048):
-            edges += [e - 1, e, e + 1]
-    rows = np.unique(np.clip(np.array(edges + [N - 1]), 0, N - 1))
+    ngroups = -(-N // 8)
+    grid = min(sms, ngroups)
+    assert -(-ngroups // grid) > 256
+    rows = [0, N - 1]
+    for c in (0, 1, grid // 2, grid - 1):
+        for m in (0, 255, 256, 257):
+            j = c + m * grid
+            rows += [8 * j - 1, 8 * j, 8 * j + 7, 8 * j + 8]
+    extra = np.random.default_rng(40 + b).choice(N, 100, replace=False)
+    rows = np.unique(np.clip(np.array(rows + list(extra)), 0, N - 1))
     Y, ref = _case(N, K, b, 1, 31 + b, 37, rows=rows)
     assert max_rel_err(Y, ref) < TOL
 
@@ -108,3 +112,32 @@ def test_lut_gemv_matches_cq_gemv_and_is_deterministic(b):
     yg = to_host(cq.cq_gemv(packed, norms, 1000, 2048, b, cb, q, s))
     assert np.array_equal(y0, y1)
     assert max_rel_err(y0, yg) < TOL
+
+
+@pytest.mark.parametrize("b", [1, 2])
+def test_lut_gemv_several_ranges_and_row_blocks(b):
+    """Rows of several 512-byte ranges (K = 4224: two ranges at 1 bit, the second of four
+    words; three at 2 bits) with more rows per CTA than one block of partial sums holds
+    (2048): random packed indices and norms, checked against the oracle on rows at the
+    block boundaries, the first and last rows and a random sample."""
+    N, K = 312_000, 4224
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(90 + b)
+    packed = rng.integers(0, 256, size=(N, K * b // 8), dtype=np.uint8)
+    norms = rng.uniform(0.25, 2.0, size=(N, K // 128)).astype(np.float16).view(np.uint16)
+    X = synth.activations(1, K, seed=91)
+    cb = fitted_cb28()
+    q, s = cq.a8_quantize(to_dev(X))
+    Y = to_host(cq.cq_gemv_lut(to_dev(packed), to_dev(norms.view(np.int16)), N, K, b, cb, q, s))
+    ngroups = -(-N // 8)
+    grid = min(sms, ngroups)
+    assert -(-ngroups // grid) > 256   # more than one block of 256 row groups per CTA
+    rows = [0, N - 1]
+    for c in (0, 1, grid // 2, grid - 1):
+        for m in (255, 256, 257):
+            j = c + m * grid
+            rows += [8 * j, 8 * j + 7]
+    rows = np.unique(np.clip(np.array(rows + list(rng.choice(N, 200, replace=False))), 0, N - 1))
+    q_ref, s_ref = oracle.a8_quantize(X)
+    ref = oracle.cq_gemv_ref(packed.reshape(N, K // 128, 16 * b), norms, b, cb, q_ref, s_ref, rows=rows)
+    assert max_rel_err(Y[:, rows], ref) < TOL
