@@ -676,8 +676,6 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
 #pragma unroll
         for (int i = 0; i < SPW; ++i) {
             if (i >= nown) break;
-            const int seg = slot + i * kWarps2;
-            const int nb = min(32, p.nblk - seg * 32);
 #pragma unroll
             for (int h = 0; h < 2; ++h, ++u) {
                 if (u + kRing - 1 < U) {
@@ -685,15 +683,15 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
                     __syncwarp();
                     issue((int)((u + kRing - 1) & (kRing - 1)));
                 }
-                const int64_t left = p.N - (rbase + h * kUnitRows);
-                const int nv = lane >= nb ? 0 : (left >= kUnitRows ? kUnitRows : (int)left);   // rows to add
                 const int d = (int)(u & (kRing - 1));
                 mbar_wait(&rfull[d], (uint32_t)(u >> 2) & 1u, p.err);
                 const uint32_t* wl = reinterpret_cast<const uint32_t*>(ring + d * kSlotB) + (o >> 2);
+                // all four rows unconditionally, so their chains interleave: rows past N and
+                // blocks past the row's end arrive as zeros (scale 0, nothing added), and the
+                // activations of blocks past K are zero
 #pragma unroll
                 for (int r = 0; r < kUnitRows; ++r)
-                    if (r < nv)
-                        q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xq[i], acc, h * kUnitRows + r);
+                    q4_block<TB>(wl + r * (kQSeg / 4), dsh, dsh + 16u, xq[i], acc, h * kUnitRows + r);
             }
         }
         group_reduce<TB, kWarps2>(rd, acc, (int)k, w, lane, nsl, rgi, p.ntok, p.err,
