@@ -181,6 +181,22 @@ __global__ void __launch_bounds__(kLutThreads, 1) cq_gemv_lut_kernel(const __gri
     const int64_t gstride = (int64_t)kLutWarps * gridDim.x;   // this warp's next group, in groups
     int64_t u_glob = 0;   // units this warp has consumed (its ring's slot and phase)
     bool built = false;
+    // this warp's int8 activations of a range (its groups w and w + 16), loaded one range
+    // ahead so a table rebuild does not wait for them
+    constexpr int kGpw = LutPlan<F>::range_pos / kGroup / kLutWarps;   // groups per warp (2 or 1)
+    char4 xpre[kGpw];
+    auto load_acts = [&](int r) {
+        const int rw = r * kRangeWords;
+        const int n = p.words - rw < kRangeWords ? p.words - rw : kRangeWords;
+        const int ngr = n * 32 / F / kGroup;
+#pragma unroll
+        for (int j = 0; j < kGpw; ++j) {
+            const int gi = w + j * kLutWarps;
+            xpre[j] = gi < ngr ? *reinterpret_cast<const char4*>(xq + rw * 32 / F + gi * kGroup + 4 * lane)
+                               : make_char4(0, 0, 0, 0);
+        }
+    };
+    load_acts(0);
     for (int64_t mb = 0; mb < ncta; mb += kBlockGroups) {
         const int nbg = (int)(ncta - mb < kBlockGroups ? ncta - mb : kBlockGroups);
         const int ngw = nbg > w ? (nbg - w + kLutWarps - 1) / kLutWarps : 0;   // this warp's groups
@@ -208,10 +224,12 @@ __global__ void __launch_bounds__(kLutThreads, 1) cq_gemv_lut_kernel(const __gri
                 // (1) xr = Hu @ q for the range's groups, one warp per group: lane l holds
                 // positions 4l..4l+3; spans 1 and 2 inside the lane, 4..64 across lanes.
                 // The values are integers below 2^24, exact in fp32.
-                const int rp0 = rw0 * 32 / F;
                 const int ngr = nw * 32 / F / kGroup;
-                for (int gi = w; gi < ngr; gi += kLutWarps) {
-                    const char4 c = *reinterpret_cast<const char4*>(xq + rp0 + gi * kGroup + 4 * lane);
+#pragma unroll
+                for (int j = 0; j < kGpw; ++j) {
+                    const int gi = w + j * kLutWarps;
+                    if (gi >= ngr) continue;
+                    const char4 c = xpre[j];
                     float v0 = c.x, v1 = c.y, v2 = c.z, v3 = c.w;
                     const float a0 = v0 + v1, a1 = v0 - v1, a2 = v2 + v3, a3 = v2 - v3;
                     v0 = a0 + a2; v2 = a0 - a2; v1 = a1 + a3; v3 = a1 - a3;
@@ -264,6 +282,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) cq_gemv_lut_kernel(const __gri
                 }
                 __syncthreads();
                 built = true;
+                if (p.nranges > 1) load_acts(r + 1 < p.nranges ? r + 1 : 0);   // the next rebuild's
             }
             // (3) the rows: units of two rows, the next three in flight; the norms of the
             // next row group loaded while the current one is looked up
