@@ -156,11 +156,15 @@ class ClockSampler:
 # The GPU arm
 # ------------------------------------------------------------------------------------
 def build_workload(dev, cb, torch, cq, synth, only=None):
-    """Encode the large-shape weights once (device) and allocate every step buffer."""
+    """Encode the large-shape weights once (device) and allocate every step buffer.  The
+    step's activations are views into one device buffer and its outputs into another
+    (``xbuf``, ``ybuf`` of every entry), so the end-to-end leg moves each with one copy."""
+    sel = [(i, m) for i, m in enumerate(synth.LARGE) if not only or m.name in only]
+    xbuf = torch.empty((sum(m.K for _, m in sel),), dtype=torch.float32, device=dev)
+    ybuf = torch.empty((sum(2 * m.N for _, m in sel),), dtype=torch.float32, device=dev)
+    xo = yo = 0
     mats = []
-    for i, m in enumerate(synth.LARGE):
-        if only and m.name not in only:
-            continue
+    for i, m in sel:
         g = torch.Generator(device=dev)
         g.manual_seed(synth.weight_seed(4, i))
         W = torch.randn((m.N, m.K), device=dev, generator=g) * 0.02
@@ -169,14 +173,18 @@ def build_workload(dev, cb, torch, cq, synth, only=None):
         del W
         gx = torch.Generator(device=dev)
         gx.manual_seed(synth.activation_seed(4, 1) + i)
-        X = torch.randn((1, m.K), device=dev, generator=gx)
+        X = xbuf[xo:xo + m.K].view(1, m.K)   # K, N are multiples of 4: 16-byte aligned views
+        X.copy_(torch.randn((1, m.K), device=dev, generator=gx))
+        xo += m.K
         mats.append(dict(
             m=m, packed=packed, norms=norms, blocks=blocks, X=X,
             Xq=torch.empty((1, m.K), dtype=torch.int8, device=dev),
             s=torch.empty((1,), dtype=torch.float32, device=dev),
             ws=torch.empty((cq.cq_gemv_workspace_bytes(1, m.K),), dtype=torch.uint8, device=dev),
-            Ycq=torch.empty((1, m.N), dtype=torch.float32, device=dev),
-            Yq4=torch.empty((1, m.N), dtype=torch.float32, device=dev)))
+            Ycq=ybuf[yo:yo + m.N].view(1, m.N),
+            Yq4=ybuf[yo + m.N:yo + 2 * m.N].view(1, m.N),
+            xbuf=xbuf, ybuf=ybuf))
+        yo += 2 * m.N
     torch.cuda.synchronize()
     torch.cuda.empty_cache()   # release the float32 weights before anything is timed
     return mats
@@ -715,19 +723,17 @@ def gpu_arm(args, rank, world, local_rank):
 
     # end to end through the public API with host buffers: pinned H2D of the step's
     # activations, the decode pass, D2H of the step's outputs
-    host_x = [torch.empty(d["X"].shape, dtype=torch.float32, pin_memory=True).copy_(d["X"])
-              for d in mats]
-    host_y = [torch.empty((2, d["m"].N), dtype=torch.float32, pin_memory=True) for d in mats]
-    h2d = sum(x.numel() * 4 for x in host_x)
-    d2h = sum(y.numel() * 4 for y in host_y)
+    # (every matrix's activations in one buffer and its outputs in another: one copy each way)
+    xbuf, ybuf = mats[0]["xbuf"], mats[0]["ybuf"]
+    host_x = torch.empty(xbuf.shape, dtype=torch.float32, pin_memory=True).copy_(xbuf)
+    host_y = torch.empty(ybuf.shape, dtype=torch.float32, pin_memory=True)
+    h2d = host_x.numel() * 4
+    d2h = host_y.numel() * 4
 
     def e2e_step():
-        for d, hx in zip(mats, host_x):
-            d["X"].copy_(hx, non_blocking=True)
+        xbuf.copy_(host_x, non_blocking=True)
         run_step(mats, cb, cq, kinds=kinds)
-        for d, hy in zip(mats, host_y):
-            hy[0].copy_(d["Ycq"][0], non_blocking=True)
-            hy[1].copy_(d["Yq4"][0], non_blocking=True)
+        host_y.copy_(ybuf, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
