@@ -181,12 +181,15 @@ cq_status cq_gemv(const uint8_t* packed, const uint16_t* norms, int64_t N, int64
  * For each token, every CTA rotates the activations (xr = Hu @ Xq per group) into shared
  * memory and tabulates, for every 4-bit nibble of the packed stream (four 1-bit or two
  * 2-bit indices), the 16 possible partial sums cb * xr over the positions it covers; a row
- * then costs one lookup and one fp32 add per nibble.  Sums in fp32 in a fixed order
- * (deterministic); the result is within 1e-3 of the exact product like cq_gemv's.
+ * then costs one lookup and one fp32 add per nibble.  K is processed in ranges of 512
+ * packed bytes per row (one table per range); rows stream through tensor copies.  Sums in
+ * fp32 in a fixed order (deterministic); the result is within 1e-3 of the exact product
+ * like cq_gemv's.
  *   packed, norms  as written by cq_encode for b = 1, 2 or CQ_TERNARY
  *   Xq [B][K] int8, scale [B] float32, Y [B][N] float32; all 16-byte aligned
  * No workspace.  Each token is one launch that reads the weights once (meant for batches
- * of 1 or 2).  K is limited to 2^24, N to 2^40, B to 2^30.
+ * of 1 or 2).  K is limited to 2^24, N to 2^31 - 64 (the tensor copies address rows with
+ * 32-bit coordinates), B to 2^30.
  * Errors: INVALID_ARG (NULL, g != 128, K % 128, b not in 1..5), UNSUPPORTED (b = 3 or 4,
  * sizes above the limits), ALIGNMENT, CUDA. */
 cq_status cq_gemv_lut(const uint8_t* packed, const uint16_t* norms, int64_t N, int64_t K, int g,
@@ -321,7 +324,11 @@ cq_status q4_0_quantize(const float* W, int64_t N, int64_t K, uint8_t* blocks, v
 
 /* ---- A8: Q4_0 decode GEMV (KMCU page, §2, §3: fixed-length 32 inner loop over
  * row-aligned blocks).  Y[t][o] = sum_blocks fp32(d) * sum_k (nib - 8) * X[t][k],
- * float32 accumulation; padding columns are skipped.
+ * float32 accumulation; padding columns are skipped.  The activations of each 32-block
+ * are held as 24-bit fixed-point integers, rint(x * 2^e) with the block's largest |x| in
+ * [2^21, 2^22) (an error of at most 2^-23 of that value), so every block sum is exact in
+ * int32: a block whose weights are all 0 contributes exactly 0, and an all-zero row or
+ * token gives exactly 0.  A non-finite activation makes the outputs of its token NaN.
  *   blocks [N][ceil(K/32) * 18] uint8, X [B][K] float32, Y [B][N] float32 (all 16-byte
  *   aligned); K is limited to 32768, N to 2^31 - 1024 and B to 2^30 (CQ_ERR_UNSUPPORTED
  *   above).

@@ -118,6 +118,7 @@ def test_gemv_lut_validation(lib):
     assert f(A, None, 8, 128, 128, 1, _cb(), A, A, 1, A, None) == INV
     assert f(A, A, 8, 128, 128, 1, _cb(), A, A, 1, M, None) == ALN
     assert f(A, A, 8, 1 << 25, 128, 5, _cb(), A, A, 1, A, None) == UNS   # K above 2^24
+    assert f(A, A, 1 << 31, 128, 128, 1, _cb(), A, A, 1, A, None) == UNS  # N: 32-bit copy rows
 
 
 def test_codebook_fit_validation(lib):

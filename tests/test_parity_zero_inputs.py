@@ -95,3 +95,20 @@ def test_q4_0_gemm_zero_inputs():
     W, X = _inputs(N, K, M, 350)
     Y = to_host(cq.q4_0_gemm(cq.q4_0_quantize(to_dev(W)), N, K, to_dev(X)))
     _check(Y, oracle.q4_0_gemv_ref(oracle.q4_0_quantize(W), K, X), 1e-3)
+
+
+@pytest.mark.parametrize("N,K,B", [(37, 312, 2), (64, 1024, 2), (40, 4096, 1)])
+def test_q4_0_gemv_non_finite_activation(N, K, B):
+    """A token with an infinite or NaN activation gets NaN outputs (every output row sums a
+    block holding it; a float32 product would give inf or NaN there too); the other token
+    is unaffected and matches the oracle."""
+    W, X = _inputs(N, K, B, 360 + N + B)
+    X = X.copy()
+    X[0, K // 3] = np.inf if K % 2 else np.nan
+    X[0, 5] = -np.inf
+    blocks = cq.q4_0_quantize(to_dev(W))
+    Y = to_host(cq.q4_0_gemv(blocks, N, K, to_dev(X)))
+    assert np.isnan(Y[0]).all()
+    if B > 1:
+        ref = oracle.q4_0_gemv_ref(oracle.q4_0_quantize(W), K, X[1:])
+        assert max_rel_err(Y[1:], ref) < 1e-3
