@@ -556,10 +556,11 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
     return out
 
 
-def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
+def narrow_report(dev, cb, torch, cq, synth, steps, warmup, case=None, codes=None):
     """Batch-1 decode of 1-bit, 2-bit and ternary rows on the large shapes: ``cq_gemv``
     against the table-lookup ``cq_gemv_lut``, each call timed alone after an L2 flush, plus
-    the largest relative difference between the two outputs (both compute the same product)."""
+    the largest relative difference between the two outputs (both compute the same product).
+    ``case`` and ``codes`` restrict the matrices and the codes (profiling runs)."""
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
 
     def one(fn):
@@ -572,10 +573,14 @@ def narrow_report(dev, cb, torch, cq, synth, steps, warmup):
            "timing": "per call, CUDA events, L2 flushed before each call",
            "unit": "us per call; GB/s of algorithmic bytes over the four matrices"}
     for b, name in ((1, "b1"), (2, "b2"), (cq.CQ_TERNARY, "ternary")):
+        if codes and name not in codes:
+            continue
         res = {"cq_gemv": {"us": {}, "ms": 0.0}, "cq_gemv_lut": {"us": {}, "ms": 0.0}}
         nbytes = 0
         diff = 0.0
         for i, m in enumerate(synth.LARGE):
+            if case and m.name not in case:
+                continue
             g = torch.Generator(device=dev)
             g.manual_seed(synth.weight_seed(4, i))
             W = torch.randn((m.N, m.K), device=dev, generator=g) * 0.02
@@ -642,7 +647,9 @@ def gpu_arm(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     cb = cq.make_codebook(load_codebook())
     if args.narrow_only:
-        print(json.dumps(narrow_report(dev, cb, torch, cq, synth, 10, args.warmup)), flush=True)
+        steps = args.steps if args.narrow_codes or args.case else 10
+        print(json.dumps(narrow_report(dev, cb, torch, cq, synth, steps, args.warmup, case=args.case,
+                                       codes=args.narrow_codes)), flush=True)
         return
     if args.small_only:
         print(json.dumps(small_report(dev, cb, torch, cq, synth, 10, args.warmup)), flush=True)
@@ -1057,6 +1064,8 @@ def main(argv=None):
                     help="skip the 1-bit / 2-bit / ternary decode report (cq_gemv vs cq_gemv_lut)")
     ap.add_argument("--small-only", action="store_true",
                     help="print only the small-workload report (profiling runs)")
+    ap.add_argument("--narrow-codes", nargs="*", default=None, choices=["b1", "b2", "ternary"],
+                    help="restrict the narrow-code report to these codes (profiling runs)")
     ap.add_argument("--narrow-only", action="store_true",
                     help="print only that report (the child process the full run starts)")
     args = ap.parse_args(argv)
