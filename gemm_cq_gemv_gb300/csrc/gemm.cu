@@ -81,10 +81,14 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //   BITS    CQ index width: 4 or 2 (the packed tile rides in the stage, 32 or 16 bytes
 //           per row), 1 or 3 (slabs of two stages)
 template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false,
-          int BITS_ = 4>
+          int BITS_ = 4, bool PF16_ = false>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
+    // PF16: fp16 operands with the bf16 output of the prefill; the dequant looks up fp16
+    // codeword pairs and scales them by the fp16 norm with one multiply
+    static constexpr bool PF16 = PF16_;
+    static constexpr bool OPF16 = F16 || PF16;     // fp16 (not bf16) MMA operands
     static constexpr int STAGES = STAGES_;
     static constexpr int FMT = FMT_;
     static constexpr int SLABS = SLABS_;
@@ -105,8 +109,9 @@ struct GemmCfg {
     static_assert(BITS == 4 || (FMT == kFmtCQ && F16), "1- to 3-bit CQ rows: decode batches only");
     static_assert(!CQSLAB || SLABS >= 2, "1- and 3-bit CQ rows run on a slab ring");
     static_assert(FMT == kFmtQ40 || CQSLAB || SLABS == 0, "4- and 2-bit CQ tiles ride in the stages");
+    static_assert(!PF16 || (!F16 && FMT == kFmtCQ && BITS == 4), "fp16 pair tables: 4-bit prefill");
 };
-using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true>;   // 24 KB activation tile, 28 KB stages
+using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true>;   // 24 KB activation tile, 28 KB stages
 using DecodeCfg = GemmCfg<32, true, 8>;                  // 4 KB activation tile, 8 KB stages
 using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2>;   // 2-bit rows: 6 KB stages
 using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1>;   // 1-bit rows: 4 KB stages + 2 KB slabs
@@ -413,6 +418,11 @@ __device__ __forceinline__ uint32_t pair_addr(uint32_t wv, uint32_t lb) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(wv), "r"(lb), "n"(0x7604 | (J << 4)));
     return a;
 }
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ float2 lds_f2(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
@@ -495,7 +505,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         slv[tid] = v;
     }
     __syncthreads();
-    if constexpr (C::FMT == kFmtCQ) {
+    if constexpr (C::PF16) {
+        // fp16 pairs (cb[e & 15] low), entry e of lane l at e << 8 | l << 2
+        uint32_t* luth = reinterpret_cast<uint32_t*>(gen(tbase));
+        for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
+            const int e = i >> 5;
+            const __half2 v = __floats2half2_rn(slv[e & 15], slv[e >> 4]);
+            luth[(e << 6) | (i & 31)] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+    } else if constexpr (C::FMT == kFmtCQ) {
         constexpr int kHalf = C::BITS;                   // bits of one index of the pair
         constexpr int kEntries = 1 << (2 * C::BITS);
         for (int i = tid; i < kEntries * 32; i += kThreadsGemm) {
@@ -596,7 +614,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16kind(kBO, kBT, C::F16);
+            constexpr uint32_t idesc = idesc_f16kind(kBO, kBT, C::OPF16);
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -806,8 +824,30 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                     wv[0] = w.x & 0x0F0F0F0Fu; wv[1] = (w.x >> 4) & 0x0F0F0F0Fu;
                     wv[2] = w.y & 0x0F0F0F0Fu; wv[3] = (w.y >> 4) & 0x0F0F0F0Fu;
                 }
-                const float2 n2 = make_float2(nrm, nrm);
                 uint32_t pk[16];
+                if constexpr (C::PF16) {
+                    // fp16 pair lookups (4 bytes) times the fp16 norm (exact: the norm is
+                    // stored as fp16): one multiply per pair, no conversion
+                    const uint32_t lb4 = tbase | ((uint32_t)lane << 2);
+                    const __half2 nh = __float2half2_rn(nrm);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t c[4] = {lds_u32(pair_addr<0>(wv[k], lb4)), lds_u32(pair_addr<1>(wv[k], lb4)),
+                                               lds_u32(pair_addr<2>(wv[k], lb4)), lds_u32(pair_addr<3>(wv[k], lb4))};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&c[j]), nh);
+                            pk[4 * k + j] = *reinterpret_cast<const uint32_t*>(&v);
+                        }
+                    }
+                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    continue;
+                }
+                const float2 n2 = make_float2(nrm, nrm);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const float2 c[4] = {lds_f2(pair_addr<0>(wv[k], lb)), lds_f2(pair_addr<1>(wv[k], lb)),
@@ -1088,7 +1128,7 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
         int64_t grid = (rp.groups + 7) / 8;
         const int64_t cap = (int64_t)sm_count() * 16;
         if (grid > cap) grid = cap;
-        const cq_status r = launch_pdl(rotate_act_kernel16<C::F16>, dim3((unsigned)grid), dim3(256), 0, cs, rp);
+        const cq_status r = launch_pdl(rotate_act_kernel16<C::OPF16>, dim3((unsigned)grid), dim3(256), 0, cs, rp);
         rp.njobs = 0;
         rp.groups = 0;
         return r;
@@ -1145,7 +1185,7 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
             const int a = act_of[pi];
             if (map_of_act[a] < 0) {
                 if (nmaps == kMaxActs) break;
-                st = make_act_map(&prm.tmap[nmaps], act_dst[a], M, act_K[a], C::BT, C::F16);
+                st = make_act_map(&prm.tmap[nmaps], act_dst[a], M, act_K[a], C::BT, C::OPF16);
                 if (st != CQ_OK) return st;
                 map_of_act[a] = nmaps++;
             }

@@ -198,9 +198,11 @@ cq_status cq_gemv_lut(const uint8_t* packed, const uint16_t* norms, int64_t N, i
 
 /* ---- A4 + A6: prefill GEMM on the tensor cores (Needle .cact page, §三: prefill is a
  * GEMM over the same [out, in] rows; §一: reconstruction formula).  Computes
- *   Y[t][o] = bf16( s_t / 128 * sum_k bf16(xr[t][k]) * bf16(cb[idx[o][k]] * norm[o][k/128]) )
- * with xr = Hu @ Xq per group (rotated once per call into `workspace`, bf16), tcgen05
- * MMA with fp32 accumulation in tensor memory.  Only b = 4 is implemented
+ *   Y[t][o] = bf16( sum_k fp16(xr[t][k] * s_t / 128) * fp16(fp16(cb[idx[o][k]]) * norm[o][k/128]) )
+ * with xr = Hu @ Xq per group (rotated once per call into `workspace`, fp16), tcgen05
+ * MMA with fp32 accumulation in tensor memory.  The fp16 operands bound the range: a
+ * token whose largest |activation| exceeds 65504, or a group whose norm times its largest
+ * codeword does, overflows (the products become infinite).  Only b = 4 is implemented
  * (CQ_ERR_UNSUPPORTED for b = 1..3 and CQ_TERNARY).  N must be a multiple of 16 (INVALID_ARG); N and K
  * are limited to 2^24 (INVALID_ARG above), M to 2^30 (INVALID_ARG), and
  * ceil(M / 192) * ceil(N / 128) output tiles to 2^23 (UNSUPPORTED above).
