@@ -4,9 +4,9 @@
 // rows the decode GEMV streams; §一: w_group = (cb[idx] * norm / sqrt(128)) @ H.  With
 // xr = Hu @ q (the rotated int8 activations, exact integers) the product is
 //   Y[t][o] = s_t / 128 * sum_k xr[t][k] * cb[idx[o][k]] * norm[o][k / 128]
-// and both factors of the contraction are fed to tcgen05.mma as bf16:
-//   A = bf16(cb[idx] * norm)        [N out-rows][K]  - dequantised into TENSOR memory
-//   B = bf16(xr * s_t / 128)        [M tokens][K]    - rotated once per call, TMA-loaded
+// and both factors of the contraction are fed to tcgen05.mma as fp16:
+//   A = fp16(fp16(cb[idx]) * norm)  [N out-rows][K]  - dequantised into TENSOR memory
+//   B = fp16(xr * s_t / 128)        [M tokens][K]    - rotated once per call, TMA-loaded
 // D[o][t] accumulates in fp32 in tensor memory; the epilogue rounds to bf16 and stores
 // the transposed tile.  Keeping the dequantised weights in tensor memory means shared
 // memory only carries the activation tile (TMA write + one MMA read) and the packed
@@ -31,6 +31,13 @@
 //               times per stage): packed tile -> codeword pairs from a per-lane shared
 //               table, scaled by the group norm, bf16, tcgen05.st into the A stage
 //               (two warps per lane quarter, 32 k each)
+// The 32-token decode tiles run MMAW issuer threads (warps 1..MMAW) instead of one: the
+// thread that issues a stage also waits for it, fences and commits it, and those steps
+// (not the tensor core: an M=128, N=32 MMA is ~25 cycles of work) set the pace of one
+// issuer, ~600 cycles per stage.  Issuer j takes the stages t of a tile with
+// t % MMAW == j into a partial accumulator of its own; each tracks only its own MMAs
+// with its commits, and the epilogue adds the partials.  The epilogue and dequant warps
+// shift up by MMAW - 1.
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a device error
 // flag, stops issuing work, frees its tensor memory and returns.
 
@@ -47,12 +54,9 @@ namespace {
 
 constexpr int kBO = 128;                 // out-rows per tile (MMA M, TMEM lanes)
 constexpr int kBK = 64;                  // K per stage (128 bytes of 16-bit operands)
-constexpr int kThreadsGemm = 832;        // 26 warps: TMA, MMA, 8 epilogue, 16 dequant
-constexpr int kEpiWarp0 = 2;             // warps 2..9: two per TMEM lane quarter
-constexpr int kEpiWarps = 8;
-constexpr int kDequantWarp0 = kEpiWarp0 + kEpiWarps;
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
 constexpr int kDequantWarps = 8;         // per stage: two per TMEM lane quarter
-constexpr int kDequantGroups = 2;        // warps 10..17 take even stages, 18..25 odd ones
+constexpr int kDequantGroups = 2;        // the first eight dequant warps take even stages
 constexpr int kTmemCols = 512;
 constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
 constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + stages + barriers
@@ -73,15 +77,21 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //   BT      tokens per tile (MMA N)
 //   F16     fp16 operands and fp32 output (the batched-decode form of the product);
 //           otherwise bf16 operands and bf16 output (prefill)
-//   STAGES  depth of the shared-memory ring (= tensor-memory A stages)
+//   STAGES  depth of the tensor-memory A ring (and of the shared-memory ring unless
+//           SSTAGES is given)
 //   FMT     weight format: CQ (packed indices + norms) or Q4_0 blocks
 //   SLABS   Q4_0 and 1-/3-bit CQ: depth of the weight-slab ring
 //   TLIST   look the CTA's tiles up once, into shared memory (grouped launches of many
 //           problems, where each lookup is a binary search over the parameter block)
 //   BITS    CQ index width: 4 or 2 (the packed tile rides in the stage, 32 or 16 bytes
 //           per row), 1 or 3 (slabs of two stages)
+//   PF16    fp16 codeword pairs and fp16 operands with bf16 output (prefill)
+//   SSTAGES depth of the shared-memory ring when deeper than the A ring: a stage's copy
+//           is then issued SSTAGES stages ahead of its MMA, while its dequant still
+//           waits for the MMA that last read its A slot, STAGES stages back
+//   MMAW    MMA issuer threads, each with a partial accumulator per buffer
 template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false,
-          int BITS_ = 4, bool PF16_ = false>
+          int BITS_ = 4, bool PF16_ = false, int SSTAGES_ = 0, int MMAW_ = 1>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
@@ -89,12 +99,16 @@ struct GemmCfg {
     // codeword pairs and scales them by the fp16 norm with one multiply
     static constexpr bool PF16 = PF16_;
     static constexpr bool OPF16 = F16 || PF16;     // fp16 (not bf16) MMA operands
+    static constexpr int BITS = BITS_;
+    static constexpr bool CQSLAB = FMT_ == kFmtCQ && (BITS == 1 || BITS == 3);
+    // fp16 codeword pairs scaled by the fp16 norm with one multiply: every CQ tile with
+    // fp16 operands whose packed indices ride in the stage (4 and 2 bits)
+    static constexpr bool HPAIR = FMT_ == kFmtCQ && !CQSLAB && OPF16;
     static constexpr int STAGES = STAGES_;
+    static constexpr int SSTAGES = SSTAGES_ > 0 ? SSTAGES_ : STAGES_;
     static constexpr int FMT = FMT_;
     static constexpr int SLABS = SLABS_;
     static constexpr bool TLIST = TLIST_;
-    static constexpr int BITS = BITS_;
-    static constexpr bool CQSLAB = FMT == kFmtCQ && (BITS == 1 || BITS == 3);
     static constexpr int PTILE = FMT == kFmtCQ && !CQSLAB ? kBO * kBK * BITS / 8 : 0;   // packed bytes per stage
     static constexpr int SPS = FMT == kFmtQ40 ? 4 : 2;                            // stages per slab
     static constexpr int SLABROW = FMT == kFmtQ40 ? kQSlabRowBytes : SPS * kBK * BITS / 8;
@@ -102,22 +116,29 @@ struct GemmCfg {
     static constexpr int XTILE = BT * kBK * 2;        // activation tile bytes
     static constexpr int STAGE = XTILE + PTILE;
     static constexpr int DCOL0 = STAGES * kACols;     // accumulators after the A stages
-    static_assert(DCOL0 + 2 * BT <= kTmemCols, "tensor memory budget");
+    static constexpr int MMAW = MMAW_;
+    static constexpr int EPI0 = 1 + MMAW;              // first epilogue warp
+    static constexpr int DEQ0 = EPI0 + kEpiWarps;      // first dequant warp
+    static constexpr int THREADS = (DEQ0 + kDequantGroups * kDequantWarps) * 32;
+    static_assert(DCOL0 + 2 * MMAW * BT <= kTmemCols, "tensor memory budget");
+    static_assert(MMAW == 1 || BT == 32, "several issuers: 32-token tiles");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-    static_assert((3 * STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
+    static_assert((2 * SSTAGES + STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
+    static_assert(SSTAGES >= STAGES, "the shared ring is at least as deep as the A ring");
     static_assert(FMT == kFmtCQ || (F16 && SLABS >= 2), "Q4_0 runs with fp16 operands on a slab ring");
     static_assert(BITS == 4 || (FMT == kFmtCQ && F16), "1- to 3-bit CQ rows: decode batches only");
     static_assert(!CQSLAB || SLABS >= 2, "1- and 3-bit CQ rows run on a slab ring");
     static_assert(FMT == kFmtQ40 || CQSLAB || SLABS == 0, "4- and 2-bit CQ tiles ride in the stages");
     static_assert(!PF16 || (!F16 && FMT == kFmtCQ && BITS == 4), "fp16 pair tables: 4-bit prefill");
 };
-using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true>;   // 24 KB activation tile, 28 KB stages
-using DecodeCfg = GemmCfg<32, true, 8>;                  // 4 KB activation tile, 8 KB stages
-using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2>;   // 2-bit rows: 6 KB stages
-using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1>;   // 1-bit rows: 4 KB stages + 2 KB slabs
-using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3>;   // 3-bit rows: 4 KB stages + 6 KB slabs
+using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true, 5>;   // 24 KB activation tile, 5 x 28 KB stages
+constexpr int kDecodeIssuers = 2;
+using DecodeCfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 4, false, 0, kDecodeIssuers>;   // 4 KB activation tile, 8 KB stages
+using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2, false, 0, kDecodeIssuers>;  // 2-bit rows: 6 KB stages
+using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1, false, 0, kDecodeIssuers>;  // 1-bit rows: 4 KB stages + 2 KB slabs
+using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3, false, 0, kDecodeIssuers>;  // 3-bit rows: 4 KB stages + 6 KB slabs
 using Q40WideCfg = GemmCfg<192, true, 4, kFmtQ40, 4>;    // Q4_0, many tokens: 96 + 72 KB
-using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4>;   // Q4_0, up to 32 tokens: 32 + 72 KB
+using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4, false, 4, false, 0, kDecodeIssuers>;   // Q4_0, up to 32 tokens: 32 + 72 KB
 
 struct GemmProblem {
     CUtensorMap pmap;        // packed bytes as [N][K/2] uint8, box 32 x 128
@@ -439,12 +460,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 
 template <class C>
-__global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr int kBT = C::BT;
-    constexpr int kStages = C::STAGES;
+    constexpr int kStages = C::SSTAGES;    // shared-memory ring (copies)
+    constexpr int kAStages = C::STAGES;    // tensor-memory A ring (dequant -> MMA)
     constexpr int kXTileBytes = C::XTILE;
     constexpr int kStageBytes = C::STAGE;
     constexpr int kDCol0 = C::DCOL0;
+    constexpr int kThreadsGemm = C::THREADS;
+    constexpr int kMmaW = C::MMAW;
+    constexpr int kEpiWarp0 = C::EPI0;
+    constexpr int kDequantWarp0 = C::DEQ0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // CQ: the codeword-pair table sits at a 64 KB boundary of the shared window (the
     // address of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
@@ -458,7 +484,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     if constexpr (C::FMT == kFmtCQ) {
         tbase = (sbase + 65535u) & ~65535u;
         nA = tbase >= a0 + kStageBytes ? min(kStages, (int)((tbase - a0) / kStageBytes)) : 0;
-        b0 = tbase + (1u << (2 * C::BITS)) * 32u * 8u;   // pair-table entries x lanes x 8 B
+        b0 = tbase + (1u << (2 * C::BITS)) * 256u;   // the pair table: one 256-byte row per entry (32 lanes)
         slab0 = b0 + (uint32_t)(kStages - nA) * kStageBytes;
         bars_at = slab0 + (uint32_t)(C::SLABS * C::SLABBYTES);
     } else {
@@ -477,10 +503,10 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     // this CTA's tile list (problem, row tile, token tile, K half), after the barriers
     const uint32_t tiles_at = bars_at + (uint32_t)kBarBytes;
     const bool layout_ok = tiles_at + (C::TLIST ? (uint32_t)(kMaxCtaTiles * sizeof(TileRef)) : 0u) <= send;
-    uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
-    uint64_t* full_b = bars + kStages;            // dequant: A stage written to TMEM
-    uint64_t* empty = bars + 2 * kStages;         // MMA: stage consumed
-    uint64_t* acc_full = bars + 3 * kStages;      // [2] accumulator buffer ready
+    uint64_t* full_a = bars;                      // [kStages] TMA: X tile + packed tile landed
+    uint64_t* empty = bars + kStages;             // [kStages] MMA: stage consumed
+    uint64_t* full_b = bars + 2 * kStages;        // [kAStages] dequant: A stage written to TMEM
+    uint64_t* acc_full = full_b + kAStages;       // [2] accumulator buffer ready
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator buffer drained
     uint64_t* slab_full = acc_empty + 2;          // [SLABS] weight slab landed
     uint64_t* slab_empty = slab_full + C::SLABS;  // [SLABS] slab read by the dequant of its stages
@@ -505,12 +531,14 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
         slv[tid] = v;
     }
     __syncthreads();
-    if constexpr (C::PF16) {
-        // fp16 pairs (cb[e & 15] low), entry e of lane l at e << 8 | l << 2
+    if constexpr (C::HPAIR) {
+        // fp16 pairs (first index low), entry e of lane l at e << 8 | l << 2
+        constexpr int kHalf = C::BITS;
+        constexpr int kEntries = 1 << (2 * C::BITS);
         uint32_t* luth = reinterpret_cast<uint32_t*>(gen(tbase));
-        for (int i = tid; i < 256 * 32; i += kThreadsGemm) {
+        for (int i = tid; i < kEntries * 32; i += kThreadsGemm) {
             const int e = i >> 5;
-            const __half2 v = __floats2half2_rn(slv[e & 15], slv[e >> 4]);
+            const __half2 v = __floats2half2_rn(slv[e & ((1 << kHalf) - 1)], slv[e >> kHalf]);
             luth[(e << 6) | (i & 31)] = *reinterpret_cast<const uint32_t*>(&v);
         }
     } else if constexpr (C::FMT == kFmtCQ) {
@@ -524,11 +552,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_a[s], 1);
-            mbar_init(&full_b[s], kDequantWarps);
             mbar_init(&empty[s], 1);
         }
+        for (int s = 0; s < kAStages; ++s) mbar_init(&full_b[s], kDequantWarps);
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_full[b], kMmaW);   // one commit per issuer
             mbar_init(&acc_empty[b], kEpiWarps);
         }
         for (int b = 0; b < C::SLABS; ++b) {
@@ -611,40 +639,59 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer --------------------------------
+    } else if (warp <= kMmaW) {
+        // ------------------------------ MMA issuers -------------------------------
+        // issuer mj takes the stages t of each tile with t % kMmaW == mj (all of them when
+        // there is one issuer) into its partial accumulator of the tile's buffer
         if (lane == 0) {
+            const int mj = warp - 1;
             constexpr uint32_t idesc = idesc_f16kind(kBO, kBT, C::OPF16);
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, sa = 0;   // shared stage, A stage
+            uint32_t pha = 0;
             int it = 0;
             bool ok = true;
+            // B descriptors differ only in the low word (the 16-byte-unit stage address):
+            // kept as a running value, stepped per stage, jumping over the pair table
+            const uint64_t dhi = smem_desc_sw128(0u);
+            const uint32_t lo_first = (uint32_t)smem_desc_sw128(smem_u32(stage_ptr(0)));
+            const uint32_t lo_above = (uint32_t)smem_desc_sw128(smem_u32(stage_ptr(nA < kStages ? nA : 0)));
+            uint32_t blo = lo_first;
+            uint32_t aaddr = tmem_base;   // A stage sa
             for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
                 const TileRef tr = tile_at(it, tile);
                 const GemmProblem& pr = p.prob[tr.prob];
                 const int buf = it & 1;
                 const uint32_t aph = (uint32_t)((it >> 1) & 1);
-                if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, p)) break;
-                tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(kDCol0 + buf * kBT);
                 int kb, ke;
                 k_range(pr, tr.ks, kb, ke);
+                // every issuer waits for the buffer, also one without a stage in this tile
+                // (its partial stays unwritten; the epilogue adds only the partials of the
+                // tile's first kMmaW stages): its acc_full commit then cannot arrive on the
+                // barrier before the buffer's previous phase has completed
+                if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, p)) break;
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(kDCol0 + (buf * kMmaW + mj) * kBT);
                 for (int kc = kb; kc < ke; ++kc) {
-                    // the dequant warps arrive on full_b only after waiting on the TMA
-                    // barrier of the same stage, so it also orders the TMA writes
-                    if (!mbar_wait(&full_b[s], ph, abort_flag, p)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint64_t bdesc0 = smem_desc_sw128(smem_u32(stage_ptr(s)));
-                    const uint32_t a0 = tmem_base + (uint32_t)(s * kACols);
+                    if ((kc - kb) % kMmaW == mj) {
+                        // the dequant warps arrive on full_b only after waiting on the TMA
+                        // barrier of the same stage, so it also orders the TMA writes
+                        if (!mbar_wait(&full_b[sa], pha, abort_flag, p)) { ok = false; break; }
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // A: 8 TMEM columns (16 bf16) per K step; B: +32 bytes along K
-                        // inside the swizzle atom = +2 in the 16-byte-unit address field
-                        umma_bf16_tmem_a(d, a0 + (uint32_t)(8 * kk), bdesc0 + 2u * kk, idesc,
-                                         (kc > kb || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            // A: 8 TMEM columns (16 bf16) per K step; B: +32 bytes along K
+                            // inside the swizzle atom = +2 in the 16-byte-unit address field
+                            umma_bf16_tmem_a(d, aaddr + (uint32_t)(8 * kk), dhi | (uint64_t)(blo + 2u * kk), idesc,
+                                             (kc - kb >= kMmaW || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&empty[s]);
                     }
-                    umma_commit(&empty[s]);
-                    if (++s == kStages) { s = 0; ph ^= 1u; }
+                    ++s;
+                    blo += (uint32_t)(kStageBytes >> 4);
+                    if (s == nA) blo = lo_above;
+                    if (s == kStages) { s = 0; blo = lo_first; }
+                    aaddr += (uint32_t)kACols;
+                    if (++sa == kAStages) { sa = 0; pha ^= 1u; aaddr = tmem_base; }
                 }
                 if (!ok) break;
                 umma_commit(&acc_full[buf]);
@@ -665,7 +712,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
             if (!mbar_wait(&acc_full[buf], (uint32_t)((it >> 1) & 1), abort_flag, p)) break;
             tc_fence_after();
             const uint32_t col0 = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                  (uint32_t)(kDCol0 + buf * kBT + th * (kBT / 2));
+                                  (uint32_t)(kDCol0 + buf * kMmaW * kBT + th * (kBT / 2));
             const int o = tr.nt * kBO + q * 32 + lane;
             const int t0 = tr.mt * kBT + th * (kBT / 2);
             const bool ook = o < pr.N;
@@ -689,12 +736,31 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                     }
                 }
             };
-            tmem_ld16_async(col0, rr[0]);
+            if constexpr (kMmaW == 1) {
+                tmem_ld16_async(col0, rr[0]);
 #pragma unroll
-            for (int pc = 0; pc < kPieces; ++pc) {
+                for (int pc = 0; pc < kPieces; ++pc) {
+                    tmem_wait_ld();
+                    if (pc + 1 < kPieces) tmem_ld16_async(col0 + 16 * (pc + 1), rr[(pc + 1) & 1]);
+                    store16(rr[pc & 1], t0 + 16 * pc);
+                }
+            } else {
+                // one 16-column piece (32-token tiles); the partials of issuers that had
+                // a stage in this tile, summed in issuer order
+                static_assert(kPieces == 1, "several issuers: one piece per warp");
+                int kb, ke;
+                k_range(pr, tr.ks, kb, ke);
+                const int np = min(kMmaW, ke - kb);
+                tmem_ld16_async(col0, rr[0]);
                 tmem_wait_ld();
-                if (pc + 1 < kPieces) tmem_ld16_async(col0 + 16 * (pc + 1), rr[(pc + 1) & 1]);
-                store16(rr[pc & 1], t0 + 16 * pc);
+                for (int j = 1; j < np; ++j) {
+                    tmem_ld16_async(col0 + (uint32_t)(j * kBT), rr[1]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        rr[0][i] = __float_as_uint(__uint_as_float(rr[0][i]) + __uint_as_float(rr[1][i]));
+                }
+                store16(rr[0], t0);
             }
             tc_fence_before();
             __syncwarp();
@@ -723,10 +789,22 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                 if (gi % kDequantGroups != grp) continue;   // the other group's stage
                 const int s = gi % kStages;
                 const uint32_t ph = (uint32_t)((gi / kStages) & 1);
+                const int sa = gi % kAStages;
+                // with a deeper shared ring the landed copy no longer implies that the MMA
+                // of stage gi - kAStages (the last reader of A slot sa) has completed: wait
+                // for its commit.  After the full_a wait every commit up to stage
+                // gi - kStages has completed, and the next commit on that barrier needs this
+                // stage's MMA, so the parity names exactly that commit.
+                auto a_slot_free = [&]() {
+                    if constexpr (kStages == kAStages) return true;
+                    if (gi < kAStages) return true;
+                    const int g4 = gi - kAStages;
+                    return mbar_wait(&empty[g4 % kStages], (uint32_t)((g4 / kStages) & 1), abort_flag, p);
+                };
                 if constexpr (C::FMT == kFmtQ40) {
                     // the full_a wait frees the A stage (its previous MMA has completed)
                     // and, through full_b, orders the activation tile for the MMA
-                    if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
+                    if (!mbar_wait(&full_a[s], ph, abort_flag, p) || !a_slot_free()) { ok = false; break; }
                     const int sg = gi / C::SPS;   // every K is a whole number of slabs
                     const int qs = sg % C::SLABS;
                     if (!mbar_wait(&slab_full[qs], (uint32_t)((sg / C::SLABS) & 1), abort_flag, p)) {
@@ -765,15 +843,15 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                             pk[4 * i + j] = *reinterpret_cast<uint32_t*>(&h);
                         }
                     }
-                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(sa * kACols + kh * 16), pk);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    if (lane == 0) mbar_arrive(&full_b[sa]);
                     continue;
                 }
                 const float nrm = load_norm(pr, tr.nt * kBO + r, kc);
-                if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
+                if (!mbar_wait(&full_a[s], ph, abort_flag, p) || !a_slot_free()) { ok = false; break; }
                 if constexpr (C::CQSLAB) {
                     const int sg = gi / C::SPS;   // every K is a whole number of slabs
                     const int qs = sg % C::SLABS;
@@ -805,11 +883,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                         __half2 h = __floats2half2_rn(cn.x, cn.y);
                         pk[pi] = *reinterpret_cast<uint32_t*>(&h);
                     }
-                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(sa * kACols + kh * 16), pk);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    if (lane == 0) mbar_arrive(&full_b[sa]);
                     continue;
                 }
                 // this lane's 32 indices of the stage half kh, as 16 pair bytes: 4-bit rows
@@ -825,7 +903,7 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                     wv[2] = w.y & 0x0F0F0F0Fu; wv[3] = (w.y >> 4) & 0x0F0F0F0Fu;
                 }
                 uint32_t pk[16];
-                if constexpr (C::PF16) {
+                if constexpr (C::HPAIR) {
                     // fp16 pair lookups (4 bytes) times the fp16 norm (exact: the norm is
                     // stored as fp16): one multiply per pair, no conversion
                     const uint32_t lb4 = tbase | ((uint32_t)lane << 2);
@@ -836,15 +914,18 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                                                lds_u32(pair_addr<2>(wv[k], lb4)), lds_u32(pair_addr<3>(wv[k], lb4))};
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
+                            // pair index within the half: byte j of word k (4-bit), or byte j
+                            // of packed word k / 2, low or high nibble (2-bit)
+                            const int pi = C::BITS == 4 ? 4 * k + j : 8 * (k >> 1) + 2 * j + (k & 1);
                             const __half2 v = __hmul2(*reinterpret_cast<const __half2*>(&c[j]), nh);
-                            pk[4 * k + j] = *reinterpret_cast<const uint32_t*>(&v);
+                            pk[pi] = *reinterpret_cast<const uint32_t*>(&v);
                         }
                     }
-                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(sa * kACols + kh * 16), pk);
                     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&full_b[s]);
+                    if (lane == 0) mbar_arrive(&full_b[sa]);
                     continue;
                 }
                 const float2 n2 = make_float2(nrm, nrm);
@@ -867,11 +948,11 @@ __global__ void __launch_bounds__(kThreadsGemm, 1) cq_gemm_kernel(const __grid_c
                         }
                     }
                 }
-                tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(s * kACols + kh * 16), pk);
+                tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(sa * kACols + kh * 16), pk);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full_b[s]);
+                if (lane == 0) mbar_arrive(&full_b[sa]);
             }
         }
     }
@@ -1215,7 +1296,7 @@ cq_status run_grouped(const cq_gemm_problem* probs, int count, int64_t M, int b,
         prm.timeout_ns = 2000000000ull;   // 2 s per wait
         const size_t smem = (size_t)kGemmSmem;
         const int grid = tiles < sm_count() ? tiles : sm_count();
-        st = launch_pdl(cq_gemm_kernel<C>, dim3(grid), dim3(kThreadsGemm), smem, cs, prm);
+        st = launch_pdl(cq_gemm_kernel<C>, dim3(grid), dim3(C::THREADS), smem, cs, prm);
         if (st != CQ_OK) return st;
     }
     return CQ_OK;
@@ -1337,7 +1418,7 @@ cq_status run_q40(const uint8_t* blocks, int64_t N, int64_t K, const float* X, i
     prm.err = err;
     prm.timeout_ns = 2000000000ull;   // 2 s per wait
     const int grid = prm.total_tiles < sm_count() ? prm.total_tiles : sm_count();
-    return launch_pdl(cq_gemm_kernel<C>, dim3(grid), dim3(kThreadsGemm), (size_t)kGemmSmem, cs, prm);
+    return launch_pdl(cq_gemm_kernel<C>, dim3(grid), dim3(C::THREADS), (size_t)kGemmSmem, cs, prm);
 }
 
 }  // namespace
