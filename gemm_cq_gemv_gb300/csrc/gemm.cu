@@ -54,9 +54,7 @@ namespace {
 
 constexpr int kBO = 128;                 // out-rows per tile (MMA M, TMEM lanes)
 constexpr int kBK = 64;                  // K per stage (128 bytes of 16-bit operands)
-constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
 constexpr int kDequantWarps = 8;         // per stage: two per TMEM lane quarter
-constexpr int kDequantGroups = 2;        // the first eight dequant warps take even stages
 constexpr int kTmemCols = 512;
 constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
 constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + stages + barriers
@@ -90,8 +88,13 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //           is then issued SSTAGES stages ahead of its MMA, while its dequant still
 //           waits for the MMA that last read its A slot, STAGES stages back
 //   MMAW    MMA issuer threads, each with a partial accumulator per buffer
+//   DGROUPS dequant groups of eight warps, taking stages in turn
+//   EPIW    epilogue warps (a multiple of 4: one set per TMEM lane quarter)
+//   PROD    copy-issuing threads: 1, or 2 (one for the activation tiles, one for the
+//           packed weight tiles or slabs)
 template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false,
-          int BITS_ = 4, bool PF16_ = false, int SSTAGES_ = 0, int MMAW_ = 1>
+          int BITS_ = 4, bool PF16_ = false, int SSTAGES_ = 0, int MMAW_ = 1, int DGROUPS_ = 2,
+          int EPIW_ = 8, int PROD_ = 1>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
@@ -117,9 +120,15 @@ struct GemmCfg {
     static constexpr int STAGE = XTILE + PTILE;
     static constexpr int DCOL0 = STAGES * kACols;     // accumulators after the A stages
     static constexpr int MMAW = MMAW_;
-    static constexpr int EPI0 = 1 + MMAW;              // first epilogue warp
-    static constexpr int DEQ0 = EPI0 + kEpiWarps;      // first dequant warp
-    static constexpr int THREADS = (DEQ0 + kDequantGroups * kDequantWarps) * 32;
+    static constexpr int PROD = PROD_;
+    static constexpr int EPI0 = PROD + MMAW;           // first epilogue warp
+    static constexpr int EPIW = EPIW_;
+    static constexpr int DGROUPS = DGROUPS_;
+    static constexpr int DEQ0 = EPI0 + EPIW;           // first dequant warp
+    static constexpr int THREADS = (DEQ0 + DGROUPS * kDequantWarps) * 32;
+    static_assert(EPIW % 4 == 0 && (BT / (EPIW / 4)) % 16 == 0, "epilogue warps: 16-column pieces");
+    static_assert(THREADS <= 1024, "one CTA per SM");
+    static_assert(PROD == 1 || PROD == 2, "one or two copy-issuing threads");
     static_assert(DCOL0 + 2 * MMAW * BT <= kTmemCols, "tensor memory budget");
     static_assert(MMAW == 1 || BT == 32, "several issuers: 32-token tiles");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
@@ -133,12 +142,13 @@ struct GemmCfg {
 };
 using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true, 5>;   // 24 KB activation tile, 5 x 28 KB stages
 constexpr int kDecodeIssuers = 2;
-using DecodeCfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 4, false, 0, kDecodeIssuers>;   // 4 KB activation tile, 8 KB stages
-using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2, false, 0, kDecodeIssuers>;  // 2-bit rows: 6 KB stages
-using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1, false, 0, kDecodeIssuers>;  // 1-bit rows: 4 KB stages + 2 KB slabs
-using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3, false, 0, kDecodeIssuers>;  // 3-bit rows: 4 KB stages + 6 KB slabs
+constexpr int kDecodeProducers = 2;
+using DecodeCfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 4, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;   // 4 KB activation tile, 8 KB stages
+using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;  // 2-bit rows: 6 KB stages
+using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;  // 1-bit rows: 4 KB stages + 2 KB slabs
+using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;  // 3-bit rows: 4 KB stages + 6 KB slabs
 using Q40WideCfg = GemmCfg<192, true, 4, kFmtQ40, 4>;    // Q4_0, many tokens: 96 + 72 KB
-using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4, false, 4, false, 0, kDecodeIssuers>;   // Q4_0, up to 32 tokens: 32 + 72 KB
+using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4, false, 4, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;   // Q4_0, up to 32 tokens: 32 + 72 KB
 
 struct GemmProblem {
     CUtensorMap pmap;        // packed bytes as [N][K/2] uint8, box 32 x 128
@@ -416,11 +426,11 @@ __device__ __forceinline__ void k_range(const GemmProblem& pr, int ks, int& kb, 
     ke = min(pr.K / kBK, kb + pr.kchunk);
 }
 
-// norm (as fp32) of row `o` for K-chunk `kc`, 0 for rows past N
-__device__ __forceinline__ float load_norm(const GemmProblem& pr, int o, int kc) {
-    if (o >= pr.N) return 0.0f;
+// norm (fp16 bits) of row `o` for K-chunk `kc`, 0 for rows past N
+__device__ __forceinline__ uint16_t norm_bits(const GemmProblem& pr, int o, int kc) {
+    if (o >= pr.N) return 0;
     const int G = pr.K / kGroup;
-    return f16_bits_to_f32(__ldg(pr.norms + (int64_t)o * G + (kc * kBK) / kGroup));
+    return __ldg(pr.norms + (int64_t)o * G + (kc * kBK) / kGroup);
 }
 
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
@@ -469,8 +479,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
     constexpr int kDCol0 = C::DCOL0;
     constexpr int kThreadsGemm = C::THREADS;
     constexpr int kMmaW = C::MMAW;
+    constexpr int kProd = C::PROD;
+    // stage barrier arrivals: one per thread that copies into the stage
+    constexpr int kFullAArrivals = (kProd == 2 && C::PTILE > 0) ? 2 : 1;
     constexpr int kEpiWarp0 = C::EPI0;
     constexpr int kDequantWarp0 = C::DEQ0;
+    constexpr int kEpiWarps = C::EPIW;
+    constexpr int kDequantGroups = C::DGROUPS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // CQ: the codeword-pair table sits at a 64 KB boundary of the shared window (the
     // address of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
@@ -551,7 +566,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
     }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_a[s], 1);
+            mbar_init(&full_a[s], kFullAArrivals);
             mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < kAStages; ++s) mbar_init(&full_b[s], kDequantWarps);
@@ -593,9 +608,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
     // of the stream finishes; global memory is touched only after it has
     pdl_wait();
 
-    if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------------
+    if (warp < kProd) {
+        // ------------------------------ TMA producers -----------------------------
+        // one thread issues every copy, or (two producers) warp 0 the activation tiles
+        // and warp 1 the packed tiles or weight slabs; a thread with no copy in a stage
+        // still walks it, to keep its ring position
         if (lane == 0) {
+            const bool cx = warp == 0;                    // activation tiles
+            const bool cp = warp == kProd - 1;            // packed tiles and slabs
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
@@ -611,7 +631,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     if constexpr (C::SLABS > 0) {
                         // the slab of this stage and the next SPS - 1 (tile K ranges are
                         // whole slabs)
-                        if (kc % C::SPS == 0) {
+                        if (cp && kc % C::SPS == 0) {
                             const int qs = pg % C::SLABS;
                             const uint32_t sph = (uint32_t)((pg / C::SLABS) & 1);
                             if (!mbar_wait(&slab_empty[qs], sph ^ 1u, abort_flag, p)) {
@@ -624,27 +644,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                             ++pg;
                         }
                     }
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p)) { ok = false; break; }
-                    uint8_t* st = stage_ptr(s);
-                    if constexpr (C::PTILE > 0) {
-                        mbar_arrive_tx(&full_a[s], kXTileBytes + C::PTILE);
-                        tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
-                        tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK * C::BITS / 8), tr.nt * kBO, &full_a[s]);
-                    } else {
-                        mbar_arrive_tx(&full_a[s], kXTileBytes);
-                        tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
+                    if (cx || (cp && C::PTILE > 0)) {
+                        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p)) { ok = false; break; }
+                        uint8_t* st = stage_ptr(s);
+                        if (cx) {
+                            // with one producer the packed tile rides on the same arrival
+                            const uint32_t bytes = kXTileBytes + (kProd == 1 ? (uint32_t)C::PTILE : 0u);
+                            mbar_arrive_tx(&full_a[s], bytes);
+                            tma_load_2d(st, xmap, kc * kBK, tr.mt * kBT, &full_a[s]);
+                        } else {
+                            mbar_arrive_tx(&full_a[s], (uint32_t)C::PTILE);
+                        }
+                        if constexpr (C::PTILE > 0) {
+                            if (cp)
+                                tma_load_2d(st + kXTileBytes, &pr.pmap, kc * (kBK * C::BITS / 8), tr.nt * kBO,
+                                            &full_a[s]);
+                        }
                     }
                     if (++s == kStages) { s = 0; ph ^= 1u; }
                 }
             }
         }
         __syncwarp();
-    } else if (warp <= kMmaW) {
+    } else if (warp < kProd + kMmaW) {
         // ------------------------------ MMA issuers -------------------------------
         // issuer mj takes the stages t of each tile with t % kMmaW == mj (all of them when
         // there is one issuer) into its partial accumulator of the tile's buffer
         if (lane == 0) {
-            const int mj = warp - 1;
+            const int mj = warp - kProd;
             constexpr uint32_t idesc = idesc_f16kind(kBO, kBT, C::OPF16);
             int s = 0, sa = 0;   // shared stage, A stage
             uint32_t pha = 0;
@@ -700,8 +727,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
         __syncwarp();
     } else if (warp < kDequantWarp0) {
         // ------------------------------ epilogue ----------------------------------
-        // warp -> TMEM lane quarter q (out-rows 32q..32q+31) and token half th (96 tokens);
-        // three 32-column loads per tile, each issued before the previous one is stored
+        // warp -> TMEM lane quarter q (out-rows 32q..32q+31) and token slice th of kTW
+        // tokens (96 of the prefill's 192 with eight epilogue warps)
+        constexpr int kTW = kBT / (kEpiWarps / 4);
         const int q = warp & 3;
         const int th = (warp - kEpiWarp0) >> 2;
         int it = 0;
@@ -712,14 +740,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
             if (!mbar_wait(&acc_full[buf], (uint32_t)((it >> 1) & 1), abort_flag, p)) break;
             tc_fence_after();
             const uint32_t col0 = tmem_base + ((uint32_t)(q * 32) << 16) +
-                                  (uint32_t)(kDCol0 + buf * kMmaW * kBT + th * (kBT / 2));
+                                  (uint32_t)(kDCol0 + buf * kMmaW * kBT + th * kTW);
             const int o = tr.nt * kBO + q * 32 + lane;
-            const int t0 = tr.mt * kBT + th * (kBT / 2);
+            const int t0 = tr.mt * kBT + th * kTW;
             const bool ook = o < pr.N;
             __nv_bfloat16* ycol = static_cast<__nv_bfloat16*>(pr.Y) + o;
             float* ycolf = static_cast<float*>(pr.Y) + o;
             // 16-column pieces, each load issued before the previous piece is stored
-            constexpr int kPieces = (kBT / 2) / 16;
+            constexpr int kPieces = kTW / 16;
             uint32_t rr[2][16];
             auto store16 = [&](const uint32_t (&r)[16], int tb) {
                 if (!ook) return;
@@ -745,22 +773,24 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     store16(rr[pc & 1], t0 + 16 * pc);
                 }
             } else {
-                // one 16-column piece (32-token tiles); the partials of issuers that had
-                // a stage in this tile, summed in issuer order
-                static_assert(kPieces == 1, "several issuers: one piece per warp");
+                // per 16-column piece, the partials of the issuers that had a stage in this
+                // tile, summed in issuer order
                 int kb, ke;
                 k_range(pr, tr.ks, kb, ke);
                 const int np = min(kMmaW, ke - kb);
-                tmem_ld16_async(col0, rr[0]);
-                tmem_wait_ld();
-                for (int j = 1; j < np; ++j) {
-                    tmem_ld16_async(col0 + (uint32_t)(j * kBT), rr[1]);
-                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        rr[0][i] = __float_as_uint(__uint_as_float(rr[0][i]) + __uint_as_float(rr[1][i]));
+                for (int pc = 0; pc < kPieces; ++pc) {
+                    tmem_ld16_async(col0 + 16 * pc, rr[0]);
+                    tmem_wait_ld();
+                    for (int j = 1; j < np; ++j) {
+                        tmem_ld16_async(col0 + (uint32_t)(j * kBT + 16 * pc), rr[1]);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            rr[0][i] = __float_as_uint(__uint_as_float(rr[0][i]) + __uint_as_float(rr[1][i]));
+                    }
+                    store16(rr[0], t0 + 16 * pc);
                 }
-                store16(rr[0], t0);
             }
             tc_fence_before();
             __syncwarp();
@@ -780,11 +810,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
         bool ok = true;
         int gi = 0;   // global stage index
         int ti = 0;
+        // this lane's row norms, eight groups (16 bytes) per load where the rows allow it:
+        // one scattered 2-byte load per lane and stage made the norms the largest
+        // consumer of the L1 data pipe
+        uint4 nv = make_uint4(0u, 0u, 0u, 0u);
+        int nv_g0 = -1;   // first group held in nv, -1: none
         for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++ti) {
             const TileRef tr = tile_at(ti, tile);
             const GemmProblem& pr = p.prob[tr.prob];
             int kb, ke;
             k_range(pr, tr.ks, kb, ke);
+            const int orow = tr.nt * kBO + r;
+            const int G = pr.K / kGroup;
+            const bool nvec = (G & 7) == 0 && (reinterpret_cast<uintptr_t>(pr.norms) & 15u) == 0;
+            nv_g0 = -1;
             for (int kc = kb; kc < ke; ++kc, ++gi) {
                 if (gi % kDequantGroups != grp) continue;   // the other group's stage
                 const int s = gi % kStages;
@@ -850,7 +889,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     if (lane == 0) mbar_arrive(&full_b[sa]);
                     continue;
                 }
-                const float nrm = load_norm(pr, tr.nt * kBO + r, kc);
+                uint16_t nb;
+                if (nvec) {
+                    const int g = (kc * kBK) / kGroup;
+                    if ((g & ~7) != nv_g0) {
+                        nv_g0 = g & ~7;
+                        nv = orow < pr.N ? __ldg(reinterpret_cast<const uint4*>(pr.norms + (int64_t)orow * G + nv_g0))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    const int j = g & 7;
+                    const uint32_t w = (j >> 1) == 0 ? nv.x : (j >> 1) == 1 ? nv.y : (j >> 1) == 2 ? nv.z : nv.w;
+                    nb = (uint16_t)(w >> ((j & 1) * 16));
+                } else {
+                    nb = norm_bits(pr, orow, kc);
+                }
                 if (!mbar_wait(&full_a[s], ph, abort_flag, p) || !a_slot_free()) { ok = false; break; }
                 if constexpr (C::CQSLAB) {
                     const int sg = gi / C::SPS;   // every K is a whole number of slabs
@@ -870,6 +922,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     w[C::BITS] = 0u;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&slab_empty[qs]);
+                    const float nrm = f16_bits_to_f32(nb);
                     const float2 n2 = make_float2(nrm, nrm);
                     uint32_t pk[16];
 #pragma unroll
@@ -907,7 +960,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     // fp16 pair lookups (4 bytes) times the fp16 norm (exact: the norm is
                     // stored as fp16): one multiply per pair, no conversion
                     const uint32_t lb4 = tbase | ((uint32_t)lane << 2);
-                    const __half2 nh = __float2half2_rn(nrm);
+                    const __half2 nh = __halves2half2(__ushort_as_half(nb), __ushort_as_half(nb));
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint32_t c[4] = {lds_u32(pair_addr<0>(wv[k], lb4)), lds_u32(pair_addr<1>(wv[k], lb4)),
@@ -928,6 +981,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     if (lane == 0) mbar_arrive(&full_b[sa]);
                     continue;
                 }
+                const float nrm = f16_bits_to_f32(nb);
                 const float2 n2 = make_float2(nrm, nrm);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
