@@ -17,7 +17,7 @@
 // the shared window, so a lookup address is one byte permute; four 28 KB stages around it.
 // Tensor memory (512 columns): 4 A stages of 32 columns (64 bf16 per row) and two
 // 192-column fp32 accumulators (the epilogue of a tile overlaps the next main loop).
-// Warp roles:
+// Warp roles (prefill):
 //   warp 0      TMA producer: per stage the activation tile (128-byte
 //               swizzle) and the packed 4-bit weight tile (128 rows x 32 bytes)
 //   warp 1      MMA issuer (one thread): 4 tcgen05.mma (M=128, N=192, K=16) per stage,
@@ -28,16 +28,20 @@
 //   warps 10-25 dequant, two groups of eight taking alternate stages (a stage's
 //               dequant latency - table loads, tensor-memory store and its wait - is
 //               longer than its share of the MMA time, so each group gets two stage
-//               times per stage): packed tile -> codeword pairs from a per-lane shared
-//               table, scaled by the group norm, bf16, tcgen05.st into the A stage
+//               times per stage): packed tile -> fp16 codeword pairs from a per-lane
+//               shared table, times the group norm, tcgen05.st into the A stage
 //               (two warps per lane quarter, 32 k each)
-// The 32-token decode tiles run MMAW issuer threads (warps 1..MMAW) instead of one: the
+// What paces the prefill, measured with clock stamps of CTA 0: the MMA issuer thread.
+// Its wait, fence, four MMAs and commit take ~600-750 cycles per stage against ~490
+// cycles of tensor work; each tcgen05 instruction costs the issuing thread ~60-90 cycles.
+// The 32-token decode tiles run two copy threads (warp 0: activation tiles, warp 1:
+// packed tiles or weight slabs) and MMAW issuer threads instead of one: the
 // thread that issues a stage also waits for it, fences and commits it, and those steps
 // (not the tensor core: an M=128, N=32 MMA is ~25 cycles of work) set the pace of one
 // issuer, ~600 cycles per stage.  Issuer j takes the stages t of a tile with
 // t % MMAW == j into a partial accumulator of its own; each tracks only its own MMAs
 // with its commits, and the epilogue adds the partials.  The epilogue and dequant warps
-// shift up by MMAW - 1.
+// follow the copy and issuer warps.
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a device error
 // flag, stops issuing work, frees its tensor memory and returns.
 
@@ -140,7 +144,7 @@ struct GemmCfg {
     static_assert(FMT == kFmtQ40 || CQSLAB || SLABS == 0, "4- and 2-bit CQ tiles ride in the stages");
     static_assert(!PF16 || (!F16 && FMT == kFmtCQ && BITS == 4), "fp16 pair tables: 4-bit prefill");
 };
-using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true, 5>;   // 24 KB activation tile, 5 x 28 KB stages
+using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true>;   // 24 KB activation tile, 28 KB stages
 constexpr int kDecodeIssuers = 2;
 constexpr int kDecodeProducers = 2;
 using DecodeCfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 4, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;   // 4 KB activation tile, 8 KB stages
@@ -810,9 +814,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
         bool ok = true;
         int gi = 0;   // global stage index
         int ti = 0;
-        // this lane's row norms, eight groups (16 bytes) per load where the rows allow it:
-        // one scattered 2-byte load per lane and stage made the norms the largest
-        // consumer of the L1 data pipe
+        // this lane's row norms, eight (16 bytes) or four groups (8 bytes) per load where
+        // the rows allow it: one scattered 2-byte load per lane and stage made the norms
+        // the largest consumer of the L1 data pipe
         uint4 nv = make_uint4(0u, 0u, 0u, 0u);
         int nv_g0 = -1;   // first group held in nv, -1: none
         for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++ti) {
@@ -822,7 +826,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
             k_range(pr, tr.ks, kb, ke);
             const int orow = tr.nt * kBO + r;
             const int G = pr.K / kGroup;
-            const bool nvec = (G & 7) == 0 && (reinterpret_cast<uintptr_t>(pr.norms) & 15u) == 0;
+            const uintptr_t nal = reinterpret_cast<uintptr_t>(pr.norms);
+            const int nvw = ((G & 7) == 0 && (nal & 15u) == 0) ? 8 : ((G & 3) == 0 && (nal & 7u) == 0) ? 4 : 0;
             nv_g0 = -1;
             for (int kc = kb; kc < ke; ++kc, ++gi) {
                 if (gi % kDequantGroups != grp) continue;   // the other group's stage
@@ -890,14 +895,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     continue;
                 }
                 uint16_t nb;
-                if (nvec) {
+                if (nvw != 0) {
                     const int g = (kc * kBK) / kGroup;
-                    if ((g & ~7) != nv_g0) {
-                        nv_g0 = g & ~7;
-                        nv = orow < pr.N ? __ldg(reinterpret_cast<const uint4*>(pr.norms + (int64_t)orow * G + nv_g0))
-                                         : make_uint4(0u, 0u, 0u, 0u);
+                    if ((g & -nvw) != nv_g0) {
+                        nv_g0 = g & -nvw;
+                        const uint16_t* src = pr.norms + (int64_t)orow * G + nv_g0;
+                        if (orow >= pr.N) {
+                            nv = make_uint4(0u, 0u, 0u, 0u);
+                        } else if (nvw == 8) {
+                            nv = __ldg(reinterpret_cast<const uint4*>(src));
+                        } else {
+                            const uint2 h = __ldg(reinterpret_cast<const uint2*>(src));
+                            nv = make_uint4(h.x, h.y, 0u, 0u);
+                        }
                     }
-                    const int j = g & 7;
+                    const int j = g & (nvw - 1);
                     const uint32_t w = (j >> 1) == 0 ? nv.x : (j >> 1) == 1 ? nv.y : (j >> 1) == 2 ? nv.z : nv.w;
                     nb = (uint16_t)(w >> ((j & 1) * 16));
                 } else {
