@@ -289,9 +289,10 @@ def prefill_report(dev, cb, torch, cq, synth, steps, warmup, peaks, kind):
     peak = float(peaks["bf16_tflops"])
     out = {"workload": "20-layer 45M-parameter model (q,o 512x512; k,v 128x512; up 1536x512; "
                        "down 512x1536), CQ-W4A8, one grouped launch of 120 matrices",
-           "dtype": "bf16 MMA, fp32 accumulate, bf16 out",
+           "dtype": "fp16 MMA operands, fp32 accumulate, bf16 out",
            "kernel": "cq_gemm_kernel", "bound": "tensor", "unit": "TFLOP/s", "peak_tflops": peak,
-           "peak_source": f"{kind} bf16_tflops (burst; the GEMM is timed alone)"}
+           "peak_source": f"{kind} bf16_tflops (burst; the GEMM is timed alone; fp16 and bf16 "
+                          "have the same nominal dense rate, ratio 1)"}
     for M in synth.PREFILL_TOKENS:
         pf = build_prefill(dev, cb, torch, cq, synth, M)
         ms = time_prefill(pf, cb, cq, torch, steps, warmup)
