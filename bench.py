@@ -385,13 +385,18 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(2, 8
 
 def mixed_report(dev, cb, torch, cq, synth, steps, warmup, hbm):
     """Config 3: CQ at every width b = 1..4 on [4096, 4096] and [11008, 4096] (weights with
-    1 % x10 outliers), batches 1 / 4 / 16, each ``cq_gemv`` call timed alone after an L2 flush.
-    Keys ``<matrix>_b<b>_B<B>_{us,GBps,Gwps,frac}``; GB/s counts packed indices, norms,
-    activations, scales and outputs."""
+    1 % x10 outliers), batches 1 / 4 / 16, each measured twice: one ``cq_gemv`` call timed
+    alone after an L2 flush (``<matrix>_b<b>_B<B>_{us,GBps,Gwps,frac}``), and streamed:
+    one CUDA graph of back-to-back calls over distinct copies of the weights spanning 4x
+    the L2, per call (``..._streamed_{us,GBps,frac}``).  GB/s counts packed indices,
+    norms, activations, scales and outputs."""
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
+    l2 = l2_bytes(torch, dev)
     out = {"workload": "CQ mixed widths: [4096,4096] (sq) and [11008,4096] (up), b=1..4, "
                        "batch 1/4/16, 1% x10 outliers",
-           "timing": "per call, CUDA events, L2 flushed before each call", "peak_hbm_gbs": hbm}
+           "timing": "per call, CUDA events, L2 flushed before each call; streamed: one graph "
+                     "over distinct weight copies spanning 4x L2, per call",
+           "peak_hbm_gbs": hbm}
     for i, m in enumerate(synth.CQ_MIXED):
         g = torch.Generator(device=dev)
         g.manual_seed(synth.weight_seed(2, i))
@@ -414,6 +419,17 @@ def mixed_report(dev, cb, torch, cq, synth, steps, warmup, hbm):
                 out[key + "_GBps"] = round(gbps, 1)
                 out[key + "_Gwps"] = round(m.N * m.K / (ms * 1e-3) / 1e9, 1)
                 out[key + "_frac"] = round(gbps / hbm, 4)
+                wbytes = packed.numel() + 2 * norms.numel()
+                copies = -(-4 * l2 // wbytes)
+                P = copies_of(torch, dev, packed, copies)
+                Q = copies_of(torch, dev, norms, copies)
+                ms_s = streamed_ms(torch, lambda: [cq.cq_gemv(P[c], Q[c], m.N, m.K, b, cb, Xq, sc, Y=Y,
+                                                             workspace=ws) for c in range(copies)]) / copies
+                gbps_s = nbytes / (ms_s * 1e-3) / 1e9
+                out[key + "_streamed_us"] = round(ms_s * 1e3, 2)
+                out[key + "_streamed_GBps"] = round(gbps_s, 1)
+                out[key + "_streamed_frac"] = round(gbps_s / hbm, 4)
+                del P, Q
             del packed, norms
         del W
         torch.cuda.empty_cache()
@@ -434,6 +450,42 @@ def _capture(torch, fn):
     return g
 
 
+def streamed_ms(torch, fn, reps=3):
+    """Device time of one replay of ``fn`` captured as a CUDA graph (after one untimed
+    replay), averaged over ``reps`` back-to-back replays."""
+    g = _capture(torch, fn)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def copies_of(torch, dev, t, n):
+    """``n`` copies of ``t`` in one buffer, each starting at a 256-byte boundary (distinct
+    memory, so that streaming them reads every copy from HBM)."""
+    per = t.numel() * t.element_size()
+    stride = -(-per // 256) * 256
+    flat = torch.empty((n * stride,), dtype=torch.uint8, device=dev)
+    src = t.contiguous().view(torch.uint8).reshape(-1)
+    views = []
+    for c in range(n):
+        v = flat[c * stride:c * stride + per]
+        v.copy_(src)
+        views.append(v.view(t.dtype).view(t.shape))
+    return views
+
+
+def l2_bytes(torch, dev):
+    props = torch.cuda.get_device_properties(dev)
+    return int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+
+
 def small_report(dev, cb, torch, cq, synth, steps, warmup):
     """Configs 1 and 2, each reported twice as SURVEY-style measurements ask: the latency
     of one call, replayed as a CUDA graph after an L2 flush, and the streamed throughput
@@ -442,38 +494,17 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
     quantization, rotation and GEMV in one launch; ``q4_0_gemv_layer``: every matrix of the
     layer in one launch); the per-matrix launches of the unfused path are timed beside
     them (``unfused_latency_us``)."""
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    l2 = l2_bytes(torch, dev)
     flush = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
 
     def latency(fn):
         return flushed_call_ms(torch, flush, _capture(torch, fn).replay, steps, warmup)
 
     def streamed(fn, reps=3):
-        g = _capture(torch, fn)
-        g.replay()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
+        return streamed_ms(torch, fn, reps)
 
-    def copies_of(t, n):
-        """``n`` copies of ``t`` in one buffer, each starting at a 256-byte boundary."""
-        per = t.numel() * t.element_size()
-        stride = -(-per // 256) * 256
-        flat = torch.empty((n * stride,), dtype=torch.uint8, device=dev)
-        src = t.contiguous().view(torch.uint8).reshape(-1)
-        views = []
-        for c in range(n):
-            v = flat[c * stride:c * stride + per]
-            v.copy_(src)
-            views.append(v.view(t.dtype).view(t.shape))
-        return views
+    def copies_of_(t, n):
+        return copies_of(torch, dev, t, n)
 
     def gen(shape, seed):
         g = torch.Generator(device=dev)
@@ -507,8 +538,8 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
 
     us_unfused = latency(unfused) * 1e3
     copies = -(-4 * l2 // nbytes)
-    P = copies_of(packed, copies)
-    Q = copies_of(norms, copies)
+    P = copies_of_(packed, copies)
+    Q = copies_of_(norms, copies)
     calls = [cq.make_gemv_layer([(P[c], Q[c], N, K, X, Y)]) for c in range(copies)]
     ms = streamed(lambda: [cq.cq_gemv_layer(c1, 4, cb) for c1 in calls])
     per = cq.LAYER_MAX_PROBLEMS
@@ -542,7 +573,7 @@ def small_report(dev, cb, torch, cq, synth, steps, warmup):
 
     us_unfused = latency(one_layer) * 1e3
     copies = -(-4 * l2 // lbytes)
-    reps = [(m, copies_of(b, copies), y) for m, b, y in layer]
+    reps = [(m, copies_of_(b, copies), y) for m, b, y in layer]
     lcalls = [cq.make_q4_0_layer([(b[c], m.N, m.K, xs[m.K], y) for m, b, y in reps]) for c in range(copies)]
     ms = streamed(lambda: [cq.q4_0_gemv_layer(c1) for c1 in lcalls])
     out["minueza_q4_0_layer"] = {"latency_us": round(us, 1), "unfused_latency_us": round(us_unfused, 1),
@@ -654,6 +685,11 @@ def gpu_arm(args, rank, world, local_rank):
         return
     if args.small_only:
         print(json.dumps(small_report(dev, cb, torch, cq, synth, 10, args.warmup)), flush=True)
+        return
+    if args.mixed_only:
+        peaks, _ = load_peaks()
+        print(json.dumps(mixed_report(dev, cb, torch, cq, synth, 10, args.warmup,
+                                      float(peaks["hbm_gbs"]))), flush=True)
         return
     if args.prefill_only:
         pf = build_prefill(dev, cb, torch, cq, synth, args.prefill_m)
@@ -1063,6 +1099,8 @@ def main(argv=None):
                     help="skip the small-workload report (CQ 512x512, one Minueza Q4_0 layer)")
     ap.add_argument("--no-narrow", action="store_true",
                     help="skip the 1-bit / 2-bit / ternary decode report (cq_gemv vs cq_gemv_lut)")
+    ap.add_argument("--mixed-only", action="store_true",
+                    help="print only the mixed-width CQ report (config 3)")
     ap.add_argument("--small-only", action="store_true",
                     help="print only the small-workload report (profiling runs)")
     ap.add_argument("--narrow-codes", nargs="*", default=None, choices=["b1", "b2", "ternary"],

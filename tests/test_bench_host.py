@@ -250,7 +250,14 @@ def test_batched_report_batch_two_uses_the_gemvs():
     assert "q4_0_gemm" not in lib.calls and lib.calls["q4_0_gemv"] == 4 * (1 + 2)
 
 
-def test_mixed_report_covers_every_width_shape_and_batch():
+def test_mixed_report_covers_every_width_shape_and_batch(monkeypatch):
+    def capture(torch_, fn):
+        g = _Graph()
+        g.fn = fn
+        fn()
+        return g
+
+    monkeypatch.setattr(bench, "_capture", capture)
     lib = _FakeLib()
     small = tuple(types.SimpleNamespace(name=m.name, N=m.N // 64, K=m.K // 8) for m in synth.CQ_MIXED)
     fs = types.SimpleNamespace(CQ_MIXED=small, CQ_MIXED_BITS=synth.CQ_MIXED_BITS,
@@ -260,12 +267,19 @@ def test_mixed_report_covers_every_width_shape_and_batch():
     ft.rand = torch.rand
     ft.where = torch.where
     out = bench.mixed_report("cpu", None, ft, lib, fs, 2, 3, 1e-3)
+    l2 = 4 << 20                                   # the fake device's L2
+    calls = 0
     for m in small:
         for b in (1, 2, 3, 4):
+            wbytes = m.N * (m.K // 128) * 16 * cqlib.cq_field_bits(b) + 2 * m.N * (m.K // 128)
+            copies = -(-4 * l2 // wbytes)          # distinct copies spanning 4x the L2
             for B in (1, 4, 16):
                 k = f"{m.name}_b{b}_B{B}"
                 assert out[k + "_us"] > 0 and out[k + "_frac"] > 0 and out[k + "_Gwps"] > 0
-    assert lib.calls["cq_gemv"] == 2 * 4 * 3 * (3 + 2)
+                assert out[k + "_streamed_us"] > 0 and out[k + "_streamed_frac"] > 0
+                # flushed: warmup + steps; streamed: capture + 1 + 3 replays of every copy
+                calls += (3 + 2) + (1 + 1 + 3) * copies
+    assert lib.calls["cq_gemv"] == calls
     json.dumps(out)
 
 
