@@ -154,7 +154,9 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  *   - B >= 3, N a multiple of 16 (any code): the tensor-core pipeline of cq_gemm with
  *     32-token tiles (4- and 2-bit rows reach shared memory per 64-index stage, 1- and
  *     3-bit rows per 128-index slab).  The weights are decoded once for all tokens; the operands are fp16
- *     (cb * norm, and xr * s_t / 128 in `workspace`), the accumulation fp32.  The
+ *     (4- and 2-bit rows: fp16(fp16(cb) * norm); 1- and 3-bit rows: fp16(cb * norm); and
+ *     xr * s_t / 128 in `workspace`), the accumulation fp32 (alternate 64-index stages of
+ *     a tile into two partial sums, added in a fixed order).  The
  *     relative error stays within 1e-3 of the exact product; activations must satisfy
  *     max |X[t][k]| <= 65504 (fp16 range).  When the row tiles are too few to occupy the
  *     GPU, K is split in two: Y is zeroed on `stream` and both halves add their fp32
