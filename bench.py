@@ -190,6 +190,26 @@ def build_workload(dev, cb, torch, cq, synth, only=None):
     return mats
 
 
+def twin_buffers(mats, torch):
+    """A second set of the step's device inputs and outputs (``xbuf``/``ybuf`` and their
+    per-matrix views at the same offsets), sharing the weights and scratch of ``mats``."""
+    xbuf = torch.empty_like(mats[0]["xbuf"]).copy_(mats[0]["xbuf"])
+    ybuf = torch.empty_like(mats[0]["ybuf"])
+    xo = yo = 0
+    out = []
+    for d in mats:
+        m = d["m"]
+        e = dict(d)
+        e["X"] = xbuf[xo:xo + m.K].view(1, m.K)
+        e["Ycq"] = ybuf[yo:yo + m.N].view(1, m.N)
+        e["Yq4"] = ybuf[yo + m.N:yo + 2 * m.N].view(1, m.N)
+        e["xbuf"], e["ybuf"] = xbuf, ybuf
+        xo += m.K
+        yo += 2 * m.N
+        out.append(e)
+    return out
+
+
 def step_bytes(mats):
     cq_b = sum(d["packed"].numel() + 2 * d["norms"].numel() + d["m"].K + 4 + 4 * d["m"].N
                for d in mats)
@@ -765,28 +785,50 @@ def gpu_arm(args, rank, world, local_rank):
             dist.destroy_process_group()
         return
 
-    # end to end through the public API with host buffers: pinned H2D of the step's
-    # activations, the decode pass, D2H of the step's outputs
-    # (every matrix's activations in one buffer and its outputs in another: one copy each way)
-    xbuf, ybuf = mats[0]["xbuf"], mats[0]["ybuf"]
-    host_x = torch.empty(xbuf.shape, dtype=torch.float32, pin_memory=True).copy_(xbuf)
-    host_y = torch.empty(ybuf.shape, dtype=torch.float32, pin_memory=True)
+    # end to end through the public API with host buffers: every step copies its
+    # activations from pinned host memory and reads its outputs back (every matrix's
+    # activations in one buffer and its outputs in another: one copy each way).  The
+    # copies run on a copy stream against two device sets of inputs and outputs, so
+    # step i's read-back and step i+1's upload overlap step i's and i+1's neighbours'
+    # compute; the timed region ends after the last read-back.
+    sets = [mats, twin_buffers(mats, torch)]
+    host_x = torch.empty(mats[0]["xbuf"].shape, dtype=torch.float32, pin_memory=True).copy_(mats[0]["xbuf"])
+    host_y = torch.empty(mats[0]["ybuf"].shape, dtype=torch.float32, pin_memory=True)
     h2d = host_x.numel() * 4
     d2h = host_y.numel() * 4
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        xbuf.copy_(host_x, non_blocking=True)
-        run_step(mats, cb, cq, kinds=kinds)
-        host_y.copy_(ybuf, non_blocking=True)
+    def e2e_run(n):
+        done = [None, None]     # per set: its last step's compute finished
+        up = [None, None]       # per set: its inputs uploaded
+        def upload(k):
+            with torch.cuda.stream(copy):
+                if done[k] is not None:
+                    copy.wait_event(done[k])   # the set's previous step no longer reads them
+                sets[k][0]["xbuf"].copy_(host_x, non_blocking=True)
+                up[k] = torch.cuda.Event()
+                up[k].record(copy)
+        upload(0)
+        for i in range(n):
+            k = i & 1
+            if i + 1 < n:
+                upload(k ^ 1)
+            comp.wait_event(up[k])
+            run_step(sets[k], cb, cq, kinds=kinds)
+            done[k] = torch.cuda.Event()
+            done[k].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done[k])
+                host_y.copy_(sets[k][0]["ybuf"], non_blocking=True)
+        comp.wait_stream(copy)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    e2e_run(max(2, args.warmup))
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     a = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     torch.cuda.synchronize()
     e2e_ms = reduce_max((time.perf_counter() - a) * 1e3 / args.steps, dist, dev)
 
