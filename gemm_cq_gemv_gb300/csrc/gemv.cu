@@ -655,8 +655,11 @@ __global__ void __launch_bounds__(kWarps2 * 32, 1) q4_0_gemv_ring_kernel(const _
             nx_base += gstep;
         }
     };
-    pdl_wait();
+    // the weight blocks are read before the wait for the previous kernel of the stream
+    // (weights come from kernels that release their dependents only at completion), the
+    // activations after it
     for (int64_t u = 0; u < kRing - 1 && u < U; ++u) issue((int)u);
+    pdl_wait();
     Q4X xq[SPW][TB];
     q4_load_x<TB, SPW>(p, slot, busy, lane, xq);
     __syncthreads();   // every warp set's reduction barriers initialised

@@ -234,7 +234,10 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
             nx_base += gstep;
         }
     };
-    pdl_wait();   // the weights and activations may come from the previous kernels
+    // The packed rows are read before the wait for the previous kernel of the stream:
+    // weights come from kernels that release their dependents only at completion (the
+    // library's encoders), so that wait concerns the activations alone, and the first
+    // copies' latency overlaps the previous kernel's tail.
     if (busy)
         for (int64_t u = 0; u < kFxRing - 1 && u < U; ++u) issue((int)u);
 
@@ -252,6 +255,7 @@ __global__ void __launch_bounds__(NW * 32, 1) cq4_gemv_fx_kernel(const __grid_co
         dst[0] = v4;
         dst[1] = v4;
     }
+    pdl_wait();   // the activations may come from the previous kernel
     // this lane's activations: int8 -> Hu q (exact integers) -> int16 pairs
     uint32_t xp[TB][16];
     if (p.share) {

@@ -22,6 +22,13 @@
  *    pointer after a call returns and allocates no device memory.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only enqueue
  *    work: they are asynchronous and do not synchronise.
+ *  - Kernels are launched with programmatic dependent launch: a kernel may start while
+ *    the one before it on the stream finishes, and waits for it before it reads that
+ *    kernel's outputs.  The batch-1 GEMVs start reading their packed weights before that
+ *    wait, so weights must be complete when the kernel launched just before the GEMV
+ *    starts: true for weights written by cq_encode or q4_0_quantize (neither releases
+ *    its dependents early), by a copy, or by any kernel that does not trigger dependent
+ *    launches itself.
  *  - Arguments are validated before anything is launched; a failed check returns an
  *    error status and launches nothing.
  *  - Row-major layouts; sizes are element counts unless named *_bytes.
