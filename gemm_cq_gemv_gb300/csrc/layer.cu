@@ -138,7 +138,10 @@ __global__ void __launch_bounds__(kLThreads) layer_gemv_kernel(const __grid_cons
             tab[i] = v;
         }
     }
-    pdl_wait();
+    // The weights are read before the wait for the previous kernel of the stream (they
+    // come from kernels that release their dependents only at completion): the first
+    // item's first chunk is requested, then the wait, then the activations.
+    bool waited = false;
     const int64_t it0 = (int64_t)blockIdx.x * p.items_per_cta;
     int64_t it1 = it0 + p.items_per_cta;
     if (it1 > p.items) it1 = p.items;
@@ -186,6 +189,10 @@ __global__ void __launch_bounds__(kLThreads) layer_gemv_kernel(const __grid_cons
         if (live) load_chunk(j, wv0, sh0, nb0);
         if (q != cur) {
             // prepare this problem's activations (the previous problem's are no longer read)
+            if (!waited) {
+                pdl_wait();
+                waited = true;
+            }
             __syncthreads();
             for (int t = 0; t < p.B; ++t) {
                 const float* x = pr.X + (int64_t)t * K;

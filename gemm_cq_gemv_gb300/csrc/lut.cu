@@ -174,12 +174,32 @@ __global__ void __launch_bounds__(kLutThreads, 1) cq_gemv_lut_kernel(const __gri
     float lv[1 << F];
 #pragma unroll
     for (int u = 0; u < (1 << F); ++u) lv[u] = p.lv[u];
-    pdl_wait();   // the activations (and weights) may come from the previous kernels
-    const float yscale = p.scale[p.t] * (1.0f / 128.0f);
-
     const int64_t ncta = p.groups_base + ((int)blockIdx.x < p.groups_extra ? 1 : 0);
     const int64_t gstride = (int64_t)kLutWarps * gridDim.x;   // this warp's next group, in groups
     int64_t u_glob = 0;   // units this warp has consumed (its ring's slot and phase)
+    // unit u of a range starting at word rw0, for the warp's groups from global group g0
+    auto issue_at = [&](int64_t g0, int rw0, int u) {
+        if (lane == 0) {
+            const int d = (int)((u_glob + u) & (kLutRing - 1));
+            const int64_t row = (g0 + (int64_t)(u >> 2) * gstride) * kRows + (u & 3) * kLutUnitRows;
+            mbar_arrive_tx(&rfull[d], kLutUnitBytes);
+            tma_box(ring + d * kLutUnitBytes, &p.pmap, rw0, (int)row, &rfull[d]);
+        }
+    };
+    auto warp_units = [&](int64_t mb) {   // this warp's units per range in the block at mb
+        const int nbg = (int)(ncta - mb < kBlockGroups ? ncta - mb : kBlockGroups);
+        const int ngw = nbg > w ? (nbg - w + kLutWarps - 1) / kLutWarps : 0;
+        return ngw * (kRows / kLutUnitRows);
+    };
+    // The packed rows are read before the wait for the previous kernel of the stream
+    // (weights come from kernels that release their dependents only at completion): the
+    // first range's first copies go out here, the activations are read after the wait.
+    {
+        const int nu0 = ncta > 0 ? warp_units(0) : 0;
+        for (int u = 0; u < kLutRing - 1 && u < nu0; ++u) issue_at(blockIdx.x + (int64_t)w * gridDim.x, 0, u);
+    }
+    pdl_wait();   // the activations may come from the previous kernel
+    const float yscale = p.scale[p.t] * (1.0f / 128.0f);
     bool built = false;
     // this warp's int8 activations of a range (its groups w and w + 16), loaded one range
     // ahead so a table rebuild does not wait for them
@@ -207,18 +227,14 @@ __global__ void __launch_bounds__(kLutThreads, 1) cq_gemv_lut_kernel(const __gri
             const int rw0 = r * kRangeWords;
             const int nw = p.words - rw0 < kRangeWords ? p.words - rw0 : kRangeWords;
             const int nunits = ngw * (kRows / kLutUnitRows);
-            auto issue = [&](int u) {
-                if (lane == 0) {
-                    const int d = (int)((u_glob + u) & (kLutRing - 1));
-                    const int64_t row = (g0 + (int64_t)(u >> 2) * gstride) * kRows + (u & 3) * kLutUnitRows;
-                    mbar_arrive_tx(&rfull[d], kLutUnitBytes);
-                    tma_box(ring + d * kLutUnitBytes, &p.pmap, rw0, (int)row, &rfull[d]);
-                }
-            };
-            // the first copies of the range go out before its table is built
-            __syncwarp();
-            if (lane == 0) fence_proxy_async();   // earlier reads of the slots are done
-            for (int u = 0; u < kLutRing - 1 && u < nunits; ++u) issue(u);
+            auto issue = [&](int u) { issue_at(g0, rw0, u); };
+            // the first copies of the range go out before its table is built (those of the
+            // first range of the first block before the dependent-launch wait)
+            if (mb > 0 || r > 0) {
+                __syncwarp();
+                if (lane == 0) fence_proxy_async();   // earlier reads of the slots are done
+                for (int u = 0; u < kLutRing - 1 && u < nunits; ++u) issue(u);
+            }
             if (!(built && p.nranges == 1)) {
                 __syncthreads();   // every warp is done with the previous table
                 // (1) xr = Hu @ q for the range's groups, one warp per group: lane l holds
