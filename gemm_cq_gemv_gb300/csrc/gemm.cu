@@ -58,7 +58,9 @@ namespace {
 
 constexpr int kBO = 128;                 // out-rows per tile (MMA M, TMEM lanes)
 constexpr int kBK = 64;                  // K per stage (128 bytes of 16-bit operands)
+constexpr int kEpiWarps = 8;             // two per TMEM lane quarter
 constexpr int kDequantWarps = 8;         // per stage: two per TMEM lane quarter
+constexpr int kDequantGroups = 2;        // the first eight dequant warps take even stages
 constexpr int kTmemCols = 512;
 constexpr int kACols = kBK / 2;                       // 32 TMEM columns per A stage
 constexpr int kGemmSmem = 227 * 1024;    // table (64 KB, 64 KB aligned) + stages + barriers
@@ -79,8 +81,7 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //   BT      tokens per tile (MMA N)
 //   F16     fp16 operands and fp32 output (the batched-decode form of the product);
 //           otherwise bf16 operands and bf16 output (prefill)
-//   STAGES  depth of the tensor-memory A ring (and of the shared-memory ring unless
-//           SSTAGES is given)
+//   STAGES  depth of the shared-memory ring (= tensor-memory A stages)
 //   FMT     weight format: CQ (packed indices + norms) or Q4_0 blocks
 //   SLABS   Q4_0 and 1-/3-bit CQ: depth of the weight-slab ring
 //   TLIST   look the CTA's tiles up once, into shared memory (grouped launches of many
@@ -88,17 +89,11 @@ enum WeightFormat { kFmtCQ = 0, kFmtQ40 = 1 };
 //   BITS    CQ index width: 4 or 2 (the packed tile rides in the stage, 32 or 16 bytes
 //           per row), 1 or 3 (slabs of two stages)
 //   PF16    fp16 codeword pairs and fp16 operands with bf16 output (prefill)
-//   SSTAGES depth of the shared-memory ring when deeper than the A ring: a stage's copy
-//           is then issued SSTAGES stages ahead of its MMA, while its dequant still
-//           waits for the MMA that last read its A slot, STAGES stages back
 //   MMAW    MMA issuer threads, each with a partial accumulator per buffer
-//   DGROUPS dequant groups of eight warps, taking stages in turn
-//   EPIW    epilogue warps (a multiple of 4: one set per TMEM lane quarter)
 //   PROD    copy-issuing threads: 1, or 2 (one for the activation tiles, one for the
 //           packed weight tiles or slabs)
 template <int BT_, bool F16_, int STAGES_, int FMT_ = kFmtCQ, int SLABS_ = 0, bool TLIST_ = false,
-          int BITS_ = 4, bool PF16_ = false, int SSTAGES_ = 0, int MMAW_ = 1, int DGROUPS_ = 2,
-          int EPIW_ = 8, int PROD_ = 1>
+          int BITS_ = 4, bool PF16_ = false, int MMAW_ = 1, int PROD_ = 1>
 struct GemmCfg {
     static constexpr int BT = BT_;
     static constexpr bool F16 = F16_;
@@ -112,7 +107,6 @@ struct GemmCfg {
     // fp16 operands whose packed indices ride in the stage (4 and 2 bits)
     static constexpr bool HPAIR = FMT_ == kFmtCQ && !CQSLAB && OPF16;
     static constexpr int STAGES = STAGES_;
-    static constexpr int SSTAGES = SSTAGES_ > 0 ? SSTAGES_ : STAGES_;
     static constexpr int FMT = FMT_;
     static constexpr int SLABS = SLABS_;
     static constexpr bool TLIST = TLIST_;
@@ -126,18 +120,15 @@ struct GemmCfg {
     static constexpr int MMAW = MMAW_;
     static constexpr int PROD = PROD_;
     static constexpr int EPI0 = PROD + MMAW;           // first epilogue warp
-    static constexpr int EPIW = EPIW_;
-    static constexpr int DGROUPS = DGROUPS_;
-    static constexpr int DEQ0 = EPI0 + EPIW;           // first dequant warp
-    static constexpr int THREADS = (DEQ0 + DGROUPS * kDequantWarps) * 32;
-    static_assert(EPIW % 4 == 0 && (BT / (EPIW / 4)) % 16 == 0, "epilogue warps: 16-column pieces");
+    static constexpr int DEQ0 = EPI0 + kEpiWarps;      // first dequant warp
+    static constexpr int THREADS = (DEQ0 + kDequantGroups * kDequantWarps) * 32;
+    static_assert((BT / (kEpiWarps / 4)) % 16 == 0, "epilogue warps: 16-column pieces");
     static_assert(THREADS <= 1024, "one CTA per SM");
     static_assert(PROD == 1 || PROD == 2, "one or two copy-issuing threads");
     static_assert(DCOL0 + 2 * MMAW * BT <= kTmemCols, "tensor memory budget");
     static_assert(MMAW == 1 || BT == 32, "several issuers: 32-token tiles");
     static_assert(STAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-    static_assert((2 * SSTAGES + STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
-    static_assert(SSTAGES >= STAGES, "the shared ring is at least as deep as the A ring");
+    static_assert((3 * STAGES + 4 + 2 * SLABS) * 8 + 16 + 64 <= kBarBytes, "barrier block");
     static_assert(FMT == kFmtCQ || (F16 && SLABS >= 2), "Q4_0 runs with fp16 operands on a slab ring");
     static_assert(BITS == 4 || (FMT == kFmtCQ && F16), "1- to 3-bit CQ rows: decode batches only");
     static_assert(!CQSLAB || SLABS >= 2, "1- and 3-bit CQ rows run on a slab ring");
@@ -147,12 +138,12 @@ struct GemmCfg {
 using PrefillCfg = GemmCfg<192, false, 4, kFmtCQ, 0, true, 4, true>;   // 24 KB activation tile, 28 KB stages
 constexpr int kDecodeIssuers = 2;
 constexpr int kDecodeProducers = 2;
-using DecodeCfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 4, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;   // 4 KB activation tile, 8 KB stages
-using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;  // 2-bit rows: 6 KB stages
-using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;  // 1-bit rows: 4 KB stages + 2 KB slabs
-using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;  // 3-bit rows: 4 KB stages + 6 KB slabs
+using DecodeCfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 4, false, kDecodeIssuers, kDecodeProducers>;   // 4 KB activation tile, 8 KB stages
+using Decode2Cfg = GemmCfg<32, true, 8, kFmtCQ, 0, false, 2, false, kDecodeIssuers, kDecodeProducers>;  // 2-bit rows: 6 KB stages
+using Decode1Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 1, false, kDecodeIssuers, kDecodeProducers>;  // 1-bit rows: 4 KB stages + 2 KB slabs
+using Decode3Cfg = GemmCfg<32, true, 8, kFmtCQ, 4, false, 3, false, kDecodeIssuers, kDecodeProducers>;  // 3-bit rows: 4 KB stages + 6 KB slabs
 using Q40WideCfg = GemmCfg<192, true, 4, kFmtQ40, 4>;    // Q4_0, many tokens: 96 + 72 KB
-using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4, false, 4, false, 0, kDecodeIssuers, 2, 8, kDecodeProducers>;   // Q4_0, up to 32 tokens: 32 + 72 KB
+using Q40NarrowCfg = GemmCfg<32, true, 8, kFmtQ40, 4, false, 4, false, kDecodeIssuers, kDecodeProducers>;   // Q4_0, up to 32 tokens: 32 + 72 KB
 
 struct GemmProblem {
     CUtensorMap pmap;        // packed bytes as [N][K/2] uint8, box 32 x 128
@@ -476,8 +467,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr int kBT = C::BT;
-    constexpr int kStages = C::SSTAGES;    // shared-memory ring (copies)
-    constexpr int kAStages = C::STAGES;    // tensor-memory A ring (dequant -> MMA)
+    constexpr int kStages = C::STAGES;     // shared-memory ring = tensor-memory A ring
     constexpr int kXTileBytes = C::XTILE;
     constexpr int kStageBytes = C::STAGE;
     constexpr int kDCol0 = C::DCOL0;
@@ -488,8 +478,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
     constexpr int kFullAArrivals = (kProd == 2 && C::PTILE > 0) ? 2 : 1;
     constexpr int kEpiWarp0 = C::EPI0;
     constexpr int kDequantWarp0 = C::DEQ0;
-    constexpr int kEpiWarps = C::EPIW;
-    constexpr int kDequantGroups = C::DGROUPS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // CQ: the codeword-pair table sits at a 64 KB boundary of the shared window (the
     // address of entry e for lane l is then base | e << 8 | l << 3, one byte permute); the
@@ -522,10 +510,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
     // this CTA's tile list (problem, row tile, token tile, K half), after the barriers
     const uint32_t tiles_at = bars_at + (uint32_t)kBarBytes;
     const bool layout_ok = tiles_at + (C::TLIST ? (uint32_t)(kMaxCtaTiles * sizeof(TileRef)) : 0u) <= send;
-    uint64_t* full_a = bars;                      // [kStages] TMA: X tile + packed tile landed
-    uint64_t* empty = bars + kStages;             // [kStages] MMA: stage consumed
-    uint64_t* full_b = bars + 2 * kStages;        // [kAStages] dequant: A stage written to TMEM
-    uint64_t* acc_full = full_b + kAStages;       // [2] accumulator buffer ready
+    uint64_t* full_a = bars;                      // TMA: X tile + packed tile landed
+    uint64_t* empty = bars + kStages;             // MMA: stage consumed
+    uint64_t* full_b = bars + 2 * kStages;        // dequant: A stage written to TMEM
+    uint64_t* acc_full = bars + 3 * kStages;      // [2] accumulator buffer ready
     uint64_t* acc_empty = acc_full + 2;           // [2] accumulator buffer drained
     uint64_t* slab_full = acc_empty + 2;          // [SLABS] weight slab landed
     uint64_t* slab_empty = slab_full + C::SLABS;  // [SLABS] slab read by the dequant of its stages
@@ -572,8 +560,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full_a[s], kFullAArrivals);
             mbar_init(&empty[s], 1);
+            mbar_init(&full_b[s], kDequantWarps);
         }
-        for (int s = 0; s < kAStages; ++s) mbar_init(&full_b[s], kDequantWarps);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], kMmaW);   // one commit per issuer
             mbar_init(&acc_empty[b], kEpiWarps);
@@ -722,7 +710,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                     if (s == nA) blo = lo_above;
                     if (s == kStages) { s = 0; blo = lo_first; }
                     aaddr += (uint32_t)kACols;
-                    if (++sa == kAStages) { sa = 0; pha ^= 1u; aaddr = tmem_base; }
+                    if (++sa == kStages) { sa = 0; pha ^= 1u; aaddr = tmem_base; }
                 }
                 if (!ok) break;
                 umma_commit(&acc_full[buf]);
@@ -833,22 +821,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                 if (gi % kDequantGroups != grp) continue;   // the other group's stage
                 const int s = gi % kStages;
                 const uint32_t ph = (uint32_t)((gi / kStages) & 1);
-                const int sa = gi % kAStages;
-                // with a deeper shared ring the landed copy no longer implies that the MMA
-                // of stage gi - kAStages (the last reader of A slot sa) has completed: wait
-                // for its commit.  After the full_a wait every commit up to stage
-                // gi - kStages has completed, and the next commit on that barrier needs this
-                // stage's MMA, so the parity names exactly that commit.
-                auto a_slot_free = [&]() {
-                    if constexpr (kStages == kAStages) return true;
-                    if (gi < kAStages) return true;
-                    const int g4 = gi - kAStages;
-                    return mbar_wait(&empty[g4 % kStages], (uint32_t)((g4 / kStages) & 1), abort_flag, p);
-                };
+                const int sa = s;   // the A stage in tensor memory (the copy of the same stage
+                                    // landing implies its previous MMA has completed)
                 if constexpr (C::FMT == kFmtQ40) {
                     // the full_a wait frees the A stage (its previous MMA has completed)
                     // and, through full_b, orders the activation tile for the MMA
-                    if (!mbar_wait(&full_a[s], ph, abort_flag, p) || !a_slot_free()) { ok = false; break; }
+                    if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
                     const int sg = gi / C::SPS;   // every K is a whole number of slabs
                     const int qs = sg % C::SLABS;
                     if (!mbar_wait(&slab_full[qs], (uint32_t)((sg / C::SLABS) & 1), abort_flag, p)) {
@@ -915,7 +893,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) cq_gemm_kernel(const __grid_con
                 } else {
                     nb = norm_bits(pr, orow, kc);
                 }
-                if (!mbar_wait(&full_a[s], ph, abort_flag, p) || !a_slot_free()) { ok = false; break; }
+                if (!mbar_wait(&full_a[s], ph, abort_flag, p)) { ok = false; break; }
                 if constexpr (C::CQSLAB) {
                     const int sg = gi / C::SPS;   // every K is a whole number of slabs
                     const int qs = sg % C::SLABS;
