@@ -13,13 +13,13 @@ each launch).  ``value`` is algorithmic GB/s: packed indices +
 norms (CQ) or Q4_0 blocks, plus activations and outputs, divided by the step time.
 
 The line also reports every other workload of the path:
-  * ``prefill`` (config 4): the grouped prefill GEMM of the 20-layer model, TFLOP/s and the
+  * ``prefill``: the grouped prefill GEMM of the 20-layer model, TFLOP/s and the
     fraction of the bf16 peak as flat keys per M;
-  * ``batched`` (config 5 at batches 2, 8, 32): ``cq_gemv`` at 4 bits, ``q4_0_gemv`` (B = 2)
+  * ``batched`` (the large-shape decode at batches 2, 8, 32): ``cq_gemv`` at 4 bits, ``q4_0_gemv`` (B = 2)
     and ``q4_0_gemm`` (B >= 8), GB/s, each call timed alone after an L2 flush;
-  * ``mixed`` (config 3): ``cq_gemv`` at b = 1..4 on [4096, 4096] and [11008, 4096] with
+  * ``mixed``: ``cq_gemv`` at b = 1..4 on [4096, 4096] and [11008, 4096] with
     outliers, batches 1 / 4 / 16;
-  * ``small`` (configs 1 and 2): CQ-W4A8 512 x 512 and one Minueza Q4_0 layer, each as
+  * ``small``: CQ-W4A8 512 x 512 and one Minueza Q4_0 layer, each as
     single-call latency and as streamed GB/s over weight copies spanning 4x the L2;
   * ``narrow``: batch-1 decode of 1-bit, 2-bit and ternary rows through ``cq_gemv`` and the
     table-lookup ``cq_gemv_lut`` (timed in a child process after everything else);
@@ -304,7 +304,7 @@ def time_prefill(pf, cb, cq, torch, steps, warmup):
 
 
 def prefill_report(dev, cb, torch, cq, synth, steps, warmup, peaks, kind):
-    """Config 4: the grouped prefill GEMM of the 20-layer model at each M, as flat scalar
+    """The grouped prefill GEMM of the 20-layer model at each M, as flat scalar
     keys (``M512_tflops``, ``M512_frac``, ...) so that every number sits one level deep."""
     peak = float(peaks["bf16_tflops"])
     out = {"workload": "20-layer 45M-parameter model (q,o 512x512; k,v 128x512; up 1536x512; "
@@ -346,7 +346,7 @@ def flushed_call_ms(torch, flush, fn, steps, warmup):
 
 def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(2, 8, 32),
                    kinds=("cq", "q4_0"), hbm=None):
-    """Config 5 at batches above 1: ``cq_gemv`` at 4 bits (B >= 3 takes the tcgen05 path, B = 2
+    """The large-shape decode at batches above 1: ``cq_gemv`` at 4 bits (B >= 3 takes the tcgen05 path, B = 2
     one two-token CUDA-core pass) and, for Q4_0, ``q4_0_gemv`` at B = 2 and ``q4_0_gemm`` on
     the tensor cores at larger batches; per large matrix, each call timed alone with CUDA
     events after an L2 flush (the [8192, 8192] weights would otherwise stay in the 129 MB L2).
@@ -404,7 +404,7 @@ def batched_report(mats, cb, torch, cq, synth, dev, steps, warmup, batches=(2, 8
 
 
 def mixed_report(dev, cb, torch, cq, synth, steps, warmup, hbm):
-    """Config 3: CQ at every width b = 1..4 on [4096, 4096] and [11008, 4096] (weights with
+    """The mixed-width sweep: CQ at every width b = 1..4 on [4096, 4096] and [11008, 4096] (weights with
     1 % x10 outliers), batches 1 / 4 / 16, each measured twice: one ``cq_gemv`` call timed
     alone after an L2 flush (``<matrix>_b<b>_B<B>_{us,GBps,Gwps,frac}``), and streamed:
     one CUDA graph of back-to-back calls over distinct copies of the weights spanning 4x
@@ -507,7 +507,7 @@ def l2_bytes(torch, dev):
 
 
 def small_report(dev, cb, torch, cq, synth, steps, warmup):
-    """Configs 1 and 2, each reported twice as SURVEY-style measurements ask: the latency
+    """The CQ 512 x 512 call and the Minueza Q4_0 layer, each reported twice: the latency
     of one call, replayed as a CUDA graph after an L2 flush, and the streamed throughput
     of back-to-back calls over distinct copies of the weights spanning 4x the L2 (one
     graph of all copies).  The calls are the fused decode chain (``cq_gemv_layer``: int8
@@ -912,12 +912,14 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 def summary_of(line, hbm):
-    """Every workload's headline numbers as flat scalar keys: c1/c2 the small workloads
-    (latency, streamed GB/s and its fraction of HBM), c3 the mixed-width sweep's fractions,
-    c4 the prefill GEMM, c5 the large-shape decode at each batch, plus the oracle check."""
+    """Every workload's headline numbers as flat scalar keys, each named by its workload:
+    ``cq512_*`` and ``minueza_q4_0_layer_*`` the small workloads (latency, streamed GB/s
+    and its fraction of HBM), ``mixed_*`` the mixed-width sweep's fractions, ``prefill_*``
+    the prefill GEMM, ``decode_B<B>_*`` the large-shape decode at each batch, plus the
+    oracle check."""
     out = {}
     sm = line.get("small") or {}
-    for key, name in (("c1", "cq_w4a8_512x512"), ("c2", "minueza_q4_0_layer")):
+    for key, name in (("cq512", "cq_w4a8_512x512"), ("minueza_q4_0_layer", "minueza_q4_0_layer")):
         r = sm.get(name)
         if isinstance(r, dict):
             out[f"{key}_latency_us"] = r.get("latency_us")
@@ -927,21 +929,21 @@ def summary_of(line, hbm):
     mx = line.get("mixed") or {}
     for k, v in mx.items():
         if k.endswith("_frac"):
-            out["c3_" + k] = v
+            out["mixed_" + k] = v
     pf = line.get("prefill") or {}
     for k in ("M512_tflops", "M512_frac", "M2048_tflops", "M2048_frac"):
         if k in pf:
-            out["c4_" + k] = pf[k]
+            out["prefill_" + k] = pf[k]
     for k, v in (line.get("kernels") or {}).items():
-        out[f"c5_B1_{k}_GBps"] = v.get("GBps")
+        out[f"decode_B1_{k}_GBps"] = v.get("GBps")
         if v.get("GBps"):
-            out[f"c5_B1_{k}_frac"] = round(v["GBps"] / hbm, 4)
+            out[f"decode_B1_{k}_frac"] = round(v["GBps"] / hbm, 4)
     for bk, rep in (line.get("batched") or {}).items():
         if bk.startswith("B") and isinstance(rep, dict):
             for kern, v in rep.items():
                 if isinstance(v, dict) and "GBps" in v:
-                    out[f"c5_{bk}_{kern}_GBps"] = v["GBps"]
-                    out[f"c5_{bk}_{kern}_frac"] = round(v["GBps"] / hbm, 4)
+                    out[f"decode_{bk}_{kern}_GBps"] = v["GBps"]
+                    out[f"decode_{bk}_{kern}_frac"] = round(v["GBps"] / hbm, 4)
     par = (line.get("cpu_baseline") or {}).get("parity")
     if par:
         out["oracle_check_ok"] = par["ok"]
@@ -1133,7 +1135,7 @@ def main(argv=None):
                     help="time only the grouped prefill GEMM (profiling runs)")
     ap.add_argument("--prefill-m", type=int, default=2048)
     ap.add_argument("--no-batched", action="store_true", help="skip the decode-batch report")
-    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-width CQ sweep (config 3)")
+    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed-width CQ sweep")
     ap.add_argument("--batched-only", action="store_true",
                     help="time only the tensor-core decode batch of --batch tokens (profiling runs)")
     ap.add_argument("--batch", type=int, default=32)
@@ -1142,7 +1144,7 @@ def main(argv=None):
     ap.add_argument("--no-narrow", action="store_true",
                     help="skip the 1-bit / 2-bit / ternary decode report (cq_gemv vs cq_gemv_lut)")
     ap.add_argument("--mixed-only", action="store_true",
-                    help="print only the mixed-width CQ report (config 3)")
+                    help="print only the mixed-width CQ report")
     ap.add_argument("--small-only", action="store_true",
                     help="print only the small-workload report (profiling runs)")
     ap.add_argument("--narrow-codes", nargs="*", default=None, choices=["b1", "b2", "ternary"],

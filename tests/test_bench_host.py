@@ -294,10 +294,10 @@ def test_summary_flattens_every_workload():
             "cpu_baseline": {"parity": {"ok": True, "cq_gemv_max_rel_err": 1e-7,
                                         "q4_0_gemv_max_rel_err": 2e-6}}}
     s = bench.summary_of(line, 1000.0)
-    assert s["c1_streamed_frac"] == 0.1 and s["c2_latency_us"] == 20.0
-    assert s["c3_sq_b4_B1_frac"] == 0.5 and "c3_sq_b4_B1_us" not in s
-    assert s["c4_M2048_frac"] == 0.52 and s["c5_B1_cq_gemv_frac"] == 0.5
-    assert s["c5_B2_cq_gemv_frac"] == 0.4 and s["oracle_check_ok"] is True
+    assert s["cq512_streamed_frac"] == 0.1 and s["minueza_q4_0_layer_latency_us"] == 20.0
+    assert s["mixed_sq_b4_B1_frac"] == 0.5 and "mixed_sq_b4_B1_us" not in s
+    assert s["prefill_M2048_frac"] == 0.52 and s["decode_B1_cq_gemv_frac"] == 0.5
+    assert s["decode_B2_cq_gemv_frac"] == 0.4 and s["oracle_check_ok"] is True
     assert all(not isinstance(v, dict) for v in s.values())
 
 
