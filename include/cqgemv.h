@@ -165,7 +165,8 @@ cq_status a8_fake_quant_groups(const float* X, int64_t T, int64_t D, int G, floa
  *     xr * s_t / 128 in `workspace`), the accumulation fp32 (alternate 64-index stages of
  *     a tile into two partial sums, added in a fixed order).  The
  *     relative error stays within 1e-3 of the exact product; activations must satisfy
- *     max |X[t][k]| <= 65504 (fp16 range).  When the row tiles are too few to occupy the
+ *     max |X[t][k]| <= 65504 (fp16 range), and so must every group's norm times its
+ *     largest codeword magnitude.  When the row tiles are too few to occupy the
  *     GPU, K is split in two: Y is zeroed on `stream` and both halves add their fp32
  *     partials into it (two addends on zero: the same sum in either order).
  *   packed, norms  as written by cq_encode (b = 1..4, or CQ_TERNARY: its 2-bit fields
